@@ -1,0 +1,340 @@
+#!/usr/bin/env python
+"""Benchmark of the ring-attention fold hot path on GB300.
+
+One step = one ra_forward over the N = 131072, d = 128, H = 8, P = 32 bf16
+workload: every query block folds all 32 visiting K/V blocks in ring order
+and writes out and lse.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W]      # this library
+  python bench.py --impl reference [--steps K] [--warmup W] # the fp64 CPU oracle
+
+Several GPUs (torchrun) run independent replicas of the same workload (the
+virtual ring lives on one GPU; there is no exchange between ranks).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "attention TFLOP/s (4·B·H·N²·d) at 1 GB300 and % of dense bf16 tensor peak"
+UNIT = "TFLOP/s"
+KERNEL_SOURCES = ["long_context_ra_gb300/csrc/ra_fold_sm103.cu",
+                  "long_context_ra_gb300/csrc/sm103_ptx.cuh"]
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update((ROOT / f).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {"bf16": d["bf16_tflops"], "bf16_sustained": d.get("bf16_tflops_sustained"),
+                "hbm": d["hbm_gbs"], "source": "measured"}
+    return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel as it is now (same source hash) and the same workload."""
+    for f in sorted((ROOT / "profiles").glob("*.md")):
+        text = f.read_text()
+        m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+        m_wl = re.search(r"bench_workload:\s*(\S+)", text)
+        m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+        if m_sha and m_b and m_wl and m_sha.group(1) == kernel_sha() and m_wl.group(1) == workload:
+            return float(m_b.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str | None):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if gpu_id:
+            cmd.insert(1, f"--id={gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.4)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.tmp.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.tmp.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def cpu_oracle_baseline(w, q, k, v, target_s: float):
+    """Time the fp64 oracle (as it stands) on a bounded, seeded sample of the
+    workload's query rows on all host cores; scale to TFLOP/s."""
+    import numpy as np
+    import torch
+
+    from oracle import ra_oracle
+
+    O = ra_oracle.get()
+    bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).cpu().view(torch.int16).numpy().view(np.uint16)
+    qa, ka, va = bits(q), bits(k), bits(v)
+    g = np.random.default_rng(99)
+    pool = np.sort(g.choice(w.rows, size=min(w.rows, 65536), replace=False))
+    per_row = 4.0 * w.N * w.d
+    probe = pool[:: max(1, len(pool) // 16)][:16]
+    t0 = time.perf_counter()
+    O.ring(qa, ka, va, w.P, dtype="bf16", rows=probe)
+    t_probe = time.perf_counter() - t0
+    n = int(min(len(pool), max(16, len(probe) * target_s / max(t_probe, 1e-6))))
+    rows = pool[np.linspace(0, len(pool) - 1, n).astype(np.int64)]
+    t0 = time.perf_counter()
+    O.ring(qa, ka, va, w.P, dtype="bf16", rows=rows)
+    dt = time.perf_counter() - t0
+    return {"value": n * per_row / dt / 1e12, "unit": UNIT, "cores": O.threads, "kind": "oracle",
+            "sample": f"{n} seeded query rows of {w.name} (ring recurrence, fp64), {dt:.1f} s; "
+                      f"value = rows x 4*N*d flops / time"}, n, dt
+
+
+def run_reference(args, w) -> None:
+    """The CPU oracle as the reference arm, on this arm's workload and metric."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    from long_context_ra_gb300 import synth
+    from oracle import ra_oracle
+
+    O = ra_oracle.get()
+    q, k, v = synth.make_inputs(w, "cpu")
+    bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).view(torch.int16).numpy().view(np.uint16)
+    qa, ka, va = bits(q), bits(k), bits(v)
+    per_row = 4.0 * w.N * w.d
+    g = np.random.default_rng(7)
+    probe = np.sort(g.choice(w.rows, size=8, replace=False))
+    t0 = time.perf_counter()
+    O.ring(qa, ka, va, w.P, dtype="bf16", rows=probe)
+    t_probe = (time.perf_counter() - t0) / len(probe)
+    budget = 120.0 / max(1, args.steps + args.warmup)  # whole run within ~2 minutes
+    n = int(max(4, min(4096, budget / max(t_probe, 1e-6))))
+    times = []
+    for s in range(args.warmup + args.steps):
+        rows = np.sort(g.choice(w.rows, size=n, replace=False))
+        t0 = time.perf_counter()
+        O.ring(qa, ka, va, w.P, dtype="bf16", rows=rows)
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    t_step = sum(times) / len(times)
+    value = n * per_row / t_step / 1e12
+    sample = f"{n} seeded query rows of {w.name} per step (fp64 ring recurrence)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {**w.describe(), "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_ours(args, w) -> None:
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    if rank == 0:
+        from long_context_ra_gb300.build import build
+        build()
+    barrier()
+    import long_context_ra_gb300 as ra
+    from long_context_ra_gb300 import synth
+
+    q, k, v = synth.make_inputs(w, dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ra.ra_forward(q, k, v, w.P, out=out, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ra.ra_last_device_status() != 0:
+        raise RuntimeError("kernel watchdog fired during warm-up")
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    sampler = ClockSampler(gpu_id)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if ra.ra_last_device_status() != 0:
+        raise RuntimeError("kernel watchdog fired in the timed region")
+    t = torch.tensor([ms], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    value = world * w.flops / (ms_max * 1e-3) / 1e12
+
+    # end to end through the C ABI: pinned host inputs -> device, forward,
+    # out and lse back to pinned host memory, every step
+    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(1, min(args.steps, 5))
+    barrier()
+    w0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = (time.perf_counter() - w0) / n_e2e
+    ms_e2e = max(e0.elapsed_time(e1) / n_e2e, wall * 1e3)
+    te = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = world * w.flops / (float(te.item()) * 1e-3) / 1e12
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+
+    peaks = load_peaks()
+    achieved = w.flops / (ms * 1e-3) / 1e12  # one fold launch per step
+    traffic = profiled_traffic(w.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": UNIT,
+                "frac": achieved / peaks["bf16"], "traffic": traffic,
+                "kernel": "fold_sm103_kernel<128>",
+                "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
+                if peaks["source"] == "measured" else "fallback 1.9 PFLOP/s bf16 burst",
+                "frac_of_sustained": achieved / peaks["bf16_sustained"]
+                if peaks.get("bf16_sustained") else None}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu, _, _ = cpu_oracle_baseline(w, q, k, v, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {**w.describe(), "parallelism": "replicas",
+                       "l2": "inputs larger than L2 (q+k+v = "
+                             f"{3 * q.numel() * q.element_size() / 2**20:.0f} MiB)"},
+            "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": float(te.item())},
+            "gpu_launches": args.steps, "clocks": clocks,
+            "pct_of_peak": 100.0 * achieved / peaks["bf16"],
+            "exps_per_s": w.B * w.H * w.N * w.N / (ms * 1e-3),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=4, help="workload key (default 4)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    from long_context_ra_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

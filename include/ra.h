@@ -1,0 +1,195 @@
+/*
+ * ra.h -- C ABI of the GB300 (sm_103a) Ring Attention fold library.
+ *
+ * The library computes exact softmax attention the way Ring Attention does:
+ * the sequence of N tokens is cut into P contiguous blocks of c = N / P tokens
+ * ("Ring Attention: the math", section "Sharding the sequence"); query block i
+ * visits the K/V blocks in ring order j = (i - t) mod P for t = 0 .. P-1
+ * (section "The ring schedule: passing K/V around") and folds each visiting
+ * block into a running per-row state (m, l, o) (section "The online-softmax
+ * identity that makes streaming legal"):
+ *
+ *     s_j = tau * q . k_j,   tau = 1 / sqrt(d)
+ *     m'  = max(m, max_j s_j)
+ *     l'  = exp(m - m') * l + sum_j exp(s_j - m')
+ *     o'  = exp(m - m') * o + sum_j exp(s_j - m') * v_j
+ *
+ * and finishes with out = o / l (section "Accumulation math, step by step").
+ * lse = m + ln l is also returned (natural log, scaled scores).
+ *
+ * The ring is virtual: one GPU holds every block and the neighbour exchange of
+ * the pages becomes double-buffered on-chip staging.
+ *
+ * Conventions shared by every call
+ *   - All data pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates no device memory; it never frees caller memory.
+ *   - Tensors are dense and row-major.  Attention tensors use [B, H, N, d]
+ *     with d contiguous (the element at (b, h, n, e) is at ((b*H + h)*N + n)*d
+ *     + e).
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream).  A
+ *     returned RA_OK means the work was validated and enqueued.  Kernel
+ *     faults surface through the CUDA runtime as usual; a bounded-wait
+ *     watchdog inside the kernels is reported by ra_last_device_status().
+ *   - Arguments are validated before anything is enqueued; on any error the
+ *     call returns the status and launches nothing.  No call throws.
+ *   - Calls whose total row count is zero return RA_OK and launch nothing.
+ *   - Element types: RA_BF16 inputs run on the tensor cores (tcgen05, fp32
+ *     accumulation) and need d in {64, 128}, c % 128 == 0 and 16-byte aligned
+ *     q, k, v and out.  RA_F32 inputs run on the fp32 FFMA path (no TF32) for
+ *     any 1 <= d <= 256 and any c >= 1; pointers must be 4-byte aligned.
+ *   - The device must be compute capability 10.3 (GB300); others give
+ *     RA_ERR_ARCH.
+ */
+#ifndef RA_H_
+#define RA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define RA_API __attribute__((visibility("default")))
+#else
+#define RA_API
+#endif
+
+/* cudaStream_t without including the CUDA headers (same type). */
+typedef struct CUstream_st* ra_stream_t;
+
+typedef enum ra_status {
+  RA_OK = 0,
+  RA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum          */
+  RA_ERR_UNSUPPORTED = 2, /* valid but not handled: P does not divide N, ... */
+  RA_ERR_MISALIGNED = 3,  /* pointer alignment below what the path needs    */
+  RA_ERR_ARCH = 4,        /* no CUDA device, or not compute capability 10.3  */
+  RA_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed               */
+  RA_ERR_TIMEOUT = 6      /* a kernel's bounded wait ran out (watchdog)      */
+} ra_status;
+
+typedef enum ra_dtype { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
+
+/* Largest number of partial states ra_forward_partial / ra_merge accept. */
+#define RA_MAX_PARTIALS 64
+
+/*
+ * Running online-softmax state of `rows` query rows (section "The
+ * online-softmax identity that makes streaming legal": "Keep three running
+ * quantities per query").  Device pointers, fp32, caller-owned:
+ *   m[rows]     running max of the scaled scores (-inf when empty)
+ *   l[rows]     running sum of exp(s - m)
+ *   o[rows, d]  running sum of exp(s - m) * v, unnormalised
+ * m is always the true running max of the scores folded so far, so a state
+ * written by the library is exactly the pages' (m, l, o).
+ */
+typedef struct ra_state {
+  float* m;
+  float* l;
+  float* o;
+  int64_t rows;
+  int32_t d;
+} ra_state;
+
+/*
+ * ra_forward -- full ring attention forward.
+ * Pages: "Ring Attention: the math", section "Accumulation math, step by step"
+ * (per-device loop over t, out = o / l) run for every query block i; ring
+ * order from section "The ring schedule: passing K/V around".
+ *   q, k, v  [B, H, N, d] of `dtype`.
+ *   out      [B, H, N, d] of `dtype` (bf16 rounded to nearest even).
+ *   lse      [B, H, N] fp32, natural log over scaled scores; may not be NULL.
+ *   P        ring blocks; must divide N (else RA_ERR_UNSUPPORTED).
+ * Errors: RA_ERR_INVALID_ARG (null pointer, B/H/N < 0, d < 1, P < 1, bad
+ * dtype), RA_ERR_UNSUPPORTED (N % P != 0; bf16 with d not in {64, 128} or
+ * c % 128 != 0; f32 with d > 256), RA_ERR_MISALIGNED, RA_ERR_ARCH, RA_ERR_CUDA.
+ */
+RA_API ra_status ra_forward(const void* q, const void* k, const void* v, void* out,
+                            float* lse, int32_t B, int32_t H, int64_t N, int32_t d,
+                            int32_t P, ra_dtype dtype, ra_stream_t stream);
+
+/*
+ * ra_forward_partial -- the ring split into G contiguous segments of steps.
+ * Partial g folds steps t in [floor(g*P/G), floor((g+1)*P/G)) of every query
+ * block's ring order from an empty state and writes its (m, l, o) to
+ * partials[g] (no normalisation).  ra_merge of the G partials gives the same
+ * out/lse as ra_forward.  This is the "Global Integration" of partial results
+ * in "Ring Attention" (bembew.net), section "The Step-by-Step Process".
+ *   partials  host array of G ra_state, each with rows = B*H*N and d = d;
+ *             their m/l/o are device buffers (o must be 16-byte aligned on
+ *             the bf16 path).
+ *   1 <= G <= min(P, RA_MAX_PARTIALS).
+ * Other arguments and errors as ra_forward.
+ */
+RA_API ra_status ra_forward_partial(const void* q, const void* k, const void* v,
+                                    int32_t B, int32_t H, int64_t N, int32_t d, int32_t P,
+                                    int32_t G, const ra_state* partials, ra_dtype dtype,
+                                    ra_stream_t stream);
+
+/*
+ * ra_state_init -- set a state to empty: m = -inf, l = 0, o = 0 ("Ring
+ * Attention: the math", section "Accumulation math, step by step": "state = (m
+ * = -inf, l = 0, o = 0)").
+ * Errors: RA_ERR_INVALID_ARG (null state or pointers, rows < 0, d < 1),
+ * RA_ERR_ARCH, RA_ERR_CUDA.
+ */
+RA_API ra_status ra_state_init(const ra_state* st, ra_stream_t stream);
+
+/*
+ * ra_fold -- fold ONE visiting K/V block into a caller-held state, in place
+ * ("Ring Attention: the math", section "The online-softmax identity that
+ * makes streaming legal": "For each incoming K/V block").  This is the
+ * operation a ring device performs at every step; chaining it over the blocks
+ * in ring order reproduces ra_forward's state.
+ *   st       state of st->rows = batch * rq rows (rq query rows per batch
+ *            entry), d = st->d.
+ *   q        [batch, rq, d] queries of `dtype`.
+ *   kblk,    [batch, kv_rows, d] keys and values of the visiting block.
+ *   vblk
+ * kv_rows == 0 leaves the state unchanged.  The bf16 path needs rq % 128 == 0
+ * and kv_rows % 128 == 0; the f32 path takes any sizes.
+ * Errors: as ra_forward; RA_ERR_UNSUPPORTED when rows is not a multiple of
+ * batch or a bf16 size rule is broken.
+ */
+RA_API ra_status ra_fold(const ra_state* st, const void* q, const void* kblk,
+                         const void* vblk, int64_t batch, int64_t kv_rows,
+                         ra_dtype dtype, ra_stream_t stream);
+
+/*
+ * ra_merge -- combine G partial states of the same rows into out and lse
+ * ("Ring Attention" (bembew.net), "Global Integration"; exact by the shift
+ * invariance in "Ring Attention: the math", section "The online-softmax
+ * identity"):
+ *     m* = max_g m_g,  w_g = exp(m_g - m*),  l* = sum_g w_g l_g,
+ *     o* = sum_g w_g o_g,  out = o* / l*,  lse = m* + ln l*.
+ * Empty partials (m = -inf, l = 0) contribute nothing; rows whose partials
+ * are all empty give out = 0 and lse = -inf.  With G = 1 this is the final
+ * normalisation out = o / l of a single state.
+ *   partials  host array of G states with equal rows and d.
+ *   out       [rows, d] of out_dtype; lse [rows] fp32.
+ * Errors: RA_ERR_INVALID_ARG (null pointers, G < 1 or > RA_MAX_PARTIALS,
+ * mismatched rows/d), RA_ERR_MISALIGNED (out or o not 4-byte aligned),
+ * RA_ERR_ARCH, RA_ERR_CUDA.
+ */
+RA_API ra_status ra_merge(const ra_state* partials, int32_t G, void* out, float* lse,
+                          ra_dtype out_dtype, ra_stream_t stream);
+
+/*
+ * ra_last_device_status -- synchronise `stream`, then read and clear the
+ * device-side watchdog word of the current device.  Returns RA_ERR_TIMEOUT if
+ * any kernel since the last call gave up a bounded wait (its results are then
+ * invalid), RA_ERR_CUDA if the synchronisation failed, else RA_OK.
+ */
+RA_API ra_status ra_last_device_status(ra_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+RA_API const char* ra_status_string(ra_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+RA_API int32_t ra_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RA_H_ */

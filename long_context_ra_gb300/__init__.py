@@ -1,0 +1,163 @@
+"""GB300-native Ring Attention fold: Python binding of ``include/ra.h``.
+
+The functions below have the names of the C entry points and only marshal
+arguments (tensor pointers, sizes, the current CUDA stream); every step of
+the computation runs in the library's kernels.  PyTorch provides device
+memory and streams.
+
+Layout: attention tensors are [B, H, N, d], contiguous, on one CUDA device;
+bf16 (tensor cores) or float32 (FFMA path).  States are fp32 (m, l, o).
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _native
+from ._native import RA_BF16, RA_F32, RA_MAX_PARTIALS, RaStateC
+
+__all__ = ["RaError", "RaState", "ra_forward", "ra_forward_partial", "ra_state_init", "ra_fold",
+           "ra_merge", "ra_last_device_status", "new_state", "library_path"]
+
+
+class RaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = _native.lib().ra_status_string(code).decode()
+        super().__init__(f"{where}: {msg}")
+
+
+def library_path() -> str:
+    return str(_native.LIB_PATH)
+
+
+def _check(code: int, where: str) -> None:
+    if code != 0:
+        raise RaError(code, where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return RA_BF16
+    if t.dtype == torch.float32:
+        return RA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: use bfloat16 or float32")
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    if not t.is_cuda:
+        raise ValueError("tensors must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+@dataclass
+class RaState:
+    """Running online-softmax state of `rows` query rows (fp32 device tensors)."""
+
+    m: torch.Tensor  # [rows]
+    l: torch.Tensor  # [rows]
+    o: torch.Tensor  # [rows, d]
+
+    @property
+    def rows(self) -> int:
+        return self.o.shape[0]
+
+    @property
+    def d(self) -> int:
+        return self.o.shape[1]
+
+    def c(self) -> RaStateC:
+        for t in (self.m, self.l, self.o):
+            if t.dtype != torch.float32:
+                raise TypeError("state tensors must be float32")
+        return RaStateC(_ptr(self.m).value, _ptr(self.l).value, _ptr(self.o).value, self.rows,
+                        self.d)
+
+
+def new_state(rows: int, d: int, device=None) -> RaState:
+    """Allocate (uninitialised) state storage; see ra_state_init."""
+    dev = device if device is not None else torch.device("cuda")
+    return RaState(torch.empty(rows, device=dev, dtype=torch.float32),
+                   torch.empty(rows, device=dev, dtype=torch.float32),
+                   torch.empty(rows, d, device=dev, dtype=torch.float32))
+
+
+def ra_forward(q, k, v, P: int, out=None, lse=None, stream=None):
+    """Ring attention forward; returns (out [B,H,N,d], lse [B,H,N] fp32)."""
+    B, H, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share shape and dtype")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, N, device=q.device, dtype=torch.float32)
+    code = _native.lib().ra_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+                                    P, _dtype_code(q), _stream(stream))
+    _check(code, "ra_forward")
+    return out, lse
+
+
+def _state_array(states):
+    arr = (RaStateC * len(states))()
+    for i, s in enumerate(states):
+        arr[i] = s.c()
+    return arr
+
+
+def ra_forward_partial(q, k, v, P: int, G: int, partials=None, stream=None):
+    """Ring split into G segments; returns G partial RaStates (rows = B*H*N)."""
+    B, H, N, d = q.shape
+    if partials is None:
+        partials = [new_state(B * H * N, d, q.device) for _ in range(G)]
+    arr = _state_array(partials)
+    code = _native.lib().ra_forward_partial(_ptr(q), _ptr(k), _ptr(v), B, H, N, d, P, G, arr,
+                                            _dtype_code(q), _stream(stream))
+    _check(code, "ra_forward_partial")
+    return partials
+
+
+def ra_state_init(state: RaState, stream=None) -> RaState:
+    sc = state.c()
+    _check(_native.lib().ra_state_init(ctypes.byref(sc), _stream(stream)), "ra_state_init")
+    return state
+
+
+def ra_fold(state: RaState, q, kblk, vblk, batch: int = 1, stream=None) -> RaState:
+    """Fold one visiting block: q [batch, rq, d], kblk/vblk [batch, kv_rows, d]."""
+    if kblk.shape != vblk.shape or kblk.dtype != q.dtype or vblk.dtype != q.dtype:
+        raise ValueError("kblk and vblk must match each other and q's dtype")
+    kv_rows = kblk.numel() // (batch * state.d) if kblk.numel() else 0
+    sc = state.c()
+    code = _native.lib().ra_fold(ctypes.byref(sc), _ptr(q), _ptr(kblk), _ptr(vblk), batch,
+                                 kv_rows, _dtype_code(q), _stream(stream))
+    _check(code, "ra_fold")
+    return state
+
+
+def ra_merge(partials, out_dtype=torch.bfloat16, out=None, lse=None, stream=None):
+    """Merge partial states; returns (out [rows, d], lse [rows])."""
+    rows, d = partials[0].rows, partials[0].d
+    dev = partials[0].o.device
+    if out is None:
+        out = torch.empty(rows, d, device=dev, dtype=out_dtype)
+    if lse is None:
+        lse = torch.empty(rows, device=dev, dtype=torch.float32)
+    arr = _state_array(partials)
+    code = _native.lib().ra_merge(arr, len(partials), _ptr(out), _ptr(lse), _dtype_code(out),
+                                  _stream(stream))
+    _check(code, "ra_merge")
+    return out, lse
+
+
+def ra_last_device_status(stream=None) -> int:
+    """Synchronise and return (and clear) the device watchdog status code."""
+    return _native.lib().ra_last_device_status(_stream(stream))

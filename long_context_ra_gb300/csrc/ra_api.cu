@@ -1,0 +1,323 @@
+// C ABI of the library: argument validation, TMA descriptor set-up and
+// kernel dispatch.  Every check runs before anything is enqueued.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "ra.h"
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+// Device-side watchdog word: kernels write a non-zero code when one of their
+// bounded waits runs out.  One copy per device.
+__device__ int g_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  bool is_sm103 = false;
+  int sms = 0;
+  int* status = nullptr;  // device address of g_status
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Looks up (once) the current device's properties and the address of its
+// watchdog word.
+ra_status current_device(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RA_ERR_ARCH;
+  if (dev < 0 || dev >= kMaxDevices) return RA_ERR_ARCH;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return RA_ERR_ARCH;
+    di.is_sm103 = prop.major == 10 && prop.minor == 3;
+    di.sms = prop.multiProcessorCount;
+    if (di.is_sm103) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return RA_ERR_CUDA;
+      di.status = static_cast<int*>(p);
+    }
+    di.ready = true;
+  }
+  if (!di.is_sm103) return RA_ERR_ARCH;
+  *out = di;
+  return RA_OK;
+}
+
+ra_status get_encoder() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_encode) return RA_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return RA_ERR_CUDA;
+  g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  return RA_OK;
+}
+
+// 2-D bf16 view [rows, d] with a box of 128 rows x 64 columns (128 bytes) and
+// the 128-byte swizzle the MMA descriptors expect.
+ra_status make_map(CUtensorMap* map, const void* ptr, int64_t rows, int d) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? RA_OK : RA_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+ra_status launched(cudaError_t e) { return e == cudaSuccess ? RA_OK : RA_ERR_CUDA; }
+
+constexpr int64_t kMaxRows = (int64_t{1} << 31) - 1;  // TMA coordinates are int32
+
+// Shared checks of the attention-shaped calls; fills the fold arguments.
+ra_status check_attention(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                          int64_t N, int32_t d, int32_t P, ra_dtype dt, FoldArgs* a) {
+  if (!q || !k || !v) return RA_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || N < 0 || d < 1 || P < 1) return RA_ERR_INVALID_ARG;
+  if (dt != RA_F32 && dt != RA_BF16) return RA_ERR_INVALID_ARG;
+  if (N % P != 0) return RA_ERR_UNSUPPORTED;
+  const int64_t rows = static_cast<int64_t>(B) * H * N;
+  if (rows > kMaxRows) return RA_ERR_UNSUPPORTED;
+  const int64_t c = N / P;
+  if (dt == RA_BF16) {
+    if (d != 64 && d != 128) return RA_ERR_UNSUPPORTED;
+    if (c % 128 != 0) return RA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return RA_ERR_MISALIGNED;
+  } else {
+    if (d > 256) return RA_ERR_UNSUPPORTED;
+    if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4)) return RA_ERR_MISALIGNED;
+  }
+  *a = FoldArgs{};
+  a->q = q;
+  a->k = k;
+  a->v = v;
+  a->slices = static_cast<int64_t>(B) * H;
+  a->nq = N;
+  a->nk = N;
+  a->d = d;
+  a->P = P;
+  a->G = 1;
+  a->tau = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  a->scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  return RA_OK;
+}
+
+// Launch a fold of either precision.  The bf16 path builds the TMA maps over
+// the [rows, d] views of q (slices * nq rows) and k, v (slices * nk rows).
+ra_status run_fold(const FoldArgs& a, ra_dtype dt, cudaStream_t s) {
+  if (dt == RA_F32) return launched(launch_fold_f32(a, s));
+  ra_status st = get_encoder();
+  if (st != RA_OK) return st;
+  CUtensorMap tq, tk, tv;
+  if ((st = make_map(&tq, a.q, a.slices * a.nq, a.d)) != RA_OK) return st;
+  if ((st = make_map(&tk, a.k, a.slices * a.nk, a.d)) != RA_OK) return st;
+  if ((st = make_map(&tv, a.v, a.slices * a.nk, a.d)) != RA_OK) return st;
+  return launched(launch_fold_sm103(a, tq, tk, tv, s));
+}
+
+bool state_ok(const ra_state* st) {
+  return st && st->m && st->l && st->o && st->rows >= 0 && st->d >= 1;
+}
+
+}  // namespace
+
+int device_sm_count() {
+  DeviceInfo di;
+  if (current_device(&di) != RA_OK) return 1;
+  return di.sms;
+}
+
+}  // namespace ra
+
+using namespace ra;
+
+extern "C" {
+
+RA_API ra_status ra_forward(const void* q, const void* k, const void* v, void* out, float* lse,
+                            int32_t B, int32_t H, int64_t N, int32_t d, int32_t P, ra_dtype dtype,
+                            ra_stream_t stream) {
+  FoldArgs a;
+  ra_status st = check_attention(q, k, v, B, H, N, d, P, dtype, &a);
+  if (st != RA_OK) return st;
+  if (!out || !lse) return RA_ERR_INVALID_ARG;
+  if (!aligned(out, dtype == RA_BF16 ? 16 : 4) || !aligned(lse, 4)) return RA_ERR_MISALIGNED;
+  if (a.slices * a.nq == 0) return RA_OK;
+  DeviceInfo di;
+  if ((st = current_device(&di)) != RA_OK) return st;
+  a.mode = kForward;
+  a.out = out;
+  a.lse = lse;
+  a.status = di.status;
+  return run_fold(a, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+RA_API ra_status ra_forward_partial(const void* q, const void* k, const void* v, int32_t B,
+                                    int32_t H, int64_t N, int32_t d, int32_t P, int32_t G,
+                                    const ra_state* partials, ra_dtype dtype,
+                                    ra_stream_t stream) {
+  FoldArgs a;
+  ra_status st = check_attention(q, k, v, B, H, N, d, P, dtype, &a);
+  if (st != RA_OK) return st;
+  if (!partials || G < 1 || G > RA_MAX_PARTIALS || G > P) return RA_ERR_INVALID_ARG;
+  const int64_t rows = a.slices * a.nq;
+  for (int g = 0; g < G; ++g) {
+    const ra_state& p = partials[g];
+    if (!state_ok(&p) || p.rows != rows || p.d != d) return RA_ERR_INVALID_ARG;
+    if (!aligned(p.m, 4) || !aligned(p.l, 4) || !aligned(p.o, dtype == RA_BF16 ? 16 : 4))
+      return RA_ERR_MISALIGNED;
+    a.part.m[g] = p.m;
+    a.part.l[g] = p.l;
+    a.part.o[g] = p.o;
+  }
+  if (rows == 0) return RA_OK;
+  DeviceInfo di;
+  if ((st = current_device(&di)) != RA_OK) return st;
+  a.mode = kPartial;
+  a.G = G;
+  a.status = di.status;
+  return run_fold(a, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+RA_API ra_status ra_state_init(const ra_state* st, ra_stream_t stream) {
+  if (!state_ok(st)) return RA_ERR_INVALID_ARG;
+  if (!aligned(st->m, 4) || !aligned(st->l, 4) || !aligned(st->o, 4)) return RA_ERR_MISALIGNED;
+  if (st->rows == 0) return RA_OK;
+  DeviceInfo di;
+  ra_status s = current_device(&di);
+  if (s != RA_OK) return s;
+  return launched(launch_state_init(st->m, st->l, st->o, st->rows, st->d,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+RA_API ra_status ra_fold(const ra_state* st, const void* q, const void* kblk, const void* vblk,
+                         int64_t batch, int64_t kv_rows, ra_dtype dtype, ra_stream_t stream) {
+  if (!state_ok(st) || !q || !kblk || !vblk) return RA_ERR_INVALID_ARG;
+  if (batch < 1 || kv_rows < 0) return RA_ERR_INVALID_ARG;
+  if (dtype != RA_F32 && dtype != RA_BF16) return RA_ERR_INVALID_ARG;
+  if (st->rows % batch != 0) return RA_ERR_UNSUPPORTED;
+  const int32_t d = st->d;
+  const int64_t rq = st->rows / batch;
+  if (st->rows > kMaxRows || batch * kv_rows > kMaxRows) return RA_ERR_UNSUPPORTED;
+  if (dtype == RA_BF16) {
+    if (d != 64 && d != 128) return RA_ERR_UNSUPPORTED;
+    if (rq % 128 != 0 || kv_rows % 128 != 0) return RA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(kblk, 16) || !aligned(vblk, 16) || !aligned(st->o, 16))
+      return RA_ERR_MISALIGNED;
+  } else {
+    if (d > 256) return RA_ERR_UNSUPPORTED;
+    if (!aligned(q, 4) || !aligned(kblk, 4) || !aligned(vblk, 4) || !aligned(st->o, 4))
+      return RA_ERR_MISALIGNED;
+  }
+  if (!aligned(st->m, 4) || !aligned(st->l, 4)) return RA_ERR_MISALIGNED;
+  if (st->rows == 0 || kv_rows == 0) return RA_OK;
+  DeviceInfo di;
+  ra_status s = current_device(&di);
+  if (s != RA_OK) return s;
+  FoldArgs a{};
+  a.q = q;
+  a.k = kblk;
+  a.v = vblk;
+  a.slices = batch;
+  a.nq = rq;
+  a.nk = kv_rows;
+  a.d = d;
+  a.P = 1;
+  a.G = 1;
+  a.mode = kFold;
+  a.tau = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  a.st_m = st->m;
+  a.st_l = st->l;
+  a.st_o = st->o;
+  a.status = di.status;
+  return run_fold(a, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+RA_API ra_status ra_merge(const ra_state* partials, int32_t G, void* out, float* lse,
+                          ra_dtype out_dtype, ra_stream_t stream) {
+  if (!partials || G < 1 || G > RA_MAX_PARTIALS || !out || !lse) return RA_ERR_INVALID_ARG;
+  if (out_dtype != RA_F32 && out_dtype != RA_BF16) return RA_ERR_INVALID_ARG;
+  MergeArgs a{};
+  const int64_t rows = partials[0].rows;
+  const int32_t d = partials[0].d;
+  bool vec = d % 4 == 0 && aligned(out, out_dtype == RA_BF16 ? 8 : 16);
+  for (int g = 0; g < G; ++g) {
+    const ra_state& p = partials[g];
+    if (!state_ok(&p) || p.rows != rows || p.d != d) return RA_ERR_INVALID_ARG;
+    if (!aligned(p.m, 4) || !aligned(p.l, 4) || !aligned(p.o, 4)) return RA_ERR_MISALIGNED;
+    vec = vec && aligned(p.o, 16);
+    a.part.m[g] = p.m;
+    a.part.l[g] = p.l;
+    a.part.o[g] = p.o;
+  }
+  if (!aligned(out, out_dtype == RA_BF16 ? 2 : 4) || !aligned(lse, 4)) return RA_ERR_MISALIGNED;
+  if (rows == 0) return RA_OK;
+  DeviceInfo di;
+  ra_status s = current_device(&di);
+  if (s != RA_OK) return s;
+  a.G = G;
+  a.rows = rows;
+  a.d = d;
+  a.out = out;
+  a.lse = lse;
+  a.out_bf16 = out_dtype == RA_BF16 ? 1 : 0;
+  a.vec4 = vec ? 1 : 0;
+  return launched(launch_merge(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+RA_API ra_status ra_last_device_status(ra_stream_t stream) {
+  DeviceInfo di;
+  ra_status s = current_device(&di);
+  if (s != RA_OK) return s;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return RA_ERR_CUDA;
+  int word = 0;
+  const int zero = 0;
+  if (cudaMemcpy(&word, di.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return RA_ERR_CUDA;
+  if (cudaMemcpy(di.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return RA_ERR_CUDA;
+  return word == 0 ? RA_OK : RA_ERR_TIMEOUT;
+}
+
+RA_API const char* ra_status_string(ra_status s) {
+  switch (s) {
+    case RA_OK: return "RA_OK";
+    case RA_ERR_INVALID_ARG: return "RA_ERR_INVALID_ARG: invalid argument";
+    case RA_ERR_UNSUPPORTED: return "RA_ERR_UNSUPPORTED: shape or type not supported";
+    case RA_ERR_MISALIGNED: return "RA_ERR_MISALIGNED: pointer alignment too small";
+    case RA_ERR_ARCH: return "RA_ERR_ARCH: no compute capability 10.3 device";
+    case RA_ERR_CUDA: return "RA_ERR_CUDA: CUDA call failed";
+    case RA_ERR_TIMEOUT: return "RA_ERR_TIMEOUT: a kernel wait ran out (watchdog)";
+  }
+  return "unknown ra_status";
+}
+
+RA_API int32_t ra_version(void) { return 100; }
+
+}  // extern "C"

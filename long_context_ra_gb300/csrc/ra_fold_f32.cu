@@ -1,0 +1,149 @@
+// fp32 fold kernel (FFMA only, no TF32): the exact-precision path for any
+// head dimension 1 <= d <= 256 and any block size.
+//
+// One warp owns one query row ("Ring Attention: the math", section "Sharding
+// the sequence": queries stay home) and walks the key blocks in ring order
+// j = (i - t) mod P (section "The ring schedule: passing K/V around").  Each
+// block is folded 32 keys at a time -- one key per lane -- with the update of
+// section "The online-softmax identity that makes streaming legal":
+//   s = tau q.k;  m' = max(m, max s);  alpha = exp(m - m');
+//   l' = alpha l + sum exp(s - m');  o' = alpha o + sum exp(s - m') v.
+// Folding a block in chunks is exact by the same identity.  The lanes split
+// o: lane e holds o[e], o[e + 32], ...
+
+#include <cmath>
+
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+constexpr int kWarps = 4;
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+template <int DV>  // o values per lane: d <= 32 * DV
+__global__ void __launch_bounds__(kWarps * 32) fold_f32_kernel(const FoldArgs a) {
+  __shared__ float qs[kWarps][32 * DV];
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int d = a.d;
+  const int64_t rid = static_cast<int64_t>(blockIdx.x) * kWarps + warp;  // query row
+  const int g = blockIdx.y;                                              // segment
+  if (rid >= a.slices * a.nq) return;  // whole warp leaves together
+  const int64_t slice = rid / a.nq;
+  const int64_t n = rid % a.nq;
+  const int64_t cq = a.nq / a.P;
+  const int64_t ck = a.nk / a.P;
+  const int i = static_cast<int>(n / cq);
+  const int t0 = static_cast<int>(static_cast<int64_t>(g) * a.P / a.G);
+  const int t1 = static_cast<int>(static_cast<int64_t>(g + 1) * a.P / a.G);
+
+  const float* q = static_cast<const float*>(a.q) + rid * d;
+  for (int e = lane; e < d; e += 32) qs[warp][e] = q[e];
+  __syncwarp();
+
+  float m = -INFINITY, l = 0.f;
+  float o[DV];
+#pragma unroll
+  for (int v = 0; v < DV; ++v) o[v] = 0.f;
+  if (a.mode == kFold) {
+    m = a.st_m[rid];
+    l = a.st_l[rid];
+#pragma unroll
+    for (int v = 0; v < DV; ++v) {
+      const int e = lane + 32 * v;
+      if (e < d) o[v] = a.st_o[rid * d + e];
+    }
+  }
+
+  for (int t = t0; t < t1; ++t) {
+    int j = (i - t) % a.P;
+    if (j < 0) j += a.P;
+    const int64_t krow0 = slice * a.nk + static_cast<int64_t>(j) * ck;
+    const float* kb = static_cast<const float*>(a.k) + krow0 * d;
+    const float* vb = static_cast<const float*>(a.v) + krow0 * d;
+    for (int64_t c0 = 0; c0 < ck; c0 += 32) {
+      const int64_t key = c0 + lane;
+      const bool valid = key < ck;
+      float s = -INFINITY;
+      if (valid) {
+        const float* kr = kb + key * d;
+        float acc = 0.f;
+        for (int e = 0; e < d; ++e) acc = fmaf(qs[warp][e], kr[e], acc);
+        s = acc * a.tau;
+      }
+      const float m_new = fmaxf(m, warp_max(s));
+      const float alpha = m_new == -INFINITY ? 1.f : expf(m - m_new);
+      const float p = valid ? expf(s - m_new) : 0.f;
+      l = alpha * l + warp_sum(p);
+#pragma unroll
+      for (int v = 0; v < DV; ++v) o[v] *= alpha;
+      const int nvalid = ck - c0 < 32 ? static_cast<int>(ck - c0) : 32;
+      for (int jj = 0; jj < nvalid; ++jj) {
+        const float pj = __shfl_sync(0xffffffffu, p, jj);
+        const float* vr = vb + (c0 + jj) * d;
+#pragma unroll
+        for (int v = 0; v < DV; ++v) {
+          const int e = lane + 32 * v;
+          if (e < d) o[v] = fmaf(pj, vr[e], o[v]);
+        }
+      }
+      m = m_new;
+    }
+  }
+
+  if (a.mode == kForward) {
+    float* out = static_cast<float*>(a.out) + rid * d;
+    const float inv = 1.f / l;
+#pragma unroll
+    for (int v = 0; v < DV; ++v) {
+      const int e = lane + 32 * v;
+      if (e < d) out[e] = o[v] * inv;
+    }
+    if (lane == 0) a.lse[rid] = m + logf(l);
+  } else {
+    float* mo = a.mode == kPartial ? a.part.m[g] : a.st_m;
+    float* lo = a.mode == kPartial ? a.part.l[g] : a.st_l;
+    float* oo = a.mode == kPartial ? a.part.o[g] : a.st_o;
+#pragma unroll
+    for (int v = 0; v < DV; ++v) {
+      const int e = lane + 32 * v;
+      if (e < d) oo[rid * d + e] = o[v];
+    }
+    if (lane == 0) {
+      mo[rid] = m;
+      lo[rid] = l;
+    }
+  }
+}
+
+template <int DV>
+cudaError_t launch_dv(const FoldArgs& a, cudaStream_t s) {
+  const int64_t rows = a.slices * a.nq;
+  const dim3 grid(static_cast<unsigned>((rows + kWarps - 1) / kWarps), static_cast<unsigned>(a.G));
+  fold_f32_kernel<DV><<<grid, kWarps * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fold_f32(const FoldArgs& a, cudaStream_t s) {
+  if (a.d <= 32) return launch_dv<1>(a, s);
+  if (a.d <= 64) return launch_dv<2>(a, s);
+  if (a.d <= 128) return launch_dv<4>(a, s);
+  if (a.d <= 256) return launch_dv<8>(a, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ra

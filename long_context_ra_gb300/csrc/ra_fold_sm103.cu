@@ -1,0 +1,577 @@
+// Tensor-core fold kernel for bf16 inputs on sm_103a (GB300).
+//
+// One CTA owns up to two 128-row query tiles of one query block i
+// ("Ring Attention: the math", section "Sharding the sequence": queries stay
+// home) and streams the key/value tiles of the blocks it visits in ring order
+// j = (i - t) mod P (section "The ring schedule: passing K/V around").  Each
+// 128-key tile is folded into the running per-row state with the update of
+// section "The online-softmax identity that makes streaming legal":
+//
+//   S = tau * Q K^T             tcgen05.mma, bf16 -> fp32 in TMEM
+//   m' = max(m, rowmax S)       softmax warps, registers
+//   p  = exp(S - m'), l' = alpha l + sum p
+//   O  = alpha O + p V          tcgen05.mma, p as bf16 from shared memory
+//
+// The pages' send/recv of the next block while the current one is computed
+// (section "Accumulation math, step by step") becomes a TMA prefetch of the
+// next K/V tile into a free stage of a shared-memory ring.
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax for query tile 0 (thread = row = TMEM lane)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    TMA producer (one thread)
+//   warp  9    TMEM allocator and MMA issuer (one thread)
+//
+// The two query tiles ping-pong: while one tile's softmax runs on the CUDA
+// cores, the tensor cores work on the other tile's products.
+//
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D),
+// O1 [256+D, 256+2D).  Shared memory (1024-byte aligned, 128-byte swizzle
+// everywhere): Q0, Q1, kStages K/V tiles, P0, P1 (bf16 probabilities),
+// mbarriers.
+//
+// The running max used for the exponentials is a per-row reference that is
+// raised only when a tile's max exceeds it by more than kRescaleLog2 (log2
+// units).  The identity holds for any reference, so l and o stay exact; most
+// tiles then need no rescale of O in TMEM.  States leaving the kernel are
+// re-expressed relative to the true running max.
+//
+// Every wait is bounded.  A wait that runs out records a timeout in the
+// device status word, raises a CTA-wide abort flag, lets the in-flight TMA
+// loads and MMAs finish (again bounded), frees TMEM and returns.
+
+#include <cmath>
+
+#include "ra_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace ra {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
+constexpr int kBN = 128;  // keys per K/V tile
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr long long kWaitLimit = 1ll << 31;  // SM cycles, about one second
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct Layout {
+  static constexpr int kBoxBytes = kBM * 128;  // 128 rows x 128 bytes (64 bf16)
+  static constexpr int kTileBytes = kBM * D * 2;
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr int kPBytes = kBM * kBN * 2;
+  static constexpr int kQ0 = 0;
+  static constexpr int kQ1 = kTileBytes;
+  static constexpr int kKV = 2 * kTileBytes;
+  static constexpr int kP0 = kKV + kStages * kTileBytes;
+  static constexpr int kP1 = kP0 + kPBytes;
+  static constexpr int kBar = kP1 + kPBytes;
+  // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 7;
+  static constexpr int kMisc = kBar + kNumBars * 8;  // TMEM base, abort flag
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kSmem = kBytes + 1024;  // slack for 1024-byte alignment
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+template <int D>
+struct Bars {
+  uint32_t base;
+  __device__ uint32_t q_full() const { return base; }
+  __device__ uint32_t kv_full(int s) const { return base + 8 * (1 + s); }
+  __device__ uint32_t kv_empty(int s) const { return base + 8 * (1 + Layout<D>::kStages + s); }
+  __device__ uint32_t s_full(int t) const { return base + 8 * (1 + 2 * Layout<D>::kStages + t); }
+  __device__ uint32_t p_full(int t) const { return base + 8 * (3 + 2 * Layout<D>::kStages + t); }
+  __device__ uint32_t o_full(int t) const { return base + 8 * (5 + 2 * Layout<D>::kStages + t); }
+  __device__ uint32_t drain() const { return base + 8 * (7 + 2 * Layout<D>::kStages); }
+};
+
+struct Abort {
+  volatile uint32_t* flag;
+  int* status;
+  __device__ void raise() const {
+    *flag = 1u;
+    atomicCAS(status, 0, kStatusTimeout);
+  }
+};
+
+// Single-thread bounded wait.
+__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const Abort& ab) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long start = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*ab.flag) return false;
+    if (clock64() - start > kWaitLimit) {
+      ab.raise();
+      return false;
+    }
+  }
+}
+
+// Bounded wait used while aborting (ignores the abort flag).
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const long long start = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - start > kWaitLimit) return;
+  }
+}
+
+// Whole-warp bounded wait: every lane polls and the warp agrees on the
+// outcome, so the warp stays converged for the .sync.aligned TMEM accesses.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Abort& ab) {
+  bool done = mbar_try_wait(bar, parity);
+  if (__all_sync(0xffffffffu, done)) return true;
+  const long long start = clock64();
+  while (true) {
+    done = done || mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    const bool timed_out = clock64() - start > kWaitLimit;
+    const bool give_up = (*ab.flag != 0u) || timed_out;
+    if (__any_sync(0xffffffffu, give_up)) {
+      if (__any_sync(0xffffffffu, timed_out) && (threadIdx.x % 32) == 0) ab.raise();
+      return false;
+    }
+  }
+}
+
+// Which key rows iteration `it` of a work unit loads.
+struct KvWalk {
+  int64_t slice_row0;  // slice * nk
+  int64_t ck;          // keys per block
+  int i, P, t0, kv_tiles;
+  __device__ int64_t row(int it) const {
+    const int t = t0 + it / kv_tiles;
+    const int kt = it % kv_tiles;
+    int j = (i - t) % P;
+    if (j < 0) j += P;
+    return slice_row0 + static_cast<int64_t>(j) * ck + static_cast<int64_t>(kt) * kBN;
+  }
+};
+
+// S[tmem] = Q K^T for one 128x128 tile: D/16 MMAs of K = 16 along d.  Q and K
+// are K-major (d contiguous) in 128-byte-swizzled boxes of 64 columns; the
+// k-th slice of 16 columns starts 32 bytes further inside its box.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * Layout<D>::kBoxBytes + (kk % 4) * 32;
+    mma_bf16_ss(d_tmem, desc_sw128(q_smem + off, 16, 1024), desc_sw128(k_smem + off, 16, 1024),
+                idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O[tmem] (+)= P V for one tile: 8 MMAs of K = 16 keys.  P is K-major (keys
+// contiguous) like Q; V is MN-major (d contiguous): 8 keys of one 64-column
+// box form a 1024-byte swizzle atom (stride byte offset), the second box of
+// 64 columns sits one box further (leading byte offset).
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_smem, uint32_t v_smem,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, true);
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk) {
+    const uint32_t aoff = (kk / 4) * Layout<D>::kBoxBytes + (kk % 4) * 32;
+    const uint32_t boff = kk * 16 * 128;
+    mma_bf16_ss(d_tmem, desc_sw128(p_smem + aoff, 16, 1024),
+                desc_sw128(v_smem + boff, Layout<D>::kBoxBytes, 1024), idesc,
+                (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fold_sm103_kernel(const __grid_constant__ FoldArgs a, const __grid_constant__ CUtensorMap tq,
+                      const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const Bars<D> bars{base + L::kBar};
+  volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + L::kMisc);
+  const Abort ab{tmem_holder + 1, a.status};
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // ---- work unit: (slice, query block i, segment g, tile pair pr) ----
+  const int64_t cq = a.nq / a.P;
+  const int64_t ck = a.nk / a.P;
+  const int tiles_q = static_cast<int>(cq / kBM);
+  const int pairs = (tiles_q + 1) / 2;
+  int64_t u = blockIdx.x;
+  const int pr = static_cast<int>(u % pairs);
+  u /= pairs;
+  const int g = static_cast<int>(u % a.G);
+  u /= a.G;
+  const int i = static_cast<int>(u % a.P);
+  const int64_t slice = u / a.P;
+  const bool has_t1 = 2 * pr + 1 < tiles_q;
+  const int t0 = static_cast<int>(static_cast<int64_t>(g) * a.P / a.G);
+  const int t1 = static_cast<int>(static_cast<int64_t>(g + 1) * a.P / a.G);
+  const int kv_tiles = static_cast<int>(ck / kBN);
+  const int n_iter = (t1 - t0) * kv_tiles;
+  const int64_t q_row0 = slice * a.nq + static_cast<int64_t>(i) * cq +
+                         static_cast<int64_t>(pr) * 2 * kBM;
+  const KvWalk walk{slice * a.nk, ck, i, a.P, t0, kv_tiles};
+
+  // ---- set-up ----
+  if (threadIdx.x == 0) {
+    mbar_init(bars.q_full(), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(bars.kv_full(s), 1);
+      mbar_init(bars.kv_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bars.s_full(t), 1);
+      mbar_init(bars.p_full(t), 128);
+      mbar_init(bars.o_full(t), 1);
+    }
+    mbar_init(bars.drain(), 1);
+    *ab.flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(base + L::kMisc, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    prefetch_tmap(&tq);
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == kLoadWarp) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      const uint32_t qbytes = (has_t1 ? 2u : 1u) * L::kTileBytes;
+      mbar_arrive_expect_tx(bars.q_full(), qbytes);
+#pragma unroll
+      for (int b = 0; b < L::kBoxes; ++b) {
+        tma_load_2d(base + L::kQ0 + b * L::kBoxBytes, &tq, b * 64, static_cast<int32_t>(q_row0),
+                    bars.q_full());
+        if (has_t1)
+          tma_load_2d(base + L::kQ1 + b * L::kBoxBytes, &tq, b * 64,
+                      static_cast<int32_t>(q_row0 + kBM), bars.q_full());
+      }
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, last_parity = 0;  // per-stage bit masks, for the drain
+      bool ok = true;
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const int32_t row = static_cast<int32_t>(walk.row(it));
+        for (int kind = 0; kind < 2; ++kind) {
+          if (!wait1(bars.kv_empty(stage), phase ^ 1u, ab)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bars.kv_full(stage), L::kTileBytes);
+          const CUtensorMap* map = kind == 0 ? &tk : &tv;
+#pragma unroll
+          for (int b = 0; b < L::kBoxes; ++b)
+            tma_load_2d(base + L::kKV + stage * L::kTileBytes + b * L::kBoxBytes, map, b * 64, row,
+                        bars.kv_full(stage));
+          issued |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == L::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Let every load already issued land before the CTA goes away.
+        wait_drain(bars.q_full(), 0);
+        for (int s = 0; s < L::kStages; ++s)
+          if (issued & (1u << s)) wait_drain(bars.kv_full(s), (last_parity >> s) & 1u);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      const uint32_t tS0 = tmem, tS1 = tmem + 128;
+      const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
+      const uint32_t sQ0 = base + L::kQ0, sQ1 = base + L::kQ1;
+      const uint32_t sP0 = base + L::kP0, sP1 = base + L::kP1;
+      const bool from_state = a.mode == kFold;
+      bool ok = wait1(bars.q_full(), 0, ab);
+      int cons = 0;  // K/V tiles consumed so far
+      if (ok) ok = wait1(bars.kv_full(0), 0, ab);
+      if (ok) {
+        tc_fence_after();
+        cons = 1;
+        issue_qk<D>(tS0, sQ0, base + L::kKV);
+        mma_commit(bars.s_full(0));
+        if (has_t1) {
+          issue_qk<D>(tS1, sQ1, base + L::kKV);
+          mma_commit(bars.s_full(1));
+        }
+        mma_commit(bars.kv_empty(0));
+      }
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const uint32_t par = static_cast<uint32_t>(it & 1);
+        const int sV = cons % L::kStages;
+        if (!wait1(bars.kv_full(sV), static_cast<uint32_t>((cons / L::kStages) & 1), ab)) {
+          ok = false;
+          break;
+        }
+        ++cons;
+        const uint32_t sVaddr = base + L::kKV + sV * L::kTileBytes;
+        if (!wait1(bars.p_full(0), par, ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool acc = it > 0 || from_state;
+        issue_pv<D>(tO0, sP0, sVaddr, acc);
+        const bool more = it + 1 < n_iter;
+        uint32_t sKaddr = 0;
+        int sK = 0;
+        if (more) {
+          sK = cons % L::kStages;
+          if (!wait1(bars.kv_full(sK), static_cast<uint32_t>((cons / L::kStages) & 1), ab)) {
+            ok = false;
+            break;
+          }
+          ++cons;
+          tc_fence_after();
+          sKaddr = base + L::kKV + sK * L::kTileBytes;
+          issue_qk<D>(tS0, sQ0, sKaddr);
+          mma_commit(bars.s_full(0));
+        }
+        if (has_t1) {
+          if (!wait1(bars.p_full(1), par, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv<D>(tO1, sP1, sVaddr, acc);
+        }
+        mma_commit(bars.kv_empty(sV));
+        if (more) {
+          if (has_t1) {
+            issue_qk<D>(tS1, sQ1, sKaddr);
+            mma_commit(bars.s_full(1));
+          }
+          mma_commit(bars.kv_empty(sK));
+        }
+      }
+      if (ok) {
+        mma_commit(bars.o_full(0));
+        if (has_t1) mma_commit(bars.o_full(1));
+      } else {
+        // Wait for every MMA already issued before TMEM is released.
+        mma_commit(bars.drain());
+        wait_drain(bars.drain(), 0);
+      }
+    }
+  } else {
+    // ================= softmax warps =================
+    const int t = warp / 4;   // query tile
+    const int wq = warp % 4;  // TMEM lane quarter of this warp
+    if (t == 0 || has_t1) {
+      const int row = wq * 32 + lane;
+      const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+      const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(t * 128);
+      const uint32_t tO = tmem + lane_off + 256u + static_cast<uint32_t>(t * D);
+      const uint32_t sP = base + (t == 0 ? L::kP0 : L::kP1);
+      const int64_t grow = q_row0 + t * kBM + row;  // global query row
+      const float sl2 = a.scale_log2;
+
+      float m_ref = -INFINITY;   // reference max of the exponentials (log2 units)
+      float m_true = -INFINITY;  // true running max (log2 units)
+      float l = 0.f;
+      bool o_valid = false;
+      if (a.mode == kFold) {
+        m_ref = a.st_m[grow] * kLog2e;
+        m_true = m_ref;
+        l = a.st_l[grow];
+        const float4* src = reinterpret_cast<const float4*>(a.st_o + grow * D);
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t r[32];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 x = src[c / 4 + e];
+            r[4 * e + 0] = __float_as_uint(x.x);
+            r[4 * e + 1] = __float_as_uint(x.y);
+            r[4 * e + 2] = __float_as_uint(x.z);
+            r[4 * e + 3] = __float_as_uint(x.w);
+          }
+          tmem_st32(tO + c, r);
+        }
+        tmem_st_wait();
+        o_valid = true;
+      }
+
+      bool ok = true;
+      for (int it = 0; it < n_iter; ++it) {
+        if (!wait_warp(bars.s_full(t), static_cast<uint32_t>(it & 1), ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t s[kBN];
+#pragma unroll
+        for (int c = 0; c < kBN; c += 32) tmem_ld32(tS + c, s + c);
+        tmem_ld_wait();
+        reg_fence(s, kBN);
+
+        float mx = __uint_as_float(s[0]);
+#pragma unroll
+        for (int j = 1; j < kBN; ++j) mx = fmaxf(mx, __uint_as_float(s[j]));
+        const float m_new = mx * sl2;
+        m_true = fmaxf(m_true, m_new);
+        const bool need = m_new > m_ref + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2(m_ref - m_new) : 1.f;
+          if (o_valid) {
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+              uint32_t r[32];
+              tmem_ld32(tO + c, r);
+              tmem_ld_wait();
+              reg_fence(r, 32);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+              tmem_st32(tO + c, r);
+            }
+            tmem_st_wait();
+          }
+          if (need) {
+            l *= alpha;
+            m_ref = m_new;
+          }
+        }
+
+        // p = exp2(s * tau * log2(e) - m_ref), rounded to bf16 and written
+        // to P in the 128-byte-swizzled K-major layout the MMA reads.
+        const float neg = -m_ref;
+        const uint32_t rbase = sP + static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128);
+        float lsum = 0.f;
+#pragma unroll
+        for (int kc = 0; kc < kBN / 8; ++kc) {
+          float p[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) p[e] = ex2(fmaf(__uint_as_float(s[kc * 8 + e]), sl2, neg));
+#pragma unroll
+          for (int e = 0; e < 8; ++e) lsum += p[e];
+          const uint32_t addr = rbase + static_cast<uint32_t>((kc >> 3) * L::kBoxBytes) +
+                                (static_cast<uint32_t>((kc & 7) ^ (row & 7)) << 4);
+          st_shared_v4(addr, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
+                       pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+        }
+        l += lsum;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bars.p_full(t));
+        o_valid = true;
+      }
+
+      if (ok && wait_warp(bars.o_full(t), 0, ab)) {
+        tc_fence_after();
+        if (a.mode == kForward) {
+          const float inv = 1.f / l;
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + grow * D);
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(tO + c, r);
+            tmem_ld_wait();
+            reg_fence(r, 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * inv, __uint_as_float(r[8 * e + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * inv, __uint_as_float(r[8 * e + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * inv, __uint_as_float(r[8 * e + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * inv, __uint_as_float(r[8 * e + 7]) * inv);
+              dst[c / 8 + e] = w;
+            }
+          }
+          a.lse[grow] = (m_ref + __log2f(l)) * kLn2;
+        } else {
+          // Re-express (l, o) relative to the true running max.
+          const float fix = ex2(m_ref - m_true);
+          float* mo = a.mode == kPartial ? a.part.m[g] : a.st_m;
+          float* lo = a.mode == kPartial ? a.part.l[g] : a.st_l;
+          float* oo = a.mode == kPartial ? a.part.o[g] : a.st_o;
+          float4* dst = reinterpret_cast<float4*>(oo + grow * D);
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(tO + c, r);
+            tmem_ld_wait();
+            reg_fence(r, 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[c / 4 + e] = make_float4(__uint_as_float(r[4 * e + 0]) * fix,
+                                           __uint_as_float(r[4 * e + 1]) * fix,
+                                           __uint_as_float(r[4 * e + 2]) * fix,
+                                           __uint_as_float(r[4 * e + 3]) * fix);
+          }
+          mo[grow] = m_true * kLn2;
+          lo[grow] = l * fix;
+        }
+      }
+    }
+  }
+
+  // ---- teardown ----
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const FoldArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                     const CUtensorMap& tv, cudaStream_t s) {
+  using L = Layout<D>;
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(fold_sm103_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kSmem);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const int64_t cq = a.nq / a.P;
+  const int64_t tiles_q = cq / kBM;
+  const int64_t pairs = (tiles_q + 1) / 2;
+  const int64_t grid = a.slices * a.P * a.G * pairs;
+  fold_sm103_kernel<D><<<static_cast<unsigned>(grid), kThreads, L::kSmem, s>>>(a, tq, tk, tv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fold_sm103(const FoldArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, cudaStream_t s) {
+  if (a.d == 128) return launch_d<128>(a, tq, tk, tv, s);
+  if (a.d == 64) return launch_d<64>(a, tq, tk, tv, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ra

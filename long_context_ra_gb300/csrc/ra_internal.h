@@ -1,0 +1,81 @@
+// Internal interface between the C ABI layer (ra_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ra.h"
+
+namespace ra {
+
+// What a fold launch does with its state.
+enum Mode : int32_t {
+  kForward = 0,  // empty state, all P ring steps, write out = o / l and lse
+  kPartial = 1,  // empty state, one segment of ring steps, write (m, l, o)
+  kFold = 2,     // load (m, l, o), fold one block, write (m, l, o) back
+};
+
+// Per-segment partial-state pointers (device).
+struct PartialPtrs {
+  float* m[RA_MAX_PARTIALS];
+  float* l[RA_MAX_PARTIALS];
+  float* o[RA_MAX_PARTIALS];
+};
+
+// Everything a fold kernel needs besides the TMA descriptors.
+//
+// The work is `slices` independent problems (B*H heads, or the batch of a
+// fold call).  Slice s has nq query rows and nk key rows, each cut into P
+// contiguous blocks (cq = nq / P, ck = nk / P).  Query block i visits key
+// block (i - t) mod P at ring step t.  In partial mode the P steps are split
+// into G contiguous segments; in fold mode P = G = 1.
+struct FoldArgs {
+  const void* q;  // [slices, nq, d]
+  const void* k;  // [slices, nk, d]
+  const void* v;  // [slices, nk, d]
+  int64_t slices;
+  int64_t nq;
+  int64_t nk;
+  int32_t d;
+  int32_t P;
+  int32_t G;
+  int32_t mode;
+  float tau;         // 1 / sqrt(d)
+  float scale_log2;  // tau * log2(e)
+  void* out;         // forward: [slices, nq, d] (input dtype)
+  float* lse;        // forward: [slices, nq]
+  float* st_m;       // fold: state in/out
+  float* st_l;
+  float* st_o;
+  int* status;       // device watchdog word (0 = fine)
+  PartialPtrs part;  // partial mode
+};
+
+struct MergeArgs {
+  PartialPtrs part;
+  int32_t G;
+  int64_t rows;
+  int32_t d;
+  void* out;
+  float* lse;
+  int32_t out_bf16;
+  int32_t vec4;  // o rows and out allow 16-byte (f32) / 8-byte (bf16) vector access
+};
+
+// Launchers (each returns the launch's cudaError_t).
+cudaError_t launch_fold_sm103(const FoldArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, cudaStream_t s);
+cudaError_t launch_fold_f32(const FoldArgs& a, cudaStream_t s);
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
+cudaError_t launch_state_init(float* m, float* l, float* o, int64_t rows, int32_t d,
+                              cudaStream_t s);
+
+// Watchdog codes written to FoldArgs::status.
+constexpr int kStatusTimeout = 1;
+
+// Number of SMs of the current device (cached).
+int device_sm_count();
+
+}  // namespace ra

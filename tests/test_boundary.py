@@ -1,0 +1,97 @@
+"""The C ABI on the host: the library loads, exports every declared entry
+point, and validates arguments before touching the GPU (no GPU needed)."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+from long_context_ra_gb300 import _native
+from long_context_ra_gb300.build import build
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return _native.lib()
+
+
+def declared_symbols():
+    text = (ROOT / "include" / "ra.h").read_text()
+    return sorted(set(re.findall(r"RA_API\s+[\w\s\*]+?\b(ra_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_symbols()
+    assert len(names) >= 8, names
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(_native.PROTOTYPES), "binding prototypes drift from the header"
+
+
+def test_status_strings(L):
+    for code in range(7):
+        s = L.ra_status_string(code).decode()
+        assert s.startswith("RA_"), s
+    assert b"unknown" in L.ra_status_string(99)
+    assert L.ra_version() >= 100
+
+
+BF16, F32 = _native.RA_BF16, _native.RA_F32
+A = 1 << 20  # a fake, 16-byte-aligned "device" address: never dereferenced
+
+
+def fwd(L, q=A, k=A, v=A, out=A, lse=A, B=1, H=1, N=256, d=64, P=2, dt=BF16):
+    return L.ra_forward(q, k, v, out, lse, B, H, N, d, P, dt, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), _native.RA_ERR_INVALID_ARG),
+    (dict(lse=None), _native.RA_ERR_INVALID_ARG),
+    (dict(B=-1), _native.RA_ERR_INVALID_ARG),
+    (dict(N=-4), _native.RA_ERR_INVALID_ARG),
+    (dict(d=0), _native.RA_ERR_INVALID_ARG),
+    (dict(P=0), _native.RA_ERR_INVALID_ARG),
+    (dict(dt=7), _native.RA_ERR_INVALID_ARG),
+    (dict(N=250, P=4), _native.RA_ERR_UNSUPPORTED),            # P does not divide N
+    (dict(d=96), _native.RA_ERR_UNSUPPORTED),                  # bf16 head dim
+    (dict(N=256, P=4), _native.RA_ERR_UNSUPPORTED),            # bf16 c = 64 not a multiple of 128
+    (dict(d=300, dt=F32), _native.RA_ERR_UNSUPPORTED),         # f32 head dim
+    (dict(q=A + 8), _native.RA_ERR_MISALIGNED),                # TMA needs 16 bytes
+    (dict(out=A + 8), _native.RA_ERR_MISALIGNED),
+    (dict(q=A + 2, dt=F32), _native.RA_ERR_MISALIGNED),
+])
+def test_forward_validation(L, kw, code):
+    assert fwd(L, **kw) == code
+
+
+def test_empty_problem_launches_nothing(L):
+    # zero rows: RA_OK without any CUDA call (no device here)
+    assert fwd(L, B=0) == _native.RA_OK
+    assert fwd(L, N=0, P=1) == _native.RA_OK
+
+
+def test_valid_call_without_device_reports_arch(L):
+    # arguments are fine; with no CUDA device the call stops at the device check
+    assert fwd(L) == _native.RA_ERR_ARCH
+
+
+def test_fold_and_merge_validation(L):
+    st = _native.RaStateC(A, A, A, 256, 64)
+    ref = ctypes.byref(st)
+    assert L.ra_fold(None, A, A, A, 1, 128, BF16, None) == _native.RA_ERR_INVALID_ARG
+    assert L.ra_fold(ref, A, A, A, 0, 128, BF16, None) == _native.RA_ERR_INVALID_ARG
+    assert L.ra_fold(ref, A, A, A, 3, 128, BF16, None) == _native.RA_ERR_UNSUPPORTED  # 256 % 3
+    assert L.ra_fold(ref, A, A, A, 1, 100, BF16, None) == _native.RA_ERR_UNSUPPORTED  # kv % 128
+    assert L.ra_fold(ref, A, A, A, 1, 0, BF16, None) == _native.RA_OK  # nothing to fold
+    arr = (_native.RaStateC * 2)(st, _native.RaStateC(A, A, A, 128, 64))
+    assert L.ra_merge(arr, 2, A, A, BF16, None) == _native.RA_ERR_INVALID_ARG  # rows differ
+    assert L.ra_merge(arr, 0, A, A, BF16, None) == _native.RA_ERR_INVALID_ARG
+    assert L.ra_merge(arr, 65, A, A, BF16, None) == _native.RA_ERR_INVALID_ARG
+    assert L.ra_forward_partial(A, A, A, 1, 1, 256, 64, 2, 3, arr, BF16, None) == \
+        _native.RA_ERR_INVALID_ARG  # G > P
+    empty = _native.RaStateC(A, A, A, 0, 64)
+    assert L.ra_state_init(ctypes.byref(empty), None) == _native.RA_OK
+    assert L.ra_state_init(None, None) == _native.RA_ERR_INVALID_ARG
