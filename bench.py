@@ -14,6 +14,7 @@ virtual ring lives on one GPU; there is no exchange between ranks).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -110,6 +111,23 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
                 "reasons": sorted(reasons)}
+
+
+def max_over_ranks(x: float, device, world: int) -> float:
+    """Largest value of x over all ranks (the slowest replica sets the time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_replica: float, world: int, ms_max: float) -> float:
+    """Whole-job TFLOP/s: every replica's work over the slowest replica's time."""
+    return world * flops_per_replica / (ms_max * 1e-3) / 1e12
 
 
 def cpu_oracle_baseline(w, q, k, v, target_s: float):
@@ -241,11 +259,8 @@ def run_ours(args, w) -> None:
     ms = e0.elapsed_time(e1) / args.steps
     if ra.ra_last_device_status() != 0:
         raise RuntimeError("kernel watchdog fired in the timed region")
-    t = torch.tensor([ms], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    value = world * w.flops / (ms_max * 1e-3) / 1e12
+    ms_max = max_over_ranks(ms, dev, world)
+    value = job_throughput(w.flops, world, ms_max)
 
     # end to end through the C ABI: pinned host inputs -> device, forward,
     # out and lse back to pinned host memory, every step
@@ -273,10 +288,8 @@ def run_ours(args, w) -> None:
     torch.cuda.synchronize()
     wall = (time.perf_counter() - w0) / n_e2e
     ms_e2e = max(e0.elapsed_time(e1) / n_e2e, wall * 1e3)
-    te = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = world * w.flops / (float(te.item()) * 1e-3) / 1e12
+    ms_e2e_max = max_over_ranks(ms_e2e, dev, world)
+    e2e_value = job_throughput(w.flops, world, ms_e2e_max)
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
     d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
 
@@ -305,7 +318,7 @@ def run_ours(args, w) -> None:
                              f"{3 * q.numel() * q.element_size() / 2**20:.0f} MiB)"},
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": float(te.item())},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e_max},
             "gpu_launches": args.steps, "clocks": clocks,
             "pct_of_peak": 100.0 * achieved / peaks["bf16"],
             "exps_per_s": w.B * w.H * w.N * w.N / (ms * 1e-3),
@@ -322,14 +335,17 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=4, help="workload key (default 4)")
+    ap.add_argument("--heads", type=int, default=None, help="override the head count")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
-    if args.warmup < 3:
-        ap.error("at least 3 warm-up steps")
+    args.warmup = max(3, args.warmup)  # timing rule: at least 3 warm-up steps
     from long_context_ra_gb300 import synth
 
     w = synth.WORKLOADS[args.workload]
+    if args.heads is not None and args.heads != w.H:
+        # a smaller case of the same workload (for profiler captures)
+        w = dataclasses.replace(w, H=args.heads, name=f"{w.name.replace(f'_H{w.H}_', f'_H{args.heads}_')}")
     if args.impl == "reference":
         run_reference(args, w)
     else:

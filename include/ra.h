@@ -32,7 +32,8 @@
  *     watchdog inside the kernels is reported by ra_last_device_status().
  *   - Arguments are validated before anything is enqueued; on any error the
  *     call returns the status and launches nothing.  No call throws.
- *   - Calls whose total row count is zero return RA_OK and launch nothing.
+ *   - Calls whose total row count is zero return RA_OK and launch nothing;
+ *     their data pointers may then be NULL (an empty tensor's address).
  *   - Element types: RA_BF16 inputs run on the tensor cores (tcgen05, fp32
  *     accumulation) and need d in {64, 128}, c % 128 == 0 and 16-byte aligned
  *     q, k, v and out.  RA_F32 inputs run on the fp32 FFMA path (no TF32) for

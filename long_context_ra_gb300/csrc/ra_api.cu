@@ -97,11 +97,11 @@ constexpr int64_t kMaxRows = (int64_t{1} << 31) - 1;  // TMA coordinates are int
 // Shared checks of the attention-shaped calls; fills the fold arguments.
 ra_status check_attention(const void* q, const void* k, const void* v, int32_t B, int32_t H,
                           int64_t N, int32_t d, int32_t P, ra_dtype dt, FoldArgs* a) {
-  if (!q || !k || !v) return RA_ERR_INVALID_ARG;
   if (B < 0 || H < 0 || N < 0 || d < 1 || P < 1) return RA_ERR_INVALID_ARG;
   if (dt != RA_F32 && dt != RA_BF16) return RA_ERR_INVALID_ARG;
-  if (N % P != 0) return RA_ERR_UNSUPPORTED;
   const int64_t rows = static_cast<int64_t>(B) * H * N;
+  if (rows != 0 && (!q || !k || !v)) return RA_ERR_INVALID_ARG;
+  if (N % P != 0) return RA_ERR_UNSUPPORTED;
   if (rows > kMaxRows) return RA_ERR_UNSUPPORTED;
   const int64_t c = N / P;
   if (dt == RA_BF16) {
@@ -141,7 +141,8 @@ ra_status run_fold(const FoldArgs& a, ra_dtype dt, cudaStream_t s) {
 }
 
 bool state_ok(const ra_state* st) {
-  return st && st->m && st->l && st->o && st->rows >= 0 && st->d >= 1;
+  // An empty state (rows == 0) may carry NULL pointers.
+  return st && st->rows >= 0 && st->d >= 1 && (st->rows == 0 || (st->m && st->l && st->o));
 }
 
 }  // namespace
@@ -164,9 +165,9 @@ RA_API ra_status ra_forward(const void* q, const void* k, const void* v, void* o
   FoldArgs a;
   ra_status st = check_attention(q, k, v, B, H, N, d, P, dtype, &a);
   if (st != RA_OK) return st;
+  if (a.slices * a.nq == 0) return RA_OK;
   if (!out || !lse) return RA_ERR_INVALID_ARG;
   if (!aligned(out, dtype == RA_BF16 ? 16 : 4) || !aligned(lse, 4)) return RA_ERR_MISALIGNED;
-  if (a.slices * a.nq == 0) return RA_OK;
   DeviceInfo di;
   if ((st = current_device(&di)) != RA_OK) return st;
   a.mode = kForward;

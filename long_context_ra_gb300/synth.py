@@ -126,11 +126,13 @@ def sample_rows(w: Workload, count: int, seed: int = 7, shape=None) -> torch.Ten
         for i in range(w.P):
             rows.append(bh * N + i * c)
             rows.append(bh * N + i * c + c - 1)
-    fixed = torch.tensor(rows, dtype=torch.int64)
+    allr = torch.unique(torch.tensor(rows, dtype=torch.int64))
     g = torch.Generator().manual_seed(seed)
-    extra = torch.randint(0, B * H * N, (max(0, count - fixed.numel()),), generator=g)
-    allr = torch.unique(torch.cat([fixed, extra]))
     if allr.numel() > count:
         keep = torch.randperm(allr.numel(), generator=g)[:count]
-        allr = torch.unique(allr[keep])
+        return torch.unique(allr[keep])
+    count = min(count, B * H * N)
+    while allr.numel() < count:
+        extra = torch.randint(0, B * H * N, (count - allr.numel(),), generator=g)
+        allr = torch.unique(torch.cat([allr, extra]))
     return allr

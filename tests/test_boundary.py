@@ -71,6 +71,8 @@ def test_empty_problem_launches_nothing(L):
     # zero rows: RA_OK without any CUDA call (no device here)
     assert fwd(L, B=0) == _native.RA_OK
     assert fwd(L, N=0, P=1) == _native.RA_OK
+    # an empty tensor's data pointer is NULL: still fine when there is no row
+    assert fwd(L, q=None, k=None, v=None, out=None, lse=None, H=0) == _native.RA_OK
 
 
 def test_valid_call_without_device_reports_arch(L):

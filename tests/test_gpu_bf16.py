@@ -157,7 +157,7 @@ def test_worked_example_embedded(O):
 
 def test_misaligned_pointer_rejected():
     x = torch.zeros(1 * 1 * 256 * 64 + 8, device=DEV, dtype=torch.bfloat16)
-    q = x[4:].view(1, 1, 256, 64)  # 8-byte offset
+    q = x[4:4 + 256 * 64].view(1, 1, 256, 64)  # 8-byte offset
     with pytest.raises(ra.RaError) as e:
         ra.ra_forward(q, q, q, P=1)
     assert e.value.code == 3

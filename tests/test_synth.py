@@ -1,0 +1,62 @@
+"""Input recipes (no GPU): seeded, shaped as stated, structure as stated."""
+import torch
+
+from long_context_ra_gb300 import synth
+
+
+def small(key, shape):
+    w = synth.WORKLOADS[key]
+    return w, synth.make_inputs(w, "cpu", shape=shape)
+
+
+def test_deterministic_and_typed():
+    w, (q, k, v) = small(4, (1, 2, 256, 128))
+    _, (q2, k2, v2) = small(4, (1, 2, 256, 128))
+    assert q.dtype == torch.bfloat16 and torch.equal(q, q2) and torch.equal(k, k2)
+    assert not torch.equal(q, k)  # separate streams
+    w1, (a, b, c) = small(1, (1, 1, 256, 64))
+    assert a.dtype == torch.float32
+
+
+def test_shift_every_4th_block():
+    w = synth.WORKLOADS[2]
+    shape = (1, 2, 1024, 64)
+    q, k, v = synth.make_inputs(w, "cpu", shape=shape)
+    c = 1024 // w.P
+    qbar = q.float().mean(dim=2)  # close to the pre-rounding mean
+    for j in range(w.P):
+        kb = k[:, :, j * c:(j + 1) * c].float().mean(dim=2)
+        shift = kb - 0.0
+        if j % 4 == 3:
+            # the block mean is pulled towards 3 * qbar
+            assert torch.cosine_similarity(shift.flatten(), qbar.flatten(), dim=0) > 0.5
+        else:
+            assert shift.abs().max() < 0.5
+
+
+def test_offset_grows_along_mean_direction():
+    w = synth.WORKLOADS[3]
+    shape = (1, 2, 2048, 128)
+    q, k, v = synth.make_inputs(w, "cpu", shape=shape)
+    c = 2048 // w.P
+    qbar = q.float().mean(dim=2)
+    u = qbar / qbar.norm(dim=-1, keepdim=True)
+    proj = [(k[:, :, j * c:(j + 1) * c].float().mean(dim=2) * u).sum(-1) for j in range(w.P)]
+    for j in range(1, w.P):
+        assert (proj[j] > proj[j - 1]).all()  # +0.25 per block along u
+    assert abs(q.float().std().item() - 2 ** -0.5) < 0.02  # N(0, 1/2)
+
+
+def test_sample_rows_cover_blocks():
+    w = synth.WORKLOADS[4]
+    rows = synth.sample_rows(w, 4096)
+    assert rows.numel() == 4096 and rows.unique().numel() == 4096
+    assert int(rows.max()) < w.rows
+    blocks = set(((rows // w.N) * w.P + (rows % w.N) // w.c).tolist())
+    assert len(blocks) == w.B * w.H * w.P  # every (b, h, query block)
+
+
+def test_workload_sizes():
+    w = synth.WORKLOADS[4]
+    assert (w.B, w.H, w.N, w.d, w.P, w.c) == (1, 8, 131072, 128, 32, 4096)
+    assert w.flops == 4.0 * 8 * 131072 ** 2 * 128
