@@ -10,25 +10,30 @@
 //   S = tau * Q K^T             tcgen05.mma, bf16 -> fp32 in TMEM
 //   m' = max(m, rowmax S)       softmax warps, registers
 //   p  = exp(S - m'), l' = alpha l + sum p
-//   O  = alpha O + p V          tcgen05.mma, p as bf16 from shared memory
+//   O  = alpha O + p V          tcgen05.mma, p as bf16 from tensor memory
 //
 // The pages' send/recv of the next block while the current one is computed
 // (section "Accumulation math, step by step") becomes a TMA prefetch of the
 // next K/V tile into a free stage of a shared-memory ring.
 //
-// Warp roles (320 threads):
-//   warps 0-3  softmax for query tile 0 (thread = row = TMEM lane)
-//   warps 4-7  softmax for query tile 1
-//   warp  8    TMA producer (one thread)
-//   warp  9    TMEM allocator and MMA issuer (one thread)
+// Warp roles (384 threads, launched at 168 registers a thread):
+//   warps 0-3   softmax for query tile 0 (thread = row = TMEM lane)
+//   warps 4-7   softmax for query tile 1
+//   warp  8     TMA producer (one thread)
+//   warp  9     TMEM allocator and MMA issuer (one thread)
+//   warps 10-11 idle (they complete the third warpgroup)
+// The third warpgroup gives registers back (setmaxnreg.dec to 72) and the two
+// softmax warpgroups take them (setmaxnreg.inc to 216): 2 x 128 x 216 +
+// 128 x 72 = 64512 = 384 x 168, the launch's register total.
 //
 // The two query tiles ping-pong: while one tile's softmax runs on the CUDA
 // cores, the tensor cores work on the other tile's products.
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D),
-// O1 [256+D, 256+2D).  Shared memory (1024-byte aligned, 128-byte swizzle
-// everywhere): Q0, Q1, kStages K/V tiles, P0, P1 (bf16 probabilities),
-// mbarriers.
+// O1 [256+D, 256+2D).  The bf16 probabilities P_t overwrite the first 64
+// columns of S_t once the softmax warps have read S_t, and feed the P V
+// product straight from TMEM.  Shared memory (1024-byte aligned, 128-byte
+// swizzle everywhere): Q0, Q1, kStages K/V tiles, mbarriers.
 //
 // The running max used for the exponentials is a per-row reference that is
 // raised only when a tile's max exceeds it by more than kRescaleLog2 (log2
@@ -52,7 +57,11 @@ using namespace ptx;
 
 constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;  // keys per K/V tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsOther = 72;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther == kThreads * 168,
+              "register split must equal the launch's register total");
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
@@ -66,14 +75,11 @@ struct Layout {
   static constexpr int kBoxBytes = kBM * 128;  // 128 rows x 128 bytes (64 bf16)
   static constexpr int kTileBytes = kBM * D * 2;
   static constexpr int kBoxes = D / 64;
-  static constexpr int kStages = D == 128 ? 3 : 4;
-  static constexpr int kPBytes = kBM * kBN * 2;
+  static constexpr int kStages = D == 128 ? 4 : 6;
   static constexpr int kQ0 = 0;
   static constexpr int kQ1 = kTileBytes;
   static constexpr int kKV = 2 * kTileBytes;
-  static constexpr int kP0 = kKV + kStages * kTileBytes;
-  static constexpr int kP1 = kP0 + kPBytes;
-  static constexpr int kBar = kP1 + kPBytes;
+  static constexpr int kBar = kKV + kStages * kTileBytes;
   // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], drain
   static constexpr int kNumBars = 1 + 2 * kStages + 7;
   static constexpr int kMisc = kBar + kNumBars * 8;  // TMEM base, abort flag
@@ -171,21 +177,20 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
   }
 }
 
-// O[tmem] (+)= P V for one tile: 8 MMAs of K = 16 keys.  P is K-major (keys
-// contiguous) like Q; V is MN-major (d contiguous): 8 keys of one 64-column
-// box form a 1024-byte swizzle atom (stride byte offset), the second box of
-// 64 columns sits one box further (leading byte offset).
+// O[tmem] (+)= P V for one tile: 8 MMAs of K = 16 keys.  P is read from TMEM
+// (packed bf16 pairs, 8 columns per 16 keys); V is MN-major (d contiguous):
+// 8 keys of one 64-column box form a 1024-byte swizzle atom (stride byte
+// offset), the second box of 64 columns sits one box further (leading byte
+// offset).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_smem, uint32_t v_smem,
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
                                          bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, true);
 #pragma unroll
   for (int kk = 0; kk < kBN / 16; ++kk) {
-    const uint32_t aoff = (kk / 4) * Layout<D>::kBoxBytes + (kk % 4) * 32;
     const uint32_t boff = kk * 16 * 128;
-    mma_bf16_ss(d_tmem, desc_sw128(p_smem + aoff, 16, 1024),
-                desc_sw128(v_smem + boff, Layout<D>::kBoxBytes, 1024), idesc,
-                (accumulate || kk > 0) ? 1u : 0u);
+    mma_bf16_ts(d_tmem, p_tmem + kk * 8, desc_sw128(v_smem + boff, Layout<D>::kBoxBytes, 1024),
+                idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -259,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kLoadWarp) {
     // ================= TMA producer =================
+    setmaxnreg_dec<kRegsOther>();
     if (lane == 0) {
       const uint32_t qbytes = (has_t1 ? 2u : 1u) * L::kTileBytes;
       mbar_arrive_expect_tx(bars.q_full(), qbytes);
@@ -304,11 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ================= MMA issuer =================
+    setmaxnreg_dec<kRegsOther>();
     if (lane == 0) {
       const uint32_t tS0 = tmem, tS1 = tmem + 128;
       const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
       const uint32_t sQ0 = base + L::kQ0, sQ1 = base + L::kQ1;
-      const uint32_t sP0 = base + L::kP0, sP1 = base + L::kP1;
       const bool from_state = a.mode == kFold;
       bool ok = wait1(bars.q_full(), 0, ab);
       int cons = 0;  // K/V tiles consumed so far
@@ -339,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const bool acc = it > 0 || from_state;
-        issue_pv<D>(tO0, sP0, sVaddr, acc);
+        issue_pv<D>(tO0, tS0, sVaddr, acc);
         const bool more = it + 1 < n_iter;
         uint32_t sKaddr = 0;
         int sK = 0;
@@ -361,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          issue_pv<D>(tO1, sP1, sVaddr, acc);
+          issue_pv<D>(tO1, tS1, sVaddr, acc);
         }
         mma_commit(bars.kv_empty(sV));
         if (more) {
@@ -381,8 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_drain(bars.drain(), 0);
       }
     }
-  } else {
+  } else if (warp < kLoadWarp) {
     // ================= softmax warps =================
+    setmaxnreg_inc<kRegsSoftmax>();
     const int t = warp / 4;   // query tile
     const int wq = warp % 4;  // TMEM lane quarter of this warp
     if (t == 0 || has_t1) {
@@ -390,7 +397,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
       const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(t * 128);
       const uint32_t tO = tmem + lane_off + 256u + static_cast<uint32_t>(t * D);
-      const uint32_t sP = base + (t == 0 ? L::kP0 : L::kP1);
       const int64_t grow = q_row0 + t * kBM + row;  // global query row
       const float sl2 = a.scale_log2;
 
@@ -433,10 +439,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         reg_fence(s, kBN);
 
-        float mx = __uint_as_float(s[0]);
+        // Row max: eight independent chains of three-input maxima.
+        float mx[8];
 #pragma unroll
-        for (int j = 1; j < kBN; ++j) mx = fmaxf(mx, __uint_as_float(s[j]));
-        const float m_new = mx * sl2;
+        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(__uint_as_float(s[e]), __uint_as_float(s[e + 8]));
+#pragma unroll
+        for (int j = 16; j < kBN; j += 16) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            mx[e] = fmax3(mx[e], __uint_as_float(s[j + e]), __uint_as_float(s[j + 8 + e]));
+        }
+        const float rmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                 fmaxf(mx[6], mx[7]));
+        const float m_new = rmax * sl2;
         m_true = fmaxf(m_true, m_new);
         const bool need = m_new > m_ref + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
@@ -460,25 +475,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 
-        // p = exp2(s * tau * log2(e) - m_ref), rounded to bf16 and written
-        // to P in the 128-byte-swizzled K-major layout the MMA reads.
-        const float neg = -m_ref;
-        const uint32_t rbase = sP + static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128);
-        float lsum = 0.f;
+        // p = exp2(s * tau * log2(e) - m_ref), two scores per FMA; the row
+        // sum runs in four independent pairs.  p is rounded to bf16 pairs and
+        // written over the first 64 columns of S, where the P V product reads
+        // it.
+        const uint64_t scale2 = pack_f32x2(sl2, sl2);
+        const uint64_t neg2 = pack_f32x2(-m_ref, -m_ref);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-        for (int kc = 0; kc < kBN / 8; ++kc) {
-          float p[8];
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) p[e] = ex2(fmaf(__uint_as_float(s[kc * 8 + e]), sl2, neg));
-#pragma unroll
-          for (int e = 0; e < 8; ++e) lsum += p[e];
-          const uint32_t addr = rbase + static_cast<uint32_t>((kc >> 3) * L::kBoxBytes) +
-                                (static_cast<uint32_t>((kc & 7) ^ (row & 7)) << 4);
-          st_shared_v4(addr, pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]),
-                       pack_bf16x2(p[4], p[5]), pack_bf16x2(p[6], p[7]));
+          for (int jj = 0; jj < 32; ++jj) {
+            const int j = half * 64 + 2 * jj;
+            const uint64_t x = fma_f32x2(
+                pack_f32x2(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), scale2, neg2);
+            float x0, x1;
+            unpack_f32x2(x, x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            acc[jj & 3] = add_f32x2(acc[jj & 3], pack_f32x2(p0, p1));
+            pk[jj] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tS + static_cast<uint32_t>(half * 32), pk);
         }
-        l += lsum;
-        fence_proxy_async_smem();
+        float a0, a1, a2, a3, a4, a5, a6, a7;
+        unpack_f32x2(acc[0], a0, a1);
+        unpack_f32x2(acc[1], a2, a3);
+        unpack_f32x2(acc[2], a4, a5);
+        unpack_f32x2(acc[3], a6, a7);
+        l += ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
+        tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bars.p_full(t));
         o_valid = true;
@@ -531,6 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+  } else {
+    setmaxnreg_dec<kRegsOther>();  // idle warps of the third warpgroup
   }
 
   // ---- teardown ----
