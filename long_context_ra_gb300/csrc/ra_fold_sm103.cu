@@ -22,9 +22,9 @@
 //   warp  8     TMA producer (one thread)
 //   warp  9     TMEM allocator and MMA issuer (one thread)
 //   warps 10-11 idle (they complete the third warpgroup)
-// The third warpgroup gives registers back (setmaxnreg.dec to 72) and the two
-// softmax warpgroups take them (setmaxnreg.inc to 216): 2 x 128 x 216 +
-// 128 x 72 = 64512 = 384 x 168, the launch's register total.
+// The third warpgroup gives registers back (setmaxnreg.dec to 88) and the two
+// softmax warpgroups take them (setmaxnreg.inc to 208): 2 x 128 x 208 +
+// 128 x 88 = 64512 = 384 x 168, the launch's register total.
 //
 // The two query tiles ping-pong: while one tile's softmax runs on the CUDA
 // cores, the tensor cores work on the other tile's products.
@@ -58,8 +58,8 @@ using namespace ptx;
 constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kThreads = 384;
-constexpr uint32_t kRegsSoftmax = 216;
-constexpr uint32_t kRegsOther = 72;
+constexpr uint32_t kRegsSoftmax = 208;
+constexpr uint32_t kRegsOther = 88;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther == kThreads * 168,
               "register split must equal the launch's register total");
 constexpr int kLoadWarp = 8;
@@ -163,17 +163,22 @@ struct KvWalk {
   }
 };
 
+// The MMA thread builds each operand's shared-memory descriptor once and
+// moves it by adding (byte offset >> 4) to its start-address field; every
+// address here stays below 2^18 bytes, so the 14-bit field never carries.
+__device__ __forceinline__ constexpr uint64_t desc_step(uint32_t bytes) { return bytes >> 4; }
+
 // S[tmem] = Q K^T for one 128x128 tile: D/16 MMAs of K = 16 along d.  Q and K
 // are K-major (d contiguous) in 128-byte-swizzled boxes of 64 columns; the
 // k-th slice of 16 columns starts 32 bytes further inside its box.
+// dq, dk: descriptors of the Q and K tiles (leading offset 16, stride 1024).
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dq, uint64_t dk) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk / 4) * Layout<D>::kBoxBytes + (kk % 4) * 32;
-    mma_bf16_ss(d_tmem, desc_sw128(q_smem + off, 16, 1024), desc_sw128(k_smem + off, 16, 1024),
-                idesc, kk > 0 ? 1u : 0u);
+    const uint64_t off = desc_step((kk / 4) * Layout<D>::kBoxBytes + (kk % 4) * 32);
+    mma_bf16_ss(d_tmem, dq + off, dk + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -182,16 +187,15 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
 // 8 keys of one 64-column box form a 1024-byte swizzle atom (stride byte
 // offset), the second box of 64 columns sits one box further (leading byte
 // offset).
+// dv: descriptor of the V tile (leading offset = one box, stride 1024).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
-                                         bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t dv,
+                                         uint32_t accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, true);
+  mma_bf16_ts(d_tmem, p_tmem, dv, idesc, accumulate);
 #pragma unroll
-  for (int kk = 0; kk < kBN / 16; ++kk) {
-    const uint32_t boff = kk * 16 * 128;
-    mma_bf16_ts(d_tmem, p_tmem + kk * 8, desc_sw128(v_smem + boff, Layout<D>::kBoxBytes, 1024),
-                idesc, (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 1; kk < kBN / 16; ++kk)
+    mma_bf16_ts(d_tmem, p_tmem + kk * 8, dv + desc_step(kk * 16 * 128), idesc, 1u);
 }
 
 template <int D>
@@ -314,7 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t tS0 = tmem, tS1 = tmem + 128;
       const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
-      const uint32_t sQ0 = base + L::kQ0, sQ1 = base + L::kQ1;
+      const uint64_t dQ0 = desc_sw128(base + L::kQ0, 16, 1024);
+      const uint64_t dQ1 = desc_sw128(base + L::kQ1, 16, 1024);
+      const uint64_t dK = desc_sw128(base + L::kKV, 16, 1024);  // stage 0, K-major
+      const uint64_t dV = desc_sw128(base + L::kKV, L::kBoxBytes, 1024);  // stage 0, MN-major
       const bool from_state = a.mode == kFold;
       bool ok = wait1(bars.q_full(), 0, ab);
       int cons = 0;  // K/V tiles consumed so far
@@ -322,10 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         tc_fence_after();
         cons = 1;
-        issue_qk<D>(tS0, sQ0, base + L::kKV);
+        issue_qk<D>(tS0, dQ0, dK);
         mma_commit(bars.s_full(0));
         if (has_t1) {
-          issue_qk<D>(tS1, sQ1, base + L::kKV);
+          issue_qk<D>(tS1, dQ1, dK);
           mma_commit(bars.s_full(1));
         }
         mma_commit(bars.kv_empty(0));
@@ -338,16 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ++cons;
-        const uint32_t sVaddr = base + L::kKV + sV * L::kTileBytes;
+        const uint64_t dVs = dV + desc_step(sV * L::kTileBytes);
         if (!wait1(bars.p_full(0), par, ab)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const bool acc = it > 0 || from_state;
-        issue_pv<D>(tO0, tS0, sVaddr, acc);
+        const uint32_t acc = (it > 0 || from_state) ? 1u : 0u;
+        issue_pv<D>(tO0, tS0, dVs, acc);
         const bool more = it + 1 < n_iter;
-        uint32_t sKaddr = 0;
+        uint64_t dKs = 0;
         int sK = 0;
         if (more) {
           sK = cons % L::kStages;
@@ -357,8 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++cons;
           tc_fence_after();
-          sKaddr = base + L::kKV + sK * L::kTileBytes;
-          issue_qk<D>(tS0, sQ0, sKaddr);
+          dKs = dK + desc_step(sK * L::kTileBytes);
+          issue_qk<D>(tS0, dQ0, dKs);
           mma_commit(bars.s_full(0));
         }
         if (has_t1) {
@@ -367,12 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          issue_pv<D>(tO1, tS1, sVaddr, acc);
+          issue_pv<D>(tO1, tS1, dVs, acc);
         }
         mma_commit(bars.kv_empty(sV));
         if (more) {
           if (has_t1) {
-            issue_qk<D>(tS1, sQ1, sKaddr);
+            issue_qk<D>(tS1, dQ1, dKs);
             mma_commit(bars.s_full(1));
           }
           mma_commit(bars.kv_empty(sK));
