@@ -17,7 +17,8 @@
 //       (partial results merged into one output).
 //   [C] "Ring attention, explained" (vibeengines.com): steps 1-4 (shard,
 //       local block first, rotate, normalise; equals full attention up to
-//       rounding).
+//       rounding) and "The causal-mask catch" (a query needs only keys at or
+//       before it; striped and zigzag assignments of tokens to devices).
 //
 // Readings where the pages are silent (each also listed in the design notes):
 //   R1  lse = m + ln l over the scaled scores tau*q.k (natural log).
@@ -29,6 +30,12 @@
 //       read per query row as in [A].
 //   R4  N = tokens, P = devices/blocks, c = N / P ([A], [C]), not [B]'s use of
 //       N for the block count.
+//   R12 Causal: query at position n sees key positions <= n.  Layouts of the
+//       tokens over the P blocks: contiguous (block j = positions j*c ..
+//       j*c + c - 1), zigzag (block j = chunk j and chunk 2P-1-j of 2P chunks
+//       of c/2 positions, each in increasing order) and striped (block j =
+//       positions j, j + P, j + 2P, ...).  A block's keys are folded in this
+//       local order; masked keys take no part (as a score of -inf would).
 //
 // Every value is computed in double precision.  Inputs are converted exactly
 // (f32 -> f64 and bf16 -> f64 are exact).  No blocking, fusion or reordering
@@ -52,6 +59,7 @@
 namespace {
 
 enum { ORA_F64 = 0, ORA_F32 = 1, ORA_BF16 = 2 };
+enum { ORA_CONTIGUOUS = 0, ORA_ZIGZAG = 1, ORA_STRIPED = 2 };
 
 const double kNegInf = -std::numeric_limits<double>::infinity();
 
@@ -108,21 +116,31 @@ struct RowState {
   std::vector<double> o;  // running sum of exp(s - m) * v, length d
 };
 
-// One fold of keys [j0, j1) of a [*, d] K/V array into `st` for query `q`
-// (already converted to double).  This is the update of [A] "For each
-// incoming K/V block":
+// One fold of the keys `rows[0..nb)` (row indices of a [*, d] K/V array)
+// into `st` for query `q` (already converted to double).  This is the update
+// of [A] "For each incoming K/V block":
 //   s_j = q . k_j * tau;  m' = max(m, max_j s_j);  alpha = exp(m - m');
 //   l' = alpha*l + sum_j exp(s_j - m');  o' = alpha*o + sum_j exp(s_j - m') v_j.
+// Causal (R12): when `pos` is given, key j takes part only if pos[j] <= qpos.
 void fold_keys(RowState& st, const double* q, int d, double tau,
-               const void* k, const void* v, int dtype, int64_t j0, int64_t j1,
-               std::vector<double>& s, std::vector<double>& krow,
-               std::vector<double>& vrow) {
-  if (j1 <= j0) return;
-  const int64_t nb = j1 - j0;
+               const void* k, const void* v, int dtype, const int64_t* rows, int64_t nb,
+               const int64_t* pos, int64_t qpos, std::vector<double>& s,
+               std::vector<double>& krow, std::vector<double>& vrow) {
+  std::vector<int64_t> keep;
+  keep.reserve(static_cast<size_t>(nb));
+  for (int64_t j = 0; j < nb; ++j) {
+#if ORA_MUTANT == 7
+    if (!pos || pos[j] < qpos) keep.push_back(rows[j]);  // planted: strict mask
+#else
+    if (!pos || pos[j] <= qpos) keep.push_back(rows[j]);
+#endif
+  }
+  nb = static_cast<int64_t>(keep.size());
+  if (nb == 0) return;  // R2: a fully masked block adds nothing
   s.resize(static_cast<size_t>(nb));
   double bmax = kNegInf;
   for (int64_t j = 0; j < nb; ++j) {
-    load_row(k, dtype, j0 + j, d, krow.data());
+    load_row(k, dtype, keep[j], d, krow.data());
     double dot = 0.0;
     for (int e = 0; e < d; ++e) dot += q[e] * krow[e];
 #if ORA_MUTANT == 4
@@ -157,9 +175,9 @@ void fold_keys(RowState& st, const double* q, int d, double tau,
 #endif
     lsum += p;
 #if ORA_MUTANT == 6
-    load_row(k, dtype, j0 + j, d, vrow.data());  // planted: K used as V
+    load_row(k, dtype, keep[j], d, vrow.data());  // planted: K used as V
 #else
-    load_row(v, dtype, j0 + j, d, vrow.data());
+    load_row(v, dtype, keep[j], d, vrow.data());
 #endif
     for (int e = 0; e < d; ++e) st.o[e] += p * vrow[e];
   }
@@ -173,6 +191,27 @@ inline int64_t ring_block(int64_t i, int64_t t, int64_t P) {
   int64_t j = (i - t) % P;
   if (j < 0) j += P;
   return j;
+}
+
+// Position of local row r of block j (R12; [A] "Sharding the sequence" for
+// the contiguous split, [C] "The causal-mask catch" for zigzag and striped).
+inline int64_t token_pos(int layout, int64_t j, int64_t r, int64_t P, int64_t c) {
+  if (layout == ORA_ZIGZAG) {
+    const int64_t h = c / 2;
+    return r < h ? j * h + r : (2 * P - 1 - j) * h + (r - h);
+  }
+  if (layout == ORA_STRIPED) return j + P * r;
+  return j * c + r;
+}
+
+// Block holding position n (inverse of token_pos).
+inline int64_t block_of(int layout, int64_t n, int64_t P, int64_t c) {
+  if (layout == ORA_ZIGZAG) {
+    const int64_t chunk = n / (c / 2);
+    return chunk < P ? chunk : 2 * P - 1 - chunk;
+  }
+  if (layout == ORA_STRIPED) return n % P;
+  return n / c;
 }
 
 // Final normalisation out = o / l ([A] "After the final block") and R1.
@@ -202,11 +241,12 @@ int ora_ring_order(int64_t P, int64_t* order) {
 // device runs out of room": S = QK^T / sqrt(d_k), and the softmax identity).
 //   q, k, v: [BH, N, d] of `dtype`.
 //   rows: R flat indices into [BH*N] (NULL means every row, R = BH*N).
+//   causal != 0: the query at position n sees keys 0 .. n only (R12).
 //   out: [R, d] doubles; lse: [R] doubles.
-// For each row: s_j = tau q.k_j over all N keys of its (b,h); M = max s;
+// For each row: s_j = tau q.k_j over its (b,h)'s visible keys; M = max s;
 // L = sum exp(s - M); out = sum exp(s - M) v / L; lse = M + ln L.
 int ora_dense(const void* q, const void* k, const void* v, int dtype, int64_t BH,
-              int64_t N, int d, const int64_t* rows, int64_t R, double* out,
+              int64_t N, int d, int causal, const int64_t* rows, int64_t R, double* out,
               double* lse, int threads) {
   if (!q || !k || !v || !out || !lse || BH < 0 || N < 0 || d < 1 || bad_dtype(dtype))
     return 1;
@@ -215,10 +255,11 @@ int ora_dense(const void* q, const void* k, const void* v, int dtype, int64_t BH
   parallel_for(R, threads, [&](int64_t ri) {
     const int64_t r = rows ? rows[ri] : ri;
     const int64_t bh = r / N;
+    const int64_t nk = causal ? r % N + 1 : N;  // visible keys 0 .. nk-1
     std::vector<double> qrow(d), krow(d), vrow(d), s(static_cast<size_t>(N));
     load_row(q, dtype, r, d, qrow.data());
     double M = kNegInf;
-    for (int64_t j = 0; j < N; ++j) {
+    for (int64_t j = 0; j < nk; ++j) {
       load_row(k, dtype, bh * N + j, d, krow.data());
       double dot = 0.0;
       for (int e = 0; e < d; ++e) dot += qrow[e] * krow[e];
@@ -227,7 +268,7 @@ int ora_dense(const void* q, const void* k, const void* v, int dtype, int64_t BH
     }
     double L = 0.0;
     std::vector<double> acc(d, 0.0);
-    for (int64_t j = 0; j < N; ++j) {
+    for (int64_t j = 0; j < nk; ++j) {
       const double p = std::exp(s[j] - M);
       L += p;
       load_row(v, dtype, bh * N + j, d, vrow.data());
@@ -240,31 +281,38 @@ int ora_dense(const void* q, const void* k, const void* v, int dtype, int64_t BH
 }
 
 // Ring-order recurrence ([A] "Accumulation math, step by step").
-//   P blocks of c = N / P contiguous rows; query row n lives in block i = n / c.
-//   Steps t in [t0, t1) are folded, visiting block order[i*P + t] (NULL means
-//   the ring order (i - t) mod P).  t0 = 0, t1 = P is the whole ring.
-//   tile > 0 folds each visiting block in consecutive key chunks of `tile`
-//   keys instead of whole (exact by the same identity); 0 folds whole blocks.
+//   P blocks of c = N / P rows; `layout` (R12) says which positions form a
+//   block (0 contiguous, 1 zigzag, 2 striped); query position n lives in block
+//   i = block_of(n).  Steps t in [t0, t1) are folded, visiting block
+//   order[i*P + t] (NULL means the ring order (i - t) mod P).  t0 = 0, t1 = P
+//   is the whole ring.
+//   tile > 0 folds each visiting block in consecutive chunks of `tile` keys
+//   (local order) instead of whole (exact by the same identity).
+//   causal != 0 masks keys at positions after the query (R12).
 //   The state starts at (m = -inf, l = 0, o = 0).
 //   Outputs (any may be NULL): out [R, d] = o / l, lse [R] = m + ln l, and the
 //   raw final state m_out [R], l_out [R], o_out [R, d].
 int ora_ring(const void* q, const void* k, const void* v, int dtype, int64_t BH,
              int64_t N, int d, int64_t P, const int64_t* order, int64_t t0,
-             int64_t t1, int64_t tile, const int64_t* rows, int64_t R,
-             double* out, double* lse, double* m_out, double* l_out,
+             int64_t t1, int64_t tile, int causal, int layout, const int64_t* rows,
+             int64_t R, double* out, double* lse, double* m_out, double* l_out,
              double* o_out, int threads) {
   if (!q || !k || !v || BH < 0 || N < 0 || d < 1 || P < 1 || bad_dtype(dtype)) return 1;
+  if (layout < ORA_CONTIGUOUS || layout > ORA_STRIPED) return 1;
   if (N % P != 0) return 2;
+  if (layout == ORA_ZIGZAG && (N / P) % 2 != 0) return 2;
   if (t0 < 0 || t1 > P || t0 > t1 || tile < 0) return 1;
   if (!rows) R = BH * N;
   const int64_t c = N / P;
   const double tau = 1.0 / std::sqrt(static_cast<double>(d));
   parallel_for(R, threads, [&](int64_t ri) {
     const int64_t r = rows ? rows[ri] : ri;
-    const int64_t bh = r / N, n = r % N, i = n / c;
+    const int64_t bh = r / N, n = r % N, i = block_of(layout, n, P, c);
     std::vector<double> qrow(d), krow(d), vrow(d), s;
+    std::vector<int64_t> krows(static_cast<size_t>(c)), kpos(static_cast<size_t>(c));
     load_row(q, dtype, r, d, qrow.data());
     RowState st{kNegInf, 0.0, std::vector<double>(d, 0.0)};
+    const int64_t* mask = causal ? kpos.data() : nullptr;
 #if ORA_MUTANT == 3
     // planted: [A]'s warning -- normalise each block, then average them.
     std::vector<double> avg(d, 0.0);
@@ -272,22 +320,24 @@ int ora_ring(const void* q, const void* k, const void* v, int dtype, int64_t BH,
 #endif
     for (int64_t t = t0; t < t1; ++t) {
       const int64_t j = order ? order[i * P + t] : ring_block(i, t, P);
-      const int64_t base = bh * N + j * c;
+      for (int64_t x = 0; x < c; ++x) {
+        kpos[x] = token_pos(layout, j, x, P, c);
+        krows[x] = bh * N + kpos[x];
+      }
 #if ORA_MUTANT == 3
       RowState b{kNegInf, 0.0, std::vector<double>(d, 0.0)};
-      fold_keys(b, qrow.data(), d, tau, k, v, dtype, base, base + c, s, krow, vrow);
-      for (int e = 0; e < d; ++e) avg[e] += b.o[e] / b.l;
-      ++nblk;
-      fold_keys(st, qrow.data(), d, tau, k, v, dtype, base, base + c, s, krow, vrow);
+      fold_keys(b, qrow.data(), d, tau, k, v, dtype, krows.data(), c, mask, n, s, krow, vrow);
+      if (b.l > 0.0) {
+        for (int e = 0; e < d; ++e) avg[e] += b.o[e] / b.l;
+        ++nblk;
+      }
+      fold_keys(st, qrow.data(), d, tau, k, v, dtype, krows.data(), c, mask, n, s, krow, vrow);
 #else
-      if (tile == 0) {
-        fold_keys(st, qrow.data(), d, tau, k, v, dtype, base, base + c, s, krow, vrow);
-      } else {
-        for (int64_t j0 = 0; j0 < c; j0 += tile) {
-          const int64_t j1 = j0 + tile < c ? j0 + tile : c;
-          fold_keys(st, qrow.data(), d, tau, k, v, dtype, base + j0, base + j1, s,
-                    krow, vrow);
-        }
+      const int64_t step = tile == 0 ? c : tile;
+      for (int64_t x0 = 0; x0 < c; x0 += step) {
+        const int64_t nb = x0 + step < c ? step : c - x0;
+        fold_keys(st, qrow.data(), d, tau, k, v, dtype, krows.data() + x0, nb,
+                  mask ? mask + x0 : nullptr, n, s, krow, vrow);
       }
 #endif
     }
@@ -302,6 +352,16 @@ int ora_ring(const void* q, const void* k, const void* v, int dtype, int64_t BH,
     if (o_out)
       for (int e = 0; e < d; ++e) o_out[ri * d + e] = st.o[e];
   });
+  return 0;
+}
+
+// Positions held by each block under a layout (R12): pos[j*c + r] = position
+// of local row r of block j.
+int ora_layout_positions(int layout, int64_t P, int64_t c, int64_t* pos) {
+  if (!pos || P < 1 || c < 0 || layout < ORA_CONTIGUOUS || layout > ORA_STRIPED) return 1;
+  if (layout == ORA_ZIGZAG && c % 2 != 0) return 2;
+  for (int64_t j = 0; j < P; ++j)
+    for (int64_t r = 0; r < c; ++r) pos[j * c + r] = token_pos(layout, j, r, P, c);
   return 0;
 }
 
@@ -324,7 +384,10 @@ int ora_fold(double* m, double* l, double* o, const void* q, const void* kb,
     std::vector<double> qrow(d), krow(d), vrow(d), s;
     load_row(q, dtype, r, d, qrow.data());
     RowState st{m[r], l[r], std::vector<double>(o + r * d, o + (r + 1) * d)};
-    fold_keys(st, qrow.data(), d, tau, kb, vb, dtype, b * Nk, (b + 1) * Nk, s, krow, vrow);
+    std::vector<int64_t> krows(static_cast<size_t>(Nk));
+    for (int64_t x = 0; x < Nk; ++x) krows[x] = b * Nk + x;
+    fold_keys(st, qrow.data(), d, tau, kb, vb, dtype, krows.data(), Nk, nullptr, 0, s, krow,
+              vrow);
     m[r] = st.m;
     l[r] = st.l;
     for (int e = 0; e < d; ++e) o[r * d + e] = st.o[e];

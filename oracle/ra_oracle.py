@@ -20,6 +20,7 @@ HERE = Path(__file__).resolve().parent
 SRC = HERE / "ra_oracle.cpp"
 
 _DTYPES = {"f64": 0, "f32": 1, "bf16": 2}
+LAYOUTS = {"contiguous": 0, "zigzag": 1, "striped": 2}
 _NP = {"f64": np.float64, "f32": np.float32, "bf16": np.uint16}
 
 _P = ctypes.c_void_p
@@ -60,12 +61,14 @@ class Oracle:
         self.threads = threads or default_threads()
         L = self.lib
         L.ora_ring_order.argtypes = [_I64, _P]
-        L.ora_dense.argtypes = [_P, _P, _P, _I32, _I64, _I64, _I32, _P, _I64, _P, _P, _I32]
+        L.ora_dense.argtypes = [_P, _P, _P, _I32, _I64, _I64, _I32, _I32, _P, _I64, _P, _P, _I32]
         L.ora_ring.argtypes = [_P, _P, _P, _I32, _I64, _I64, _I32, _I64, _P, _I64, _I64,
-                               _I64, _P, _I64, _P, _P, _P, _P, _P, _I32]
+                               _I64, _I32, _I32, _P, _I64, _P, _P, _P, _P, _P, _I32]
+        L.ora_layout_positions.argtypes = [_I32, _I64, _I64, _P]
         L.ora_fold.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I32, _I32]
         L.ora_merge.argtypes = [_P, _P, _P, _I64, _I64, _I32, _P, _P, _P, _P, _P]
-        for f in (L.ora_ring_order, L.ora_dense, L.ora_ring, L.ora_fold, L.ora_merge):
+        for f in (L.ora_ring_order, L.ora_dense, L.ora_ring, L.ora_fold, L.ora_merge,
+                  L.ora_layout_positions):
             f.restype = _I32
         L.ora_mutant.restype = _I32
         self.mutant = L.ora_mutant()
@@ -94,7 +97,14 @@ class Oracle:
         self._check(self.lib.ora_ring_order(P, out.ctypes.data), "ring_order")
         return out
 
-    def dense(self, q, k, v, dtype="f64", rows=None):
+    def layout_positions(self, layout: str, P: int, c: int) -> np.ndarray:
+        """[P, c]: position of local row r of block j under `layout`."""
+        out = np.zeros((P, c), dtype=np.int64)
+        self._check(self.lib.ora_layout_positions(LAYOUTS[layout], P, c, out.ctypes.data),
+                    "layout_positions")
+        return out
+
+    def dense(self, q, k, v, dtype="f64", rows=None, causal=False):
         """q, k, v: [BH, N, d].  Returns out [R, d], lse [R] (float64)."""
         BH, N, d = q.shape
         qa, qp = self._arr(q, dtype)
@@ -105,12 +115,12 @@ class Oracle:
             R = BH * N
         out = np.empty((R, d), np.float64)
         lse = np.empty((R,), np.float64)
-        self._check(self.lib.ora_dense(qp, kp, vp, _DTYPES[dtype], BH, N, d, rp, R,
+        self._check(self.lib.ora_dense(qp, kp, vp, _DTYPES[dtype], BH, N, d, int(causal), rp, R,
                                        out.ctypes.data, lse.ctypes.data, self.threads), "dense")
         return out, lse
 
     def ring(self, q, k, v, P, dtype="f64", order=None, t0=0, t1=None, tile=0, rows=None,
-             state=False):
+             state=False, causal=False, layout="contiguous"):
         """Ring recurrence over steps [t0, t1) of the visiting order.
 
         Returns (out, lse) or, with ``state=True``, (out, lse, m, l, o)."""
@@ -132,7 +142,8 @@ class Oracle:
         m = np.empty((R,), np.float64)
         l = np.empty((R,), np.float64)
         o = np.empty((R, d), np.float64)
-        rc = self.lib.ora_ring(qp, kp, vp, _DTYPES[dtype], BH, N, d, P, op, t0, t1, tile, rp, R,
+        rc = self.lib.ora_ring(qp, kp, vp, _DTYPES[dtype], BH, N, d, P, op, t0, t1, tile,
+                               int(causal), LAYOUTS[layout], rp, R,
                                out.ctypes.data, lse.ctypes.data, m.ctypes.data, l.ctypes.data,
                                o.ctypes.data, self.threads)
         self._check(rc, "ring")

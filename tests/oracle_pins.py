@@ -53,10 +53,13 @@ def _rand(rng, BH, N, d, scale=1.0):
             rng.standard_normal((BH, N, d)))
 
 
-def _lib_reference(q, k, v):
+def _lib_reference(q, k, v, causal=False):
     """Dense attention from numpy matmul + scipy softmax/logsumexp."""
     d = q.shape[-1]
     s = np.einsum("bnd,bmd->bnm", q, k) / math.sqrt(d)
+    if causal:
+        n = s.shape[-1]
+        s = np.where(np.tril(np.ones((n, n), dtype=bool)), s, -np.inf)
     out = np.einsum("bnm,bmd->bnd", softmax(s, axis=-1), v)
     return out.reshape(-1, d), logsumexp(s, axis=-1).reshape(-1)
 
@@ -362,6 +365,99 @@ def pin_row_subset(O):
     assert np.array_equal(out_s, out[rows]) and np.array_equal(lse_s, lse[rows])
     outd, lsed = O.dense(q, k, v, rows=rows)
     assert np.abs(outd - out[rows]).max() <= 1e-12
+
+
+# ---------------------------------------------------------------------------
+# causal mask and layouts ("Ring attention, explained", "The causal-mask
+# catch"; "Ring Attention: the math", "Causal masking, load balance, and other
+# wrinkles")
+# ---------------------------------------------------------------------------
+LAYOUTS = ("contiguous", "zigzag", "striped")
+
+
+def pin_layout_tables(O):
+    g = json.loads((GOLDEN / "layouts_p4_c4.json").read_text())
+    for name in LAYOUTS:
+        assert (O.layout_positions(name, g["P"], g["c"]) == np.array(g[name])).all(), name
+    for name in LAYOUTS:  # every layout is a permutation of the positions
+        for P, c in ((3, 6), (8, 4), (5, 2)):
+            pos = O.layout_positions(name, P, c)
+            assert sorted(pos.ravel().tolist()) == list(range(P * c))
+
+
+def pin_zigzag_balances_causal_work(O):
+    """Visible (query, key) pairs per device: equal under zigzag, within c of
+    each other under striped, growing with the device under contiguous."""
+    P, c = 8, 6
+    work = {}
+    for name in LAYOUTS:
+        pos = O.layout_positions(name, P, c)
+        work[name] = [int(sum(p + 1 for p in pos[j])) for j in range(P)]  # keys 0..p
+    assert len(set(work["zigzag"])) == 1
+    assert max(work["striped"]) - min(work["striped"]) == c * (P - 1)
+    assert all(a < b for a, b in zip(work["contiguous"], work["contiguous"][1:]))
+    assert sum(work["zigzag"]) == sum(work["contiguous"]) == P * c * (P * c + 1) // 2
+
+
+def pin_causal_library_reference(O):
+    rng = np.random.default_rng(20)
+    for BH, N, d, P in ((1, 16, 4, 4), (2, 24, 3, 6), (1, 12, 5, 2)):
+        q, k, v = _rand(rng, BH, N, d, 1.5)
+        want_out, want_lse = _lib_reference(q, k, v, causal=True)
+        out_d, lse_d = O.dense(q, k, v, causal=True)
+        assert np.abs(out_d - want_out).max() <= 1e-12
+        assert np.abs(lse_d - want_lse).max() <= 1e-12
+        for layout in LAYOUTS:
+            for PP in (1, P):
+                out, lse = O.ring(q, k, v, P=PP, causal=True, layout=layout)
+                assert np.abs(out - want_out).max() <= 1e-12, (layout, PP)
+                assert np.abs(lse - want_lse).max() <= 1e-12, (layout, PP)
+
+
+def pin_causal_first_token(O):
+    """Position 0 sees only itself: out = v_0, lse = tau q_0 . k_0."""
+    rng = np.random.default_rng(21)
+    BH, N, d = 2, 8, 4
+    q, k, v = _rand(rng, BH, N, d, 2.0)
+    for layout in LAYOUTS:
+        out, lse = O.ring(q, k, v, P=4, causal=True, layout=layout, rows=[0, N])
+        for b, r in enumerate((0, N)):
+            assert np.abs(out[b] - v[b, 0]).max() <= 1e-12
+            assert abs(lse[b] - q[b, 0] @ k[b, 0] / math.sqrt(d)) <= 1e-12
+
+
+def pin_causal_identical_keys(O):
+    """Identical keys: position n averages v_0..v_n; lse = tau q.k + ln(n + 1)."""
+    rng = np.random.default_rng(22)
+    BH, N, d = 1, 12, 3
+    q = rng.standard_normal((BH, N, d))
+    k = np.broadcast_to(rng.standard_normal((BH, 1, d)), (BH, N, d)).copy()
+    v = rng.standard_normal((BH, N, d))
+    want = np.cumsum(v[0], axis=0) / np.arange(1, N + 1)[:, None]
+    want_lse = q[0] @ k[0, 0] / math.sqrt(d) + np.log(np.arange(1, N + 1))
+    for layout in LAYOUTS:
+        out, lse = O.ring(q, k, v, P=3 if layout != "zigzag" else 2, causal=True, layout=layout)
+        assert np.abs(out - want).max() <= 1e-12, layout
+        assert np.abs(lse - want_lse).max() <= 1e-12, layout
+
+
+def pin_causal_segments_merge(O):
+    """Ring segments under the mask (some fully masked, hence empty) merge back
+    to the whole causal ring."""
+    rng = np.random.default_rng(23)
+    BH, N, d, P = 1, 16, 4, 4
+    q, k, v = _rand(rng, BH, N, d, 2.0)
+    for layout in LAYOUTS:
+        full_out, full_lse = O.ring(q, k, v, P=P, causal=True, layout=layout)
+        ms, ls, os_ = [], [], []
+        for g in range(P):
+            _, _, m, l, o = O.ring(q, k, v, P=P, t0=g, t1=g + 1, causal=True, layout=layout,
+                                   state=True)
+            ms.append(m), ls.append(l), os_.append(o)
+        assert np.isneginf(np.stack(ms)).any()  # some segments see only future keys
+        out, lse = O.merge(np.stack(ms), np.stack(ls), np.stack(os_))
+        assert np.abs(out - full_out).max() <= 1e-12
+        assert np.abs(lse - full_lse).max() <= 1e-12
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
