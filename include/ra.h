@@ -71,6 +71,24 @@ typedef enum ra_status {
 
 typedef enum ra_dtype { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
 
+/*
+ * How the N tokens of a (b, h) slice are dealt to the P ring blocks ("Ring
+ * attention, explained", section "The causal-mask catch"; the contiguous
+ * split is "Ring Attention: the math", section "Sharding the sequence").
+ * Tensors stay in token order; the layout only decides which positions form
+ * block j, hence which keys each ring step brings and how the causal work is
+ * spread over the blocks:
+ *   RA_LAYOUT_CONTIGUOUS  block j = positions j*c .. j*c + c - 1
+ *   RA_LAYOUT_ZIGZAG      block j = chunks j and 2P-1-j of 2P chunks of c/2
+ *                         positions (equal causal work per block)
+ *   RA_LAYOUT_STRIPED     block j = positions j, j + P, j + 2P, ...
+ */
+typedef enum ra_layout {
+  RA_LAYOUT_CONTIGUOUS = 0,
+  RA_LAYOUT_ZIGZAG = 1,
+  RA_LAYOUT_STRIPED = 2
+} ra_layout;
+
 /* Largest number of partial states ra_forward_partial / ra_merge accept. */
 #define RA_MAX_PARTIALS 64
 
@@ -110,6 +128,23 @@ RA_API ra_status ra_forward(const void* q, const void* k, const void* v, void* o
                             int32_t P, ra_dtype dtype, ra_stream_t stream);
 
 /*
+ * ra_forward_causal -- ring attention forward under the causal mask: the
+ * query at position n attends to key positions 0 .. n only ("Ring Attention:
+ * the math", section "Causal masking, load balance, and other wrinkles";
+ * "Ring attention, explained", section "The causal-mask catch").  Query block
+ * i visits the blocks in ring order (i - t) mod P as ra_forward does; K/V
+ * tiles that hold no visible key are skipped, the others are masked per key.
+ *   layout   which positions form each block (see ra_layout).
+ * Other arguments as ra_forward.  Extra rules: zigzag needs c even (bf16:
+ * c % 256 == 0); the bf16 path needs P <= 1024.
+ * Errors: as ra_forward, and RA_ERR_INVALID_ARG for an unknown layout.
+ */
+RA_API ra_status ra_forward_causal(const void* q, const void* k, const void* v, void* out,
+                                   float* lse, int32_t B, int32_t H, int64_t N, int32_t d,
+                                   int32_t P, ra_layout layout, ra_dtype dtype,
+                                   ra_stream_t stream);
+
+/*
  * ra_forward_partial -- the ring split into G contiguous segments of steps.
  * Partial g folds steps t in [floor(g*P/G), floor((g+1)*P/G)) of every query
  * block's ring order from an empty state and writes its (m, l, o) to
@@ -126,6 +161,17 @@ RA_API ra_status ra_forward_partial(const void* q, const void* k, const void* v,
                                     int32_t B, int32_t H, int64_t N, int32_t d, int32_t P,
                                     int32_t G, const ra_state* partials, ra_dtype dtype,
                                     ra_stream_t stream);
+
+/*
+ * ra_forward_partial_causal -- ra_forward_partial under the causal mask and
+ * a layout (see ra_forward_causal).  A row that sees no visible key in a
+ * segment gets an empty partial (m = -inf, l = 0, o = 0), which ra_merge
+ * ignores.
+ */
+RA_API ra_status ra_forward_partial_causal(const void* q, const void* k, const void* v,
+                                           int32_t B, int32_t H, int64_t N, int32_t d, int32_t P,
+                                           int32_t G, const ra_state* partials, ra_layout layout,
+                                           ra_dtype dtype, ra_stream_t stream);
 
 /*
  * ra_state_init -- set a state to empty: m = -inf, l = 0, o = 0 ("Ring

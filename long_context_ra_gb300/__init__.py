@@ -18,8 +18,9 @@ import torch
 from . import _native
 from ._native import RA_BF16, RA_F32, RA_MAX_PARTIALS, RaStateC
 
-__all__ = ["RaError", "RaState", "ra_forward", "ra_forward_partial", "ra_state_init", "ra_fold",
-           "ra_merge", "ra_last_device_status", "new_state", "library_path"]
+__all__ = ["RaError", "RaState", "ra_forward", "ra_forward_causal", "ra_forward_partial",
+           "ra_forward_partial_causal", "ra_state_init", "ra_fold", "ra_merge",
+           "ra_last_device_status", "new_state", "library_path"]
 
 
 class RaError(RuntimeError):
@@ -106,6 +107,24 @@ def ra_forward(q, k, v, P: int, out=None, lse=None, stream=None):
     return out, lse
 
 
+def ra_forward_causal(q, k, v, P: int, layout: str = "contiguous", out=None, lse=None,
+                      stream=None):
+    """Causal ring attention forward (query n sees keys 0..n); `layout` is
+    "contiguous", "zigzag" or "striped".  Returns (out, lse)."""
+    B, H, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share shape and dtype")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, N, device=q.device, dtype=torch.float32)
+    code = _native.lib().ra_forward_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H,
+                                           N, d, P, _native.RA_LAYOUTS[layout], _dtype_code(q),
+                                           _stream(stream))
+    _check(code, "ra_forward_causal")
+    return out, lse
+
+
 def _state_array(states):
     arr = (RaStateC * len(states))()
     for i, s in enumerate(states):
@@ -122,6 +141,20 @@ def ra_forward_partial(q, k, v, P: int, G: int, partials=None, stream=None):
     code = _native.lib().ra_forward_partial(_ptr(q), _ptr(k), _ptr(v), B, H, N, d, P, G, arr,
                                             _dtype_code(q), _stream(stream))
     _check(code, "ra_forward_partial")
+    return partials
+
+
+def ra_forward_partial_causal(q, k, v, P: int, G: int, layout: str = "contiguous",
+                              partials=None, stream=None):
+    """Causal ring split into G segments; returns G partial RaStates."""
+    B, H, N, d = q.shape
+    if partials is None:
+        partials = [new_state(B * H * N, d, q.device) for _ in range(G)]
+    arr = _state_array(partials)
+    code = _native.lib().ra_forward_partial_causal(_ptr(q), _ptr(k), _ptr(v), B, H, N, d, P, G,
+                                                   arr, _native.RA_LAYOUTS[layout],
+                                                   _dtype_code(q), _stream(stream))
+    _check(code, "ra_forward_partial_causal")
     return partials
 
 

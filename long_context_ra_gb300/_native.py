@@ -14,6 +14,7 @@ LIB_PATH = Path(__file__).resolve().parent / "_lib" / "libra_gb300.so"
 RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_MISALIGNED, RA_ERR_ARCH, RA_ERR_CUDA, \
     RA_ERR_TIMEOUT = range(7)
 RA_F32, RA_BF16 = 0, 1
+RA_LAYOUTS = {"contiguous": 0, "zigzag": 1, "striped": 2}
 RA_MAX_PARTIALS = 64
 
 
@@ -31,7 +32,11 @@ _I64 = ctypes.c_int64
 _SP = ctypes.POINTER(RaStateC)
 PROTOTYPES = {
     "ra_forward": (_I32, [_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _P]),
+    "ra_forward_causal": (_I32, [_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _I32,
+                                 _P]),
     "ra_forward_partial": (_I32, [_P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _SP, _I32, _P]),
+    "ra_forward_partial_causal": (_I32, [_P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _SP,
+                                         _I32, _I32, _P]),
     "ra_state_init": (_I32, [_SP, _P]),
     "ra_fold": (_I32, [_SP, _P, _P, _P, _I64, _I64, _I32, _P]),
     "ra_merge": (_I32, [_SP, _I32, _P, _P, _I32, _P]),

@@ -88,6 +88,23 @@ ra_status make_map(CUtensorMap* map, const void* ptr, int64_t rows, int d) {
   return r == CUDA_SUCCESS ? RA_OK : RA_ERR_CUDA;
 }
 
+// Strided (striped-layout) bf16 view of a [slices, N, d] tensor as
+// [slices * N / P, P, d]: block j's local row r of slice s is (s*N/P + r, j).
+// Box: 128 local rows x 1 block x 64 columns, 128-byte swizzle.
+ra_status make_map_striped(CUtensorMap* map, const void* ptr, int64_t rows, int d, int P) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(P),
+                              static_cast<cuuint64_t>(rows / P)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(P)};
+  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? RA_OK : RA_ERR_CUDA;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 ra_status launched(cudaError_t e) { return e == cudaSuccess ? RA_OK : RA_ERR_CUDA; }
@@ -134,9 +151,15 @@ ra_status run_fold(const FoldArgs& a, ra_dtype dt, cudaStream_t s) {
   ra_status st = get_encoder();
   if (st != RA_OK) return st;
   CUtensorMap tq, tk, tv;
-  if ((st = make_map(&tq, a.q, a.slices * a.nq, a.d)) != RA_OK) return st;
-  if ((st = make_map(&tk, a.k, a.slices * a.nk, a.d)) != RA_OK) return st;
-  if ((st = make_map(&tv, a.v, a.slices * a.nk, a.d)) != RA_OK) return st;
+  if (a.layout == kStriped) {
+    if ((st = make_map_striped(&tq, a.q, a.slices * a.nq, a.d, a.P)) != RA_OK) return st;
+    if ((st = make_map_striped(&tk, a.k, a.slices * a.nk, a.d, a.P)) != RA_OK) return st;
+    if ((st = make_map_striped(&tv, a.v, a.slices * a.nk, a.d, a.P)) != RA_OK) return st;
+  } else {
+    if ((st = make_map(&tq, a.q, a.slices * a.nq, a.d)) != RA_OK) return st;
+    if ((st = make_map(&tk, a.k, a.slices * a.nk, a.d)) != RA_OK) return st;
+    if ((st = make_map(&tv, a.v, a.slices * a.nk, a.d)) != RA_OK) return st;
+  }
   return launched(launch_fold_sm103(a, tq, tk, tv, s));
 }
 
@@ -159,12 +182,33 @@ using namespace ra;
 
 extern "C" {
 
-RA_API ra_status ra_forward(const void* q, const void* k, const void* v, void* out, float* lse,
-                            int32_t B, int32_t H, int64_t N, int32_t d, int32_t P, ra_dtype dtype,
-                            ra_stream_t stream) {
+}  // extern "C"
+
+namespace ra {
+namespace {
+
+// Causal / layout checks shared by the causal entry points.
+ra_status check_causal(int64_t N, int32_t P, ra_layout layout, ra_dtype dt, FoldArgs* a) {
+  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG && layout != RA_LAYOUT_STRIPED)
+    return RA_ERR_INVALID_ARG;
+  const int64_t c = P > 0 ? N / P : 0;
+  if (layout == RA_LAYOUT_ZIGZAG && c % 2 != 0) return RA_ERR_UNSUPPORTED;
+  if (dt == RA_BF16) {
+    if (layout == RA_LAYOUT_ZIGZAG && c % 256 != 0) return RA_ERR_UNSUPPORTED;
+    if (P > kMaxCausalSteps) return RA_ERR_UNSUPPORTED;
+  }
+  a->causal = 1;
+  a->layout = static_cast<int32_t>(layout);
+  return RA_OK;
+}
+
+ra_status forward_impl(const void* q, const void* k, const void* v, void* out, float* lse,
+                       int32_t B, int32_t H, int64_t N, int32_t d, int32_t P, bool causal,
+                       ra_layout layout, ra_dtype dtype, ra_stream_t stream) {
   FoldArgs a;
   ra_status st = check_attention(q, k, v, B, H, N, d, P, dtype, &a);
   if (st != RA_OK) return st;
+  if (causal && (st = check_causal(N, P, layout, dtype, &a)) != RA_OK) return st;
   if (a.slices * a.nq == 0) return RA_OK;
   if (!out || !lse) return RA_ERR_INVALID_ARG;
   if (!aligned(out, dtype == RA_BF16 ? 16 : 4) || !aligned(lse, 4)) return RA_ERR_MISALIGNED;
@@ -177,13 +221,13 @@ RA_API ra_status ra_forward(const void* q, const void* k, const void* v, void* o
   return run_fold(a, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
-RA_API ra_status ra_forward_partial(const void* q, const void* k, const void* v, int32_t B,
-                                    int32_t H, int64_t N, int32_t d, int32_t P, int32_t G,
-                                    const ra_state* partials, ra_dtype dtype,
-                                    ra_stream_t stream) {
+ra_status partial_impl(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                       int64_t N, int32_t d, int32_t P, int32_t G, const ra_state* partials,
+                       bool causal, ra_layout layout, ra_dtype dtype, ra_stream_t stream) {
   FoldArgs a;
   ra_status st = check_attention(q, k, v, B, H, N, d, P, dtype, &a);
   if (st != RA_OK) return st;
+  if (causal && (st = check_causal(N, P, layout, dtype, &a)) != RA_OK) return st;
   if (!partials || G < 1 || G > RA_MAX_PARTIALS || G > P) return RA_ERR_INVALID_ARG;
   const int64_t rows = a.slices * a.nq;
   for (int g = 0; g < G; ++g) {
@@ -202,6 +246,40 @@ RA_API ra_status ra_forward_partial(const void* q, const void* k, const void* v,
   a.G = G;
   a.status = di.status;
   return run_fold(a, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace ra
+
+extern "C" {
+
+RA_API ra_status ra_forward(const void* q, const void* k, const void* v, void* out, float* lse,
+                            int32_t B, int32_t H, int64_t N, int32_t d, int32_t P, ra_dtype dtype,
+                            ra_stream_t stream) {
+  return forward_impl(q, k, v, out, lse, B, H, N, d, P, false, RA_LAYOUT_CONTIGUOUS, dtype,
+                      stream);
+}
+
+RA_API ra_status ra_forward_causal(const void* q, const void* k, const void* v, void* out,
+                                   float* lse, int32_t B, int32_t H, int64_t N, int32_t d,
+                                   int32_t P, ra_layout layout, ra_dtype dtype,
+                                   ra_stream_t stream) {
+  return forward_impl(q, k, v, out, lse, B, H, N, d, P, true, layout, dtype, stream);
+}
+
+RA_API ra_status ra_forward_partial(const void* q, const void* k, const void* v, int32_t B,
+                                    int32_t H, int64_t N, int32_t d, int32_t P, int32_t G,
+                                    const ra_state* partials, ra_dtype dtype,
+                                    ra_stream_t stream) {
+  return partial_impl(q, k, v, B, H, N, d, P, G, partials, false, RA_LAYOUT_CONTIGUOUS, dtype,
+                      stream);
+}
+
+RA_API ra_status ra_forward_partial_causal(const void* q, const void* k, const void* v,
+                                           int32_t B, int32_t H, int64_t N, int32_t d, int32_t P,
+                                           int32_t G, const ra_state* partials, ra_layout layout,
+                                           ra_dtype dtype, ra_stream_t stream) {
+  return partial_impl(q, k, v, B, H, N, d, P, G, partials, true, layout, dtype, stream);
 }
 
 RA_API ra_status ra_state_init(const ra_state* st, ra_stream_t stream) {

@@ -10,6 +10,11 @@
 //   l' = alpha l + sum exp(s - m');  o' = alpha o + sum exp(s - m') v.
 // Folding a block in chunks is exact by the same identity.  The lanes split
 // o: lane e holds o[e], o[e + 32], ...
+//
+// Causal ("Ring attention, explained", "The causal-mask catch"): a query at
+// position n sees key positions <= n.  Under every layout the positions of a
+// block increase along its local order, so the visible keys of a block are a
+// prefix and the walk over it stops at the first chunk that starts after n.
 
 #include <cmath>
 
@@ -19,6 +24,27 @@ namespace ra {
 namespace {
 
 constexpr int kWarps = 4;
+
+// Position of local row r of block j under `layout` (P blocks of c rows).
+__device__ __forceinline__ int64_t pos_of(int layout, int64_t j, int64_t r, int64_t P,
+                                          int64_t c) {
+  if (layout == kZigzag) {
+    const int64_t h = c / 2;
+    return r < h ? j * h + r : (2 * P - 1 - j) * h + (r - h);
+  }
+  if (layout == kStriped) return j + P * r;
+  return j * c + r;
+}
+
+// Block holding position n.
+__device__ __forceinline__ int64_t block_of(int layout, int64_t n, int64_t P, int64_t c) {
+  if (layout == kZigzag) {
+    const int64_t chunk = n / (c / 2);
+    return chunk < P ? chunk : 2 * P - 1 - chunk;
+  }
+  if (layout == kStriped) return n % P;
+  return n / c;
+}
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -45,7 +71,7 @@ __global__ void __launch_bounds__(kWarps * 32) fold_f32_kernel(const FoldArgs a)
   const int64_t n = rid % a.nq;
   const int64_t cq = a.nq / a.P;
   const int64_t ck = a.nk / a.P;
-  const int i = static_cast<int>(n / cq);
+  const int i = static_cast<int>(block_of(a.layout, n, a.P, cq));
   const int t0 = static_cast<int>(static_cast<int64_t>(g) * a.P / a.G);
   const int t1 = static_cast<int>(static_cast<int64_t>(g + 1) * a.P / a.G);
 
@@ -70,15 +96,16 @@ __global__ void __launch_bounds__(kWarps * 32) fold_f32_kernel(const FoldArgs a)
   for (int t = t0; t < t1; ++t) {
     int j = (i - t) % a.P;
     if (j < 0) j += a.P;
-    const int64_t krow0 = slice * a.nk + static_cast<int64_t>(j) * ck;
-    const float* kb = static_cast<const float*>(a.k) + krow0 * d;
-    const float* vb = static_cast<const float*>(a.v) + krow0 * d;
+    const float* kbase = static_cast<const float*>(a.k) + slice * a.nk * d;
+    const float* vbase = static_cast<const float*>(a.v) + slice * a.nk * d;
     for (int64_t c0 = 0; c0 < ck; c0 += 32) {
+      if (a.causal && pos_of(a.layout, j, c0, a.P, ck) > n) break;  // rest of block masked
       const int64_t key = c0 + lane;
-      const bool valid = key < ck;
+      const int64_t kpos = key < ck ? pos_of(a.layout, j, key, a.P, ck) : 0;
+      const bool valid = key < ck && (!a.causal || kpos <= n);
       float s = -INFINITY;
       if (valid) {
-        const float* kr = kb + key * d;
+        const float* kr = kbase + kpos * d;
         float acc = 0.f;
         for (int e = 0; e < d; ++e) acc = fmaf(qs[warp][e], kr[e], acc);
         s = acc * a.tau;
@@ -92,7 +119,8 @@ __global__ void __launch_bounds__(kWarps * 32) fold_f32_kernel(const FoldArgs a)
       const int nvalid = ck - c0 < 32 ? static_cast<int>(ck - c0) : 32;
       for (int jj = 0; jj < nvalid; ++jj) {
         const float pj = __shfl_sync(0xffffffffu, p, jj);
-        const float* vr = vb + (c0 + jj) * d;
+        if (pj == 0.f) continue;  // masked (or underflowed) key adds nothing
+        const float* vr = vbase + __shfl_sync(0xffffffffu, kpos, jj) * d;
 #pragma unroll
         for (int v = 0; v < DV; ++v) {
           const int e = lane + 32 * v;

@@ -74,7 +74,6 @@ template <int D>
 struct Layout {
   static constexpr int kBoxBytes = kBM * 128;  // 128 rows x 128 bytes (64 bf16)
   static constexpr int kTileBytes = kBM * D * 2;
-  static constexpr int kBoxes = D / 64;
   static constexpr int kStages = D == 128 ? 4 : 6;
   static constexpr int kQ0 = 0;
   static constexpr int kQ1 = kTileBytes;
@@ -83,7 +82,8 @@ struct Layout {
   // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], drain
   static constexpr int kNumBars = 1 + 2 * kStages + 7;
   static constexpr int kMisc = kBar + kNumBars * 8;  // TMEM base, abort flag
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kSteps = kMisc + 16;          // causal step table (int4 per step)
+  static constexpr int kBytes = kSteps + kMaxCausalSteps * 16;
   static constexpr int kSmem = kBytes + 1024;  // slack for 1024-byte alignment
   static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -149,19 +149,120 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const A
   }
 }
 
-// Which key rows iteration `it` of a work unit loads.
-struct KvWalk {
-  int64_t slice_row0;  // slice * nk
-  int64_t ck;          // keys per block
-  int i, P, t0, kv_tiles;
-  __device__ int64_t row(int it) const {
-    const int t = t0 + it / kv_tiles;
-    const int kt = it % kv_tiles;
-    int j = (i - t) % P;
-    if (j < 0) j += P;
-    return slice_row0 + static_cast<int64_t>(j) * ck + static_cast<int64_t>(kt) * kBN;
+// The K/V tiles one work unit visits, in order: ring steps t = t0 .. t1-1
+// visit block j = (i - t) mod P ("Ring Attention: the math", "The ring
+// schedule"), and within a block its 128-key tiles in local order.  Under the
+// causal mask ("Ring attention, explained", "The causal-mask catch") only the
+// tiles holding a key at or before the unit's last query take part; in every
+// layout these are a prefix of the block's tiles, so fully masked tiles and
+// blocks are skipped and every role walks the same sequence.
+struct Walk {
+  int64_t slice, N, c;  // slice index, tokens per slice, tokens per block
+  int i, P, t0, t1, tiles, layout;
+  bool causal;
+  int64_t qlast;  // last query position of the unit (striped: last local row)
+  int t, kt, nt;  // iteration state: step, tile within the block, tiles in it
+
+  __device__ int block(int tt) const {
+    int j = (i - tt) % P;
+    return j < 0 ? j + P : j;
+  }
+  // Position of local row r of block j.
+  __device__ int64_t pos(int j, int64_t r) const {
+    if (layout == kZigzag) {
+      const int64_t h = c / 2;
+      return r < h ? j * h + r : (2 * static_cast<int64_t>(P) - 1 - j) * h + (r - h);
+    }
+    if (layout == kStriped) return j + static_cast<int64_t>(P) * r;
+    return j * c + r;
+  }
+  // Tiles kt in [0, ntile) whose first key position first + kt*128 <= qlast.
+  __device__ int prefix(int64_t first, int ntile) const {
+    if (qlast < first) return 0;
+    const int64_t n = (qlast - first) / kBN + 1;
+    return n < ntile ? static_cast<int>(n) : ntile;
+  }
+  __device__ int count(int j) const {
+    if (!causal) return tiles;
+    if (layout == kStriped) {
+      // key local row b is visible to query local row a iff b < a, or b == a and j <= i
+      const int64_t lim = qlast - (j > i ? 1 : 0);
+      if (lim < 0) return 0;
+      const int64_t n = lim / kBN + 1;
+      return n < tiles ? static_cast<int>(n) : tiles;
+    }
+    if (layout == kZigzag) {
+      const int half = tiles / 2;
+      const int a = prefix(j * (c / 2), half);
+      return a < half ? a : half + prefix((2 * static_cast<int64_t>(P) - 1 - j) * (c / 2), half);
+    }
+    return prefix(j * c, tiles);
+  }
+  __device__ int total() const {
+    int n = 0;
+    for (int tt = t0; tt < t1; ++tt) n += count(block(tt));
+    return n;
+  }
+  __device__ void skip() {
+    while (t < t1 && kt >= nt) {
+      ++t;
+      kt = 0;
+      nt = t < t1 ? count(block(t)) : 0;
+    }
+  }
+  __device__ void start() {
+    t = t0;
+    kt = 0;
+    nt = t < t1 ? count(block(t)) : 0;
+    skip();
+  }
+  __device__ void next() {
+    ++kt;
+    skip();
+  }
+  // Current tile: first key position (contiguous, zigzag) or first local row.
+  __device__ int64_t key_first() const {
+    return layout == kStriped ? static_cast<int64_t>(kt) * kBN : pos(block(t), static_cast<int64_t>(kt) * kBN);
   }
 };
+
+// Per ring step of a causal unit, as the softmax warps see it: the number of
+// tiles visited and the offsets that give the first key of tile kt,
+//   first(kt) = kt < tiles/2 ? a + kt*128 : b + (kt - tiles/2)*128,
+// in the units of the query reference `qref` (the token position, or for the
+// striped layout the local row, shifted by one when j > i).  The number of
+// keys of the tile visible to the query is then qref - first(kt) + 1,
+// clamped to [0, 128].
+__device__ __forceinline__ int4 step_entry(const Walk& w, int tt) {
+  const int j = w.block(tt);
+  const int half = w.tiles / 2;
+  int4 e;
+  e.x = w.count(j);
+  if (w.layout == kStriped) {
+    e.y = j > w.i ? 1 : 0;
+    e.z = e.y + half * kBN;
+  } else {
+    e.y = static_cast<int>(w.pos(j, 0));
+    e.z = static_cast<int>(w.pos(j, static_cast<int64_t>(half) * kBN));
+  }
+  e.w = 0;
+  return e;
+}
+
+// Issue the TMA loads of one 128-row tile (all its 64-column boxes): 2-D at
+// row `row` of the [rows, d] view, or, for the striped layout, 3-D at
+// (block j, local row) of the [slices * N / P, P, d] view.
+template <int D>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, bool striped,
+                                          int64_t row, int j, int64_t lrow, uint32_t bar) {
+#pragma unroll
+  for (int b = 0; b < D / 64; ++b) {
+    if (striped)
+      tma_load_3d(dst + b * kBM * 128, map, b * 64, j, static_cast<int32_t>(lrow), bar);
+    else
+      tma_load_2d(dst + b * kBM * 128, map, b * 64, static_cast<int32_t>(row), bar);
+  }
+}
 
 // The MMA thread builds each operand's shared-memory descriptor once and
 // moves it by adding (byte offset >> 4) to its start-address field; every
@@ -198,7 +299,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
     mma_bf16_ts(d_tmem, p_tmem + kk * 8, dv + desc_step(kk * 16 * 128), idesc, 1u);
 }
 
-template <int D>
+template <int D, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     fold_sm103_kernel(const __grid_constant__ FoldArgs a, const __grid_constant__ CUtensorMap tq,
                       const __grid_constant__ CUtensorMap tk,
@@ -216,25 +317,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x % 32;
 
   // ---- work unit: (slice, query block i, segment g, tile pair pr) ----
+  // Consecutive CTAs share (slice, i, g) and so walk the same K/V tiles in
+  // the same order (L2 reuse).  Under the causal mask the heaviest units (the
+  // last query rows) are numbered first.
   const int64_t cq = a.nq / a.P;
   const int64_t ck = a.nk / a.P;
   const int tiles_q = static_cast<int>(cq / kBM);
   const int pairs = (tiles_q + 1) / 2;
   int64_t u = blockIdx.x;
-  const int pr = static_cast<int>(u % pairs);
+  int pr = static_cast<int>(u % pairs);
   u /= pairs;
   const int g = static_cast<int>(u % a.G);
   u /= a.G;
-  const int i = static_cast<int>(u % a.P);
+  int i = static_cast<int>(u % a.P);
   const int64_t slice = u / a.P;
+  if (kCausal) {
+    pr = pairs - 1 - pr;
+    i = a.P - 1 - i;
+  }
   const bool has_t1 = 2 * pr + 1 < tiles_q;
-  const int t0 = static_cast<int>(static_cast<int64_t>(g) * a.P / a.G);
-  const int t1 = static_cast<int>(static_cast<int64_t>(g + 1) * a.P / a.G);
-  const int kv_tiles = static_cast<int>(ck / kBN);
-  const int n_iter = (t1 - t0) * kv_tiles;
-  const int64_t q_row0 = slice * a.nq + static_cast<int64_t>(i) * cq +
-                         static_cast<int64_t>(pr) * 2 * kBM;
-  const KvWalk walk{slice * a.nk, ck, i, a.P, t0, kv_tiles};
+  const bool striped = a.layout == kStriped;
+  Walk walk;
+  walk.slice = slice;
+  walk.N = a.nk;
+  walk.c = ck;
+  walk.i = i;
+  walk.P = a.P;
+  walk.t0 = static_cast<int>(static_cast<int64_t>(g) * a.P / a.G);
+  walk.t1 = static_cast<int>(static_cast<int64_t>(g + 1) * a.P / a.G);
+  walk.tiles = static_cast<int>(ck / kBN);
+  walk.layout = a.layout;
+  walk.causal = kCausal;
+  const int64_t lr0 = static_cast<int64_t>(pr) * 2 * kBM;  // first local query row
+  const int64_t lr_last = lr0 + (has_t1 ? 2 * kBM : kBM) - 1;
+  walk.qlast = striped ? lr_last : walk.pos(i, lr_last);
+  const int n_iter = walk.total();
 
   // ---- set-up ----
   if (threadIdx.x == 0) {
@@ -270,33 +387,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= TMA producer =================
     setmaxnreg_dec<kRegsOther>();
     if (lane == 0) {
-      const uint32_t qbytes = (has_t1 ? 2u : 1u) * L::kTileBytes;
-      mbar_arrive_expect_tx(bars.q_full(), qbytes);
-#pragma unroll
-      for (int b = 0; b < L::kBoxes; ++b) {
-        tma_load_2d(base + L::kQ0 + b * L::kBoxBytes, &tq, b * 64, static_cast<int32_t>(q_row0),
-                    bars.q_full());
-        if (has_t1)
-          tma_load_2d(base + L::kQ1 + b * L::kBoxBytes, &tq, b * 64,
-                      static_cast<int32_t>(q_row0 + kBM), bars.q_full());
-      }
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, last_parity = 0;  // per-stage bit masks, for the drain
       bool ok = true;
-      for (int it = 0; it < n_iter && ok; ++it) {
-        const int32_t row = static_cast<int32_t>(walk.row(it));
+      if (n_iter > 0) {
+        const uint32_t qbytes = (has_t1 ? 2u : 1u) * L::kTileBytes;
+        mbar_arrive_expect_tx(bars.q_full(), qbytes);
+        load_tile<D>(base + L::kQ0, &tq, striped, slice * a.nq + walk.pos(i, lr0), i,
+                     slice * cq + lr0, bars.q_full());
+        if (has_t1)
+          load_tile<D>(base + L::kQ1, &tq, striped, slice * a.nq + walk.pos(i, lr0 + kBM), i,
+                       slice * cq + lr0 + kBM, bars.q_full());
+      }
+      Walk kw = walk;
+      kw.start();
+      for (int it = 0; it < n_iter && ok; ++it, kw.next()) {
+        const int j = kw.block(kw.t);
+        const int64_t row = slice * a.nk + kw.key_first();         // 2-D row (not striped)
+        const int64_t lrow = slice * ck + static_cast<int64_t>(kw.kt) * kBN;  // 3-D (striped)
         for (int kind = 0; kind < 2; ++kind) {
           if (!wait1(bars.kv_empty(stage), phase ^ 1u, ab)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(bars.kv_full(stage), L::kTileBytes);
-          const CUtensorMap* map = kind == 0 ? &tk : &tv;
-#pragma unroll
-          for (int b = 0; b < L::kBoxes; ++b)
-            tma_load_2d(base + L::kKV + stage * L::kTileBytes + b * L::kBoxBytes, map, b * 64, row,
-                        bars.kv_full(stage));
+          load_tile<D>(base + L::kKV + stage * L::kTileBytes, kind == 0 ? &tk : &tv, striped, row, j,
+                       lrow, bars.kv_full(stage));
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == L::kStages) {
@@ -307,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         // Let every load already issued land before the CTA goes away.
-        wait_drain(bars.q_full(), 0);
+        if (n_iter > 0) wait_drain(bars.q_full(), 0);
         for (int s = 0; s < L::kStages; ++s)
           if (issued & (1u << s)) wait_drain(bars.kv_full(s), (last_parity >> s) & 1u);
       }
@@ -323,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dK = desc_sw128(base + L::kKV, 16, 1024);  // stage 0, K-major
       const uint64_t dV = desc_sw128(base + L::kKV, L::kBoxBytes, 1024);  // stage 0, MN-major
       const bool from_state = a.mode == kFold;
-      bool ok = wait1(bars.q_full(), 0, ab);
+      bool ok = n_iter > 0 && wait1(bars.q_full(), 0, ab);
       int cons = 0;  // K/V tiles consumed so far
       if (ok) ok = wait1(bars.kv_full(0), 0, ab);
       if (ok) {
@@ -388,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         mma_commit(bars.o_full(0));
         if (has_t1) mma_commit(bars.o_full(1));
-      } else {
+      } else if (n_iter > 0) {
         // Wait for every MMA already issued before TMEM is released.
         mma_commit(bars.drain());
         wait_drain(bars.drain(), 0);
@@ -399,13 +516,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     setmaxnreg_inc<kRegsSoftmax>();
     const int t = warp / 4;   // query tile
     const int wq = warp % 4;  // TMEM lane quarter of this warp
+    if (kCausal) {
+      // Step table for the mask, built by the 8 softmax warps together.
+      const int nsteps = walk.t1 - walk.t0;
+      int4* tab = reinterpret_cast<int4*>(gbase + L::kSteps);
+      for (int x = threadIdx.x; x < nsteps; x += 256) tab[x] = step_entry(walk, walk.t0 + x);
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+    }
     if (t == 0 || has_t1) {
       const int row = wq * 32 + lane;
       const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
       const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(t * 128);
       const uint32_t tO = tmem + lane_off + 256u + static_cast<uint32_t>(t * D);
-      const int64_t grow = q_row0 + t * kBM + row;  // global query row
+      const int64_t lrow = lr0 + t * kBM + row;  // local row in query block i
+      const int64_t grow = slice * a.nq + walk.pos(i, lrow);  // row of q, out, lse, states
       const float sl2 = a.scale_log2;
+      // causal: this thread's place in the step table (query reference,
+      // current step and tile within it)
+      const int4* steps = reinterpret_cast<const int4*>(gbase + L::kSteps);
+      const int qref = kCausal ? static_cast<int>(striped ? lrow : walk.pos(i, lrow)) : 0;
+      int ts = 0, tkt = 0;
+      if (kCausal && n_iter > 0)
+        while (tkt >= steps[ts].x) ++ts;
 
       float m_ref = -INFINITY;   // reference max of the exponentials (log2 units)
       float m_true = -INFINITY;  // true running max (log2 units)
@@ -435,6 +567,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       bool ok = true;
       for (int it = 0; it < n_iter; ++it) {
+        if (kCausal && it > 0) {
+          ++tkt;
+          while (tkt >= steps[ts].x) {
+            ++ts;
+            tkt = 0;
+          }
+        }
         if (!wait_warp(bars.s_full(t), static_cast<uint32_t>(it & 1), ab)) {
           ok = false;
           break;
@@ -445,6 +584,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBN; c += 32) tmem_ld32(tS + c, s + c);
         tmem_ld_wait();
         reg_fence(s, kBN);
+        if (kCausal) {
+          // keys after the query's own position take no part (score -inf)
+          const int4 ent = steps[ts];
+          const int half = walk.tiles / 2;
+          const int first = tkt < half ? ent.y + tkt * kBN : ent.z + (tkt - half) * kBN;
+          int nvis = qref - first + 1;
+          nvis = nvis < 0 ? 0 : (nvis > kBN ? kBN : nvis);
+          if (__any_sync(0xffffffffu, nvis < kBN)) {
+#pragma unroll
+            for (int c = 0; c < kBN; ++c)
+              if (c >= nvis) s[c] = __float_as_uint(-INFINITY);
+          }
+        }
 
         // Row max: eight independent chains of three-input maxima.
         float mx[8];
@@ -487,7 +639,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // written over the first 64 columns of S, where the P V product reads
         // it.
         const uint64_t scale2 = pack_f32x2(sl2, sl2);
-        const uint64_t neg2 = pack_f32x2(-m_ref, -m_ref);
+        // a row that has seen no visible key yet keeps m_ref = -inf; its
+        // masked scores must still give p = 0 rather than NaN
+        const float neg = (kCausal && m_ref == -INFINITY) ? 0.f : -m_ref;
+        const uint64_t neg2 = pack_f32x2(neg, neg);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -517,7 +672,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         o_valid = true;
       }
 
-      if (ok && wait_warp(bars.o_full(t), 0, ab)) {
+      if (n_iter == 0) {
+        // Nothing of this unit is visible in its segment: an empty state.
+        if (a.mode == kPartial) {
+          float4* dst = reinterpret_cast<float4*>(a.part.o[g] + grow * D);
+#pragma unroll
+          for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+          a.part.m[g][grow] = -INFINITY;
+          a.part.l[g][grow] = 0.f;
+        }
+      } else if (ok && wait_warp(bars.o_full(t), 0, ab)) {
         tc_fence_after();
         if (a.mode == kForward) {
           const float inv = 1.f / l;
@@ -541,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           a.lse[grow] = (m_ref + __log2f(l)) * kLn2;
         } else {
           // Re-express (l, o) relative to the true running max.
-          const float fix = ex2(m_ref - m_true);
+          const float fix = m_true == -INFINITY ? 1.f : ex2(m_ref - m_true);
           float* mo = a.mode == kPartial ? a.part.m[g] : a.st_m;
           float* lo = a.mode == kPartial ? a.part.l[g] : a.st_l;
           float* oo = a.mode == kPartial ? a.part.o[g] : a.st_o;
@@ -578,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kCausal>
 cudaError_t launch_d(const FoldArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, cudaStream_t s) {
   using L = Layout<D>;
@@ -587,8 +751,8 @@ cudaError_t launch_d(const FoldArgs& a, const CUtensorMap& tq, const CUtensorMap
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(fold_sm103_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kSmem);
+    e = cudaFuncSetAttribute(fold_sm103_kernel<D, kCausal>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
@@ -596,7 +760,8 @@ cudaError_t launch_d(const FoldArgs& a, const CUtensorMap& tq, const CUtensorMap
   const int64_t tiles_q = cq / kBM;
   const int64_t pairs = (tiles_q + 1) / 2;
   const int64_t grid = a.slices * a.P * a.G * pairs;
-  fold_sm103_kernel<D><<<static_cast<unsigned>(grid), kThreads, L::kSmem, s>>>(a, tq, tk, tv);
+  fold_sm103_kernel<D, kCausal>
+      <<<static_cast<unsigned>(grid), kThreads, L::kSmem, s>>>(a, tq, tk, tv);
   return cudaGetLastError();
 }
 
@@ -604,8 +769,13 @@ cudaError_t launch_d(const FoldArgs& a, const CUtensorMap& tq, const CUtensorMap
 
 cudaError_t launch_fold_sm103(const FoldArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                               const CUtensorMap& tv, cudaStream_t s) {
-  if (a.d == 128) return launch_d<128>(a, tq, tk, tv, s);
-  if (a.d == 64) return launch_d<64>(a, tq, tk, tv, s);
+  if (a.causal) {
+    if (a.d == 128) return launch_d<128, true>(a, tq, tk, tv, s);
+    if (a.d == 64) return launch_d<64, true>(a, tq, tk, tv, s);
+  } else {
+    if (a.d == 128) return launch_d<128, false>(a, tq, tk, tv, s);
+    if (a.d == 64) return launch_d<64, false>(a, tq, tk, tv, s);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -17,6 +17,13 @@ enum Mode : int32_t {
   kFold = 2,     // load (m, l, o), fold one block, write (m, l, o) back
 };
 
+// How the tokens of a slice are dealt to the P blocks (causal load balance).
+enum Layout : int32_t {
+  kContiguous = 0,  // block j = positions j*c .. j*c + c - 1
+  kZigzag = 1,      // block j = chunks j and 2P-1-j of 2P chunks of c/2 positions
+  kStriped = 2,     // block j = positions j, j + P, j + 2P, ...
+};
+
 // Per-segment partial-state pointers (device).
 struct PartialPtrs {
   float* m[RA_MAX_PARTIALS];
@@ -30,7 +37,9 @@ struct PartialPtrs {
 // fold call).  Slice s has nq query rows and nk key rows, each cut into P
 // contiguous blocks (cq = nq / P, ck = nk / P).  Query block i visits key
 // block (i - t) mod P at ring step t.  In partial mode the P steps are split
-// into G contiguous segments; in fold mode P = G = 1.
+// into G contiguous segments; in fold mode P = G = 1.  Tensors are in token
+// order; `layout` says which positions form block j (the rows a query block
+// holds and the key rows a ring step brings), `causal` masks later keys.
 struct FoldArgs {
   const void* q;  // [slices, nq, d]
   const void* k;  // [slices, nk, d]
@@ -42,6 +51,8 @@ struct FoldArgs {
   int32_t P;
   int32_t G;
   int32_t mode;
+  int32_t causal;    // 1: a query sees key positions <= its own
+  int32_t layout;    // Layout of the tokens over the blocks
   float tau;         // 1 / sqrt(d)
   float scale_log2;  // tau * log2(e)
   void* out;         // forward: [slices, nq, d] (input dtype)
@@ -71,6 +82,10 @@ cudaError_t launch_fold_f32(const FoldArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
 cudaError_t launch_state_init(float* m, float* l, float* o, int64_t rows, int32_t d,
                               cudaStream_t s);
+
+// Largest P of the causal tensor-core path: the softmax warps keep one
+// 16-byte entry per ring step of a work unit in shared memory.
+constexpr int kMaxCausalSteps = 1024;
 
 // Watchdog codes written to FoldArgs::status.
 constexpr int kStatusTimeout = 1;

@@ -97,3 +97,15 @@ def test_fold_and_merge_validation(L):
     empty = _native.RaStateC(A, A, A, 0, 64)
     assert L.ra_state_init(ctypes.byref(empty), None) == _native.RA_OK
     assert L.ra_state_init(None, None) == _native.RA_ERR_INVALID_ARG
+
+
+def test_causal_validation(L):
+    def fc(layout=0, N=1024, P=4, d=64, dt=BF16):
+        return L.ra_forward_causal(A, A, A, A, A, 1, 1, N, d, P, layout, dt, None)
+    assert fc(layout=3) == _native.RA_ERR_INVALID_ARG
+    assert fc(layout=-1) == _native.RA_ERR_INVALID_ARG
+    assert fc(layout=1, N=1536, P=4) == _native.RA_ERR_UNSUPPORTED   # zigzag bf16: c % 256
+    assert fc(layout=1, N=12, P=4, dt=F32) == _native.RA_ERR_UNSUPPORTED  # zigzag: c odd
+    assert fc(layout=0, N=2048 * 128, P=2048) == _native.RA_ERR_UNSUPPORTED  # bf16 P > 1024
+    assert fc(layout=2, N=1024, P=8) == _native.RA_ERR_ARCH  # valid: stops at the device check
+    assert fc(layout=1, N=16, P=4, dt=F32) == _native.RA_ERR_ARCH
