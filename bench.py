@@ -125,6 +125,12 @@ def max_over_ranks(x: float, device, world: int) -> float:
     return float(t.item())
 
 
+def causal_flops(w) -> float:
+    """Work of causal attention: 4 d flops per visible (query, key) pair,
+    N (N + 1) / 2 pairs per head."""
+    return 4.0 * w.B * w.H * w.d * w.N * (w.N + 1) / 2.0
+
+
 def job_throughput(flops_per_replica: float, world: int, ms_max: float) -> float:
     """Whole-job TFLOP/s: every replica's work over the slowest replica's time."""
     return world * flops_per_replica / (ms_max * 1e-3) / 1e12
@@ -230,8 +236,13 @@ def run_ours(args, w) -> None:
     lse = torch.empty(w.B, w.H, w.N, device=dev, dtype=torch.float32)
     stream = torch.cuda.current_stream()
 
-    def step():
-        ra.ra_forward(q, k, v, w.P, out=out, lse=lse)
+    if args.causal:
+        def step():
+            ra.ra_forward_causal(q, k, v, w.P, layout=args.causal, out=out, lse=lse)
+    else:
+        def step():
+            ra.ra_forward(q, k, v, w.P, out=out, lse=lse)
+    flops = causal_flops(w) if args.causal else w.flops
 
     for _ in range(args.warmup):
         step()
@@ -260,7 +271,7 @@ def run_ours(args, w) -> None:
     if ra.ra_last_device_status() != 0:
         raise RuntimeError("kernel watchdog fired in the timed region")
     ms_max = max_over_ranks(ms, dev, world)
-    value = job_throughput(w.flops, world, ms_max)
+    value = job_throughput(flops, world, ms_max)
 
     # end to end through the C ABI: pinned host inputs -> device, forward,
     # out and lse back to pinned host memory, every step
@@ -289,13 +300,13 @@ def run_ours(args, w) -> None:
     wall = (time.perf_counter() - w0) / n_e2e
     ms_e2e = max(e0.elapsed_time(e1) / n_e2e, wall * 1e3)
     ms_e2e_max = max_over_ranks(ms_e2e, dev, world)
-    e2e_value = job_throughput(w.flops, world, ms_e2e_max)
+    e2e_value = job_throughput(flops, world, ms_e2e_max)
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
     d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
 
     peaks = load_peaks()
-    achieved = w.flops / (ms * 1e-3) / 1e12  # one fold launch per step
-    traffic = profiled_traffic(w.name)
+    achieved = flops / (ms * 1e-3) / 1e12  # one fold launch per step
+    traffic = None if args.causal else profiled_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": UNIT,
                 "frac": achieved / peaks["bf16"], "traffic": traffic,
                 "kernel": "fold_sm103_kernel<128>",
@@ -305,7 +316,7 @@ def run_ours(args, w) -> None:
                 if peaks.get("bf16_sustained") else None}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.causal:
         cpu, _, _ = cpu_oracle_baseline(w, q, k, v, args.cpu_seconds)
 
     if rank == 0:
@@ -314,6 +325,7 @@ def run_ours(args, w) -> None:
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {**w.describe(), "parallelism": "replicas",
+                       **({"causal": args.causal} if args.causal else {}),
                        "l2": "inputs larger than L2 (q+k+v = "
                              f"{3 * q.numel() * q.element_size() / 2**20:.0f} MiB)"},
             "roofline": roofline, "cpu_baseline": cpu,
@@ -321,7 +333,7 @@ def run_ours(args, w) -> None:
                     "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e_max},
             "gpu_launches": args.steps, "clocks": clocks,
             "pct_of_peak": 100.0 * achieved / peaks["bf16"],
-            "exps_per_s": w.B * w.H * w.N * w.N / (ms * 1e-3),
+            "exps_per_s": (flops / (4.0 * w.d)) / (ms * 1e-3),
         }
         print(json.dumps(line))
     if world > 1:
@@ -336,6 +348,8 @@ def main() -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=4, help="workload key (default 4)")
     ap.add_argument("--heads", type=int, default=None, help="override the head count")
+    ap.add_argument("--causal", choices=["contiguous", "zigzag", "striped"], default=None,
+                    help="time ra_forward_causal with this layout instead of ra_forward")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
