@@ -236,7 +236,14 @@ def run_ours(args, w) -> None:
     lse = torch.empty(w.B, w.H, w.N, device=dev, dtype=torch.float32)
     stream = torch.cuda.current_stream()
 
-    if args.causal:
+    if args.split is not None:
+        G = args.split or ra.ra_forward_split_segments(w.B, w.H, w.N, w.d, w.P, w.dtype)
+        ws = torch.empty(ra.ra_forward_split_workspace_bytes(w.B, w.H, w.N, w.d, G), device=dev,
+                         dtype=torch.uint8)
+
+        def step():
+            ra.ra_forward_split(q, k, v, w.P, G=G, workspace=ws, out=out, lse=lse)
+    elif args.causal:
         def step():
             ra.ra_forward_causal(q, k, v, w.P, layout=args.causal, out=out, lse=lse)
     else:
@@ -326,12 +333,13 @@ def run_ours(args, w) -> None:
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {**w.describe(), "parallelism": "replicas",
                        **({"causal": args.causal} if args.causal else {}),
+                       **({"split_segments": G} if args.split is not None else {}),
                        "l2": "inputs larger than L2 (q+k+v = "
                              f"{3 * q.numel() * q.element_size() / 2**20:.0f} MiB)"},
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e_max},
-            "gpu_launches": args.steps, "clocks": clocks,
+            "gpu_launches": args.steps * (2 if args.split is not None else 1), "clocks": clocks,
             "pct_of_peak": 100.0 * achieved / peaks["bf16"],
             "exps_per_s": (flops / (4.0 * w.d)) / (ms * 1e-3),
         }
@@ -350,6 +358,8 @@ def main() -> None:
     ap.add_argument("--heads", type=int, default=None, help="override the head count")
     ap.add_argument("--causal", choices=["contiguous", "zigzag", "striped"], default=None,
                     help="time ra_forward_causal with this layout instead of ra_forward")
+    ap.add_argument("--split", type=int, default=None,
+                    help="time ra_forward_split with G segments (0 = recommended)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()

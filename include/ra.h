@@ -174,6 +174,41 @@ RA_API ra_status ra_forward_partial_causal(const void* q, const void* k, const v
                                            ra_dtype dtype, ra_stream_t stream);
 
 /*
+ * ra_forward_split -- ra_forward for problems too small to fill the GPU: the
+ * ring of every query block is split into G contiguous segments of steps
+ * that are folded in parallel into partial states, which are then merged
+ * ("Ring Attention" (bembew.net), "Global Integration"; exact by the
+ * shift invariance of "Ring Attention: the math", section "The online-softmax
+ * identity").  Same result as ra_forward up to rounding.
+ *   G          1 <= G <= min(P, RA_MAX_PARTIALS); ra_forward_split_segments
+ *              gives a choice for the current device.
+ *   workspace  caller-owned device scratch of at least
+ *              ra_forward_split_workspace_bytes(B, H, N, d, G) bytes,
+ *              256-byte aligned; overwritten (no initial value needed).
+ * Other arguments as ra_forward.  Errors: as ra_forward; RA_ERR_INVALID_ARG
+ * for a bad G, a NULL or too small workspace; RA_ERR_MISALIGNED if the
+ * workspace is not 256-byte aligned.
+ */
+RA_API ra_status ra_forward_split(const void* q, const void* k, const void* v, void* out,
+                                  float* lse, int32_t B, int32_t H, int64_t N, int32_t d,
+                                  int32_t P, int32_t G, void* workspace, int64_t workspace_bytes,
+                                  ra_dtype dtype, ra_stream_t stream);
+
+/* Scratch bytes ra_forward_split needs (-1 for invalid sizes). */
+RA_API int64_t ra_forward_split_workspace_bytes(int32_t B, int32_t H, int64_t N, int32_t d,
+                                                int32_t G);
+
+/*
+ * Segments for ra_forward_split on the current device: 1 when the plain
+ * forward already gives every SM work, else the largest G whose G x (CTAs
+ * of the plain forward) still fit in one wave of the SMs, keeping
+ * at least 32 K/V tiles (4096 keys) per segment and at most
+ * min(P, RA_MAX_PARTIALS).  bf16 only (returns 1 otherwise).
+ */
+RA_API int32_t ra_forward_split_segments(int32_t B, int32_t H, int64_t N, int32_t d, int32_t P,
+                                         ra_dtype dtype);
+
+/*
  * ra_state_init -- set a state to empty: m = -inf, l = 0, o = 0 ("Ring
  * Attention: the math", section "Accumulation math, step by step": "state = (m
  * = -inf, l = 0, o = 0)").

@@ -19,7 +19,8 @@ from . import _native
 from ._native import RA_BF16, RA_F32, RA_MAX_PARTIALS, RaStateC
 
 __all__ = ["RaError", "RaState", "ra_forward", "ra_forward_causal", "ra_forward_partial",
-           "ra_forward_partial_causal", "ra_state_init", "ra_fold", "ra_merge",
+           "ra_forward_partial_causal", "ra_forward_split", "ra_forward_split_workspace_bytes",
+           "ra_forward_split_segments", "ra_state_init", "ra_fold", "ra_merge",
            "ra_last_device_status", "new_state", "library_path"]
 
 
@@ -156,6 +157,39 @@ def ra_forward_partial_causal(q, k, v, P: int, G: int, layout: str = "contiguous
                                                    _dtype_code(q), _stream(stream))
     _check(code, "ra_forward_partial_causal")
     return partials
+
+
+def ra_forward_split_workspace_bytes(B: int, H: int, N: int, d: int, G: int) -> int:
+    return int(_native.lib().ra_forward_split_workspace_bytes(B, H, N, d, G))
+
+
+def ra_forward_split_segments(B: int, H: int, N: int, d: int, P: int, dtype) -> int:
+    code = RA_BF16 if dtype == torch.bfloat16 else RA_F32
+    return int(_native.lib().ra_forward_split_segments(B, H, N, d, P, code))
+
+
+def ra_forward_split(q, k, v, P: int, G: int | None = None, workspace=None, out=None, lse=None,
+                     stream=None):
+    """Ring split into G segments folded in parallel, then merged.
+
+    G=None takes ra_forward_split_segments' choice; `workspace` (a CUDA
+    uint8 tensor of ra_forward_split_workspace_bytes bytes) is allocated
+    when not given.  Returns (out, lse)."""
+    B, H, N, d = q.shape
+    if G is None:
+        G = ra_forward_split_segments(B, H, N, d, P, q.dtype)
+    nbytes = ra_forward_split_workspace_bytes(B, H, N, d, G)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, N, device=q.device, dtype=torch.float32)
+    code = _native.lib().ra_forward_split(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H,
+                                          N, d, P, G, _ptr(workspace), workspace.numel(),
+                                          _dtype_code(q), _stream(stream))
+    _check(code, "ra_forward_split")
+    return out, lse
 
 
 def ra_state_init(state: RaState, stream=None) -> RaState:

@@ -37,6 +37,10 @@ PROTOTYPES = {
     "ra_forward_partial": (_I32, [_P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _SP, _I32, _P]),
     "ra_forward_partial_causal": (_I32, [_P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _SP,
                                          _I32, _I32, _P]),
+    "ra_forward_split": (_I32, [_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _P, _I64,
+                                _I32, _P]),
+    "ra_forward_split_workspace_bytes": (_I64, [_I32, _I32, _I64, _I32, _I32]),
+    "ra_forward_split_segments": (_I32, [_I32, _I32, _I64, _I32, _I32, _I32]),
     "ra_state_init": (_I32, [_SP, _P]),
     "ra_fold": (_I32, [_SP, _P, _P, _P, _I64, _I64, _I32, _P]),
     "ra_merge": (_I32, [_SP, _I32, _P, _P, _I32, _P]),

@@ -249,6 +249,55 @@ ra_status partial_impl(const void* q, const void* k, const void* v, int32_t B, i
 }
 
 }  // namespace
+
+int64_t split_workspace_bytes(int64_t rows, int32_t d, int32_t G) {
+  auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
+  return static_cast<int64_t>(G) * (2 * up(rows * 4) + up(rows * static_cast<int64_t>(d) * 4));
+}
+
+ra_status split_forward(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int32_t B, int32_t H, int64_t N, int32_t d, int32_t P, int32_t G,
+                        void* workspace, int64_t workspace_bytes, ra_dtype dtype,
+                        cudaStream_t stream) {
+  FoldArgs a;
+  ra_status st = check_attention(q, k, v, B, H, N, d, P, dtype, &a);
+  if (st != RA_OK) return st;
+  if (G < 1 || G > RA_MAX_PARTIALS || G > P) return RA_ERR_INVALID_ARG;
+  const int64_t rows = a.slices * a.nq;
+  if (rows == 0) return RA_OK;
+  if (!out || !lse || !workspace || workspace_bytes < 0) return RA_ERR_INVALID_ARG;
+  if (!aligned(out, dtype == RA_BF16 ? 16 : 4) || !aligned(lse, 4) || !aligned(workspace, 256))
+    return RA_ERR_MISALIGNED;
+  if (workspace_bytes < split_workspace_bytes(rows, d, G)) return RA_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if ((st = current_device(&di)) != RA_OK) return st;
+  // carve the G partial states out of the workspace
+  auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
+  char* p = static_cast<char*>(workspace);
+  MergeArgs mg{};
+  for (int g = 0; g < G; ++g) {
+    a.part.m[g] = reinterpret_cast<float*>(p);
+    p += up(rows * 4);
+    a.part.l[g] = reinterpret_cast<float*>(p);
+    p += up(rows * 4);
+    a.part.o[g] = reinterpret_cast<float*>(p);
+    p += up(rows * static_cast<int64_t>(d) * 4);
+  }
+  mg.part = a.part;
+  a.mode = kPartial;
+  a.G = G;
+  a.status = di.status;
+  if ((st = run_fold(a, dtype, stream)) != RA_OK) return st;
+  mg.G = G;
+  mg.rows = rows;
+  mg.d = d;
+  mg.out = out;
+  mg.lse = lse;
+  mg.out_bf16 = dtype == RA_BF16 ? 1 : 0;
+  mg.vec4 = (d % 4 == 0 && aligned(out, dtype == RA_BF16 ? 8 : 16)) ? 1 : 0;
+  return launched(launch_merge(mg, stream));
+}
+
 }  // namespace ra
 
 extern "C" {
@@ -280,6 +329,38 @@ RA_API ra_status ra_forward_partial_causal(const void* q, const void* k, const v
                                            int32_t G, const ra_state* partials, ra_layout layout,
                                            ra_dtype dtype, ra_stream_t stream) {
   return partial_impl(q, k, v, B, H, N, d, P, G, partials, true, layout, dtype, stream);
+}
+
+RA_API int64_t ra_forward_split_workspace_bytes(int32_t B, int32_t H, int64_t N, int32_t d,
+                                                int32_t G) {
+  if (B < 0 || H < 0 || N < 0 || d < 1 || G < 1 || G > RA_MAX_PARTIALS) return -1;
+  return split_workspace_bytes(static_cast<int64_t>(B) * H * N, d, G);
+}
+
+RA_API int32_t ra_forward_split_segments(int32_t B, int32_t H, int64_t N, int32_t d, int32_t P,
+                                         ra_dtype dtype) {
+  if (B < 1 || H < 1 || N < 1 || d < 1 || P < 1 || N % P != 0 || dtype != RA_BF16) return 1;
+  const int64_t c = N / P;
+  if (c % 128 != 0) return 1;
+  const int64_t units = static_cast<int64_t>(B) * H * P * ((c / 128 + 1) / 2);
+  const int64_t sms = device_sm_count();
+  if (units >= sms) return 1;
+  int64_t G = sms / units;  // the largest split that still runs in one wave
+  // A segment needs enough K/V tiles to pay for its partial state and the
+  // merge: at least 32 of them.
+  const int64_t max_by_tiles = (N / 128) / 32;
+  if (G > max_by_tiles) G = max_by_tiles;
+  if (G > P) G = P;
+  if (G > RA_MAX_PARTIALS) G = RA_MAX_PARTIALS;
+  return static_cast<int32_t>(G < 1 ? 1 : G);
+}
+
+RA_API ra_status ra_forward_split(const void* q, const void* k, const void* v, void* out,
+                                  float* lse, int32_t B, int32_t H, int64_t N, int32_t d,
+                                  int32_t P, int32_t G, void* workspace, int64_t workspace_bytes,
+                                  ra_dtype dtype, ra_stream_t stream) {
+  return split_forward(q, k, v, out, lse, B, H, N, d, P, G, workspace, workspace_bytes, dtype,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 RA_API ra_status ra_state_init(const ra_state* st, ra_stream_t stream) {

@@ -93,4 +93,15 @@ constexpr int kStatusTimeout = 1;
 // Number of SMs of the current device (cached).
 int device_sm_count();
 
+// Bytes of scratch for G partial states of `rows` rows of width d: per
+// segment m [rows], l [rows], o [rows, d] fp32, each 256-byte aligned.
+int64_t split_workspace_bytes(int64_t rows, int32_t d, int32_t G);
+
+// The split forward: fold G segments of the ring into partial states held in
+// `workspace`, then merge them into out and lse (all on `stream`).
+ra_status split_forward(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int32_t B, int32_t H, int64_t N, int32_t d, int32_t P, int32_t G,
+                        void* workspace, int64_t workspace_bytes, ra_dtype dtype,
+                        cudaStream_t stream);
+
 }  // namespace ra

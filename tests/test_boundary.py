@@ -109,3 +109,21 @@ def test_causal_validation(L):
     assert fc(layout=0, N=2048 * 128, P=2048) == _native.RA_ERR_UNSUPPORTED  # bf16 P > 1024
     assert fc(layout=2, N=1024, P=8) == _native.RA_ERR_ARCH  # valid: stops at the device check
     assert fc(layout=1, N=16, P=4, dt=F32) == _native.RA_ERR_ARCH
+
+
+def test_split_validation(L):
+    need = L.ra_forward_split_workspace_bytes(1, 2, 1024, 64, 4)
+    rows = 2 * 1024
+    up = lambda x: (x + 255) // 256 * 256
+    assert need == 4 * (2 * up(rows * 4) + up(rows * 64 * 4))
+    assert L.ra_forward_split_workspace_bytes(1, 2, 1024, 64, 0) == -1
+    assert L.ra_forward_split_workspace_bytes(1, 2, 1024, 64, 65) == -1
+
+    def fs(ws=A, nbytes=need, G=4, P=4):
+        return L.ra_forward_split(A, A, A, A, A, 1, 2, 1024, 64, P, G, ws, nbytes, BF16, None)
+    assert fs(ws=None) == _native.RA_ERR_INVALID_ARG
+    assert fs(nbytes=need - 1) == _native.RA_ERR_INVALID_ARG
+    assert fs(ws=A + 16) == _native.RA_ERR_MISALIGNED   # needs 256-byte alignment
+    assert fs(G=0) == _native.RA_ERR_INVALID_ARG
+    assert fs(G=8, P=4) == _native.RA_ERR_INVALID_ARG   # G > P
+    assert fs() == _native.RA_ERR_ARCH                  # valid; no device here
