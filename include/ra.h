@@ -208,6 +208,36 @@ RA_API int64_t ra_forward_split_workspace_bytes(int32_t B, int32_t H, int64_t N,
 RA_API int32_t ra_forward_split_segments(int32_t B, int32_t H, int64_t N, int32_t d, int32_t P,
                                          ra_dtype dtype);
 
+/* Size of the fixed device scratch of ra_forward_split_noalloc: 32 MiB. */
+#define RA_SPLIT_NOALLOC_SCRATCH_BYTES (32ll * 1024 * 1024)
+
+/*
+ * ra_forward_split_noalloc -- ra_forward_split for callers that cannot
+ * allocate device memory.  The pages have no counterpart; this is a service
+ * of the library.  Some callers may not call cudaMalloc once they run: a
+ * plug-in inside a host whose memory pool already owns the device, or a
+ * latency-bound loop that cannot accept an allocation's implicit device
+ * synchronisation.  They pass only inputs and outputs; the G partial states
+ * live in one library-owned device array of RA_SPLIT_NOALLOC_SCRATCH_BYTES
+ * that every GPU which loads the library holds until the process exits.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the array: calls that overlap on the GPU
+ *     (other streams, unordered host threads) race and corrupt each other.
+ *     Nothing in it needs to start at zero; each call writes all it reads.
+ * Arguments as ra_forward_split, without the workspace.
+ * Errors: as ra_forward_split; RA_ERR_UNSUPPORTED when the partial states
+ * (ra_forward_split_workspace_bytes(B, H, N, d, G)) exceed
+ * RA_SPLIT_NOALLOC_SCRATCH_BYTES -- nothing is launched then; use
+ * ra_forward_split with a caller workspace, or a smaller G.
+ */
+RA_API ra_status ra_forward_split_noalloc(const void* q, const void* k, const void* v,
+                                          void* out, float* lse, int32_t B, int32_t H, int64_t N,
+                                          int32_t d, int32_t P, int32_t G, ra_dtype dtype,
+                                          ra_stream_t stream);
+
 /*
  * ra_state_init -- set a state to empty: m = -inf, l = 0, o = 0 ("Ring
  * Attention: the math", section "Accumulation math, step by step": "state = (m

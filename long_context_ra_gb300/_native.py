@@ -16,6 +16,7 @@ RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_MISALIGNED, RA_ERR_ARCH, R
 RA_F32, RA_BF16 = 0, 1
 RA_LAYOUTS = {"contiguous": 0, "zigzag": 1, "striped": 2}
 RA_MAX_PARTIALS = 64
+RA_SPLIT_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 class RaStateC(ctypes.Structure):
@@ -40,6 +41,8 @@ PROTOTYPES = {
     "ra_forward_split": (_I32, [_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _P, _I64,
                                 _I32, _P]),
     "ra_forward_split_workspace_bytes": (_I64, [_I32, _I32, _I64, _I32, _I32]),
+    "ra_forward_split_noalloc": (_I32, [_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32,
+                                        _I32, _P]),
     "ra_forward_split_segments": (_I32, [_I32, _I32, _I64, _I32, _I32, _I32]),
     "ra_state_init": (_I32, [_SP, _P]),
     "ra_fold": (_I32, [_SP, _P, _P, _P, _I64, _I64, _I32, _P]),

@@ -127,3 +127,13 @@ def test_split_validation(L):
     assert fs(G=0) == _native.RA_ERR_INVALID_ARG
     assert fs(G=8, P=4) == _native.RA_ERR_INVALID_ARG   # G > P
     assert fs() == _native.RA_ERR_ARCH                  # valid; no device here
+
+
+def test_noalloc_split_rejects_oversize_without_device(L):
+    # the size check comes before any device work
+    assert L.ra_forward_split_noalloc(A, A, A, A, A, 1, 1, 65536, 128, 8, 8, BF16, None) == \
+        _native.RA_ERR_UNSUPPORTED
+    assert L.ra_forward_split_noalloc(A, A, A, A, A, 1, 1, 65536, 128, 8, 0, BF16, None) == \
+        _native.RA_ERR_INVALID_ARG
+    assert L.ra_forward_split_noalloc(A, A, A, A, A, 1, 2, 4096, 128, 8, 2, BF16, None) == \
+        _native.RA_ERR_ARCH
