@@ -36,6 +36,10 @@
 //       of c/2 positions, each in increasing order) and striped (block j =
 //       positions j, j + P, j + 2P, ...).  A block's keys are folded in this
 //       local order; masked keys take no part (as a score of -inf would).
+//   R13 Backward: the loss is L = sum(dO * out); P is recomputed from the
+//       forward's lse; the row term D = sum(dO * out) ([C] step 6 names the
+//       ring and the travelling accumulators, not the formulas, which are the
+//       derivative of the forward written out).
 //
 // Every value is computed in double precision.  Inputs are converted exactly
 // (f32 -> f64 and bf16 -> f64 are exact).  No blocking, fusion or reordering
@@ -424,6 +428,102 @@ int ora_merge(const double* m, const double* l, const double* o, int64_t G, int6
     if (o_out)
       for (int e = 0; e < d; ++e) o_out[r * d + e] = st.o[e];
   }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Backward pass ([C] step 6: "Run the backward pass on the same ring": the
+// key-value blocks travel with their gradient accumulators).  For the loss
+// L = sum(dO * out), with P = softmax(tau Q K^T) per row:
+//   dV = P^T dO;  dP = dO V^T;  D_r = sum_e dO_re * out_re (= sum_j P_rj dP_rj);
+//   dS = P * (dP - D);  dQ = tau dS K;  dK = tau dS^T Q.
+// P is recomputed from the forward's lse: P_rj = exp(tau q_r . k_j - lse_r).
+// ---------------------------------------------------------------------------
+
+// Ring-order backward of one (b, h) slice, fp64.  Query block i (device i)
+// keeps Q_i, dO_i, out_i, lse_i and its dQ_i; at step t it holds key block
+// j = (i - t) mod P together with that block's dK_j, dV_j accumulators and
+// adds the contributions of the pair (i, j).  Inputs are converted to fp64;
+// lse and out are the forward's (any precision, given as doubles).
+static void backward_slice(const std::vector<double>& q, const std::vector<double>& k,
+                           const std::vector<double>& v, const std::vector<double>& out,
+                           const std::vector<double>& dout, const std::vector<double>& lse,
+                           int64_t N, int d, int64_t P, int causal, int layout,
+                           std::vector<double>& dq, std::vector<double>& dk,
+                           std::vector<double>& dv) {
+  const double tau = 1.0 / std::sqrt(static_cast<double>(d));
+  const int64_t c = N / P;
+  std::vector<double> D(static_cast<size_t>(N));
+  for (int64_t r = 0; r < N; ++r) {
+    double acc = 0.0;
+    for (int e = 0; e < d; ++e) acc += dout[r * d + e] * out[r * d + e];
+    D[r] = acc;
+  }
+  for (int64_t i = 0; i < P; ++i) {
+    for (int64_t t = 0; t < P; ++t) {
+      const int64_t j = ring_block(i, t, P);
+      for (int64_t x = 0; x < c; ++x) {
+        const int64_t r = token_pos(layout, i, x, P, c);  // query position
+        for (int64_t y = 0; y < c; ++y) {
+          const int64_t n = token_pos(layout, j, y, P, c);  // key position
+#if ORA_MUTANT == 7
+          if (causal && n >= r) continue;
+#else
+          if (causal && n > r) continue;
+#endif
+          double s = 0.0;
+          for (int e = 0; e < d; ++e) s += q[r * d + e] * k[n * d + e];
+          const double p = std::exp(s * tau - lse[r]);
+          double dp = 0.0;
+          for (int e = 0; e < d; ++e) dp += dout[r * d + e] * v[n * d + e];
+#if ORA_MUTANT == 8
+          const double ds = p * dp;  // planted: the row term D dropped
+#else
+          const double ds = p * (dp - D[r]);
+#endif
+          for (int e = 0; e < d; ++e) {
+            dq[r * d + e] += tau * ds * k[n * d + e];
+            dk[n * d + e] += tau * ds * q[r * d + e];
+            dv[n * d + e] += p * dout[r * d + e];
+          }
+        }
+      }
+    }
+  }
+}
+
+// Backward of ring attention for every (b, h) slice (threads over slices).
+//   q, k, v: [BH, N, d] of `dtype`; out, dout: [BH, N, d] doubles; lse: [BH*N]
+//   doubles (the forward's outputs and the incoming gradient).
+//   dq, dk, dv: [BH, N, d] doubles (written).
+int ora_backward(const void* q, const void* k, const void* v, int dtype, const double* out,
+                 const double* dout, const double* lse, int64_t BH, int64_t N, int d, int64_t P,
+                 int causal, int layout, double* dq, double* dk, double* dv, int threads) {
+  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return 1;
+  if (BH < 0 || N < 0 || d < 1 || P < 1 || bad_dtype(dtype)) return 1;
+  if (layout < ORA_CONTIGUOUS || layout > ORA_STRIPED) return 1;
+  if (N % P != 0 || (layout == ORA_ZIGZAG && (N / P) % 2 != 0)) return 2;
+  parallel_for(BH, threads, [&](int64_t bh) {
+    const size_t sz = static_cast<size_t>(N) * d;
+    std::vector<double> qs(sz), ks(sz), vs(sz), os(sz), dos(sz), ls(static_cast<size_t>(N));
+    std::vector<double> gq(sz, 0.0), gk(sz, 0.0), gv(sz, 0.0);
+    for (int64_t r = 0; r < N; ++r) {
+      load_row(q, dtype, bh * N + r, d, qs.data() + r * d);
+      load_row(k, dtype, bh * N + r, d, ks.data() + r * d);
+      load_row(v, dtype, bh * N + r, d, vs.data() + r * d);
+      ls[r] = lse[bh * N + r];
+    }
+    for (size_t x = 0; x < sz; ++x) {
+      os[x] = out[bh * sz + x];
+      dos[x] = dout[bh * sz + x];
+    }
+    backward_slice(qs, ks, vs, os, dos, ls, N, d, P, causal, layout, gq, gk, gv);
+    for (size_t x = 0; x < sz; ++x) {
+      dq[bh * sz + x] = gq[x];
+      dk[bh * sz + x] = gk[x];
+      dv[bh * sz + x] = gv[x];
+    }
+  });
   return 0;
 }
 

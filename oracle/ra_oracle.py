@@ -65,10 +65,12 @@ class Oracle:
         L.ora_ring.argtypes = [_P, _P, _P, _I32, _I64, _I64, _I32, _I64, _P, _I64, _I64,
                                _I64, _I32, _I32, _P, _I64, _P, _P, _P, _P, _P, _I32]
         L.ora_layout_positions.argtypes = [_I32, _I64, _I64, _P]
+        L.ora_backward.argtypes = [_P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I32, _I64, _I32,
+                                   _I32, _P, _P, _P, _I32]
         L.ora_fold.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I32, _I32]
         L.ora_merge.argtypes = [_P, _P, _P, _I64, _I64, _I32, _P, _P, _P, _P, _P]
         for f in (L.ora_ring_order, L.ora_dense, L.ora_ring, L.ora_fold, L.ora_merge,
-                  L.ora_layout_positions):
+                  L.ora_layout_positions, L.ora_backward):
             f.restype = _I32
         L.ora_mutant.restype = _I32
         self.mutant = L.ora_mutant()
@@ -163,6 +165,26 @@ class Oracle:
                                _DTYPES[dtype], batch, R, Nk, d, self.threads)
         self._check(rc, "fold")
         return m, l, o
+
+    def backward(self, q, k, v, out, dout, lse, P, dtype="f64", causal=False,
+                 layout="contiguous"):
+        """Gradients (dq, dk, dv) of L = sum(dout * out); q, k, v, out, dout:
+        [BH, N, d]; lse: [BH, N] (the forward's)."""
+        BH, N, d = q.shape
+        qa, qp = self._arr(q, dtype)
+        ka, kp = self._arr(k, dtype)
+        va, vp = self._arr(v, dtype)
+        oa = np.ascontiguousarray(out, dtype=np.float64)
+        da = np.ascontiguousarray(dout, dtype=np.float64)
+        la = np.ascontiguousarray(lse, dtype=np.float64)
+        dq = np.empty((BH, N, d), np.float64)
+        dk = np.empty((BH, N, d), np.float64)
+        dv = np.empty((BH, N, d), np.float64)
+        rc = self.lib.ora_backward(qp, kp, vp, _DTYPES[dtype], oa.ctypes.data, da.ctypes.data,
+                                   la.ctypes.data, BH, N, d, P, int(causal), LAYOUTS[layout],
+                                   dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, self.threads)
+        self._check(rc, "backward")
+        return dq, dk, dv
 
     def merge(self, m, l, o, state=False):
         """m, l: [G, R]; o: [G, R, d].  Returns out, lse (and the merged state)."""

@@ -460,4 +460,67 @@ def pin_causal_segments_merge(O):
         assert np.abs(lse - full_lse).max() <= 1e-12
 
 
+# ---------------------------------------------------------------------------
+# backward ("Ring attention, explained", step 6: the same ring, with the K/V
+# blocks carrying their gradient accumulators)
+# ---------------------------------------------------------------------------
+def _loss(O, q, k, v, dout, causal):
+    out, _ = O.dense(q, k, v, causal=causal)
+    return float((out.reshape(dout.shape) * dout).sum())
+
+
+def pin_backward_finite_differences(O):
+    """Every gradient against central differences of the forward oracle."""
+    rng = np.random.default_rng(30)
+    BH, N, d = 2, 12, 3
+    eps = 1e-5
+    for causal, layout, P in ((False, "contiguous", 3), (True, "zigzag", 2), (True, "striped", 4)):
+        q, k, v = _rand(rng, BH, N, d, 1.5)
+        dout = rng.standard_normal((BH, N, d))
+        out, lse = O.dense(q, k, v, causal=causal)
+        grads = O.backward(q, k, v, out.reshape(BH, N, d), dout, lse.reshape(BH, N), P=P,
+                           causal=causal, layout=layout)
+        for which, (x, g) in enumerate(zip((q, k, v), grads)):
+            for _ in range(6):
+                idx = tuple(int(rng.integers(0, s)) for s in x.shape)
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += eps
+                xm[idx] -= eps
+                args_p = [q, k, v]
+                args_m = [q, k, v]
+                args_p[which], args_m[which] = xp, xm
+                fd = (_loss(O, *args_p, dout, causal) - _loss(O, *args_m, dout, causal)) / (2 * eps)
+                assert abs(g[idx] - fd) <= 1e-7 * max(1.0, abs(fd)), (which, idx, g[idx], fd)
+
+
+def pin_backward_ring_order_invariance(O):
+    """Gradients do not depend on P or on the layout (the ring only reorders)."""
+    rng = np.random.default_rng(31)
+    BH, N, d = 1, 16, 4
+    q, k, v = _rand(rng, BH, N, d, 1.5)
+    dout = rng.standard_normal((BH, N, d))
+    for causal in (False, True):
+        out, lse = O.dense(q, k, v, causal=causal)
+        base = O.backward(q, k, v, out.reshape(BH, N, d), dout, lse.reshape(BH, N), P=1,
+                          causal=causal)
+        for layout, P in (("contiguous", 4), ("zigzag", 2), ("striped", 8)):
+            g = O.backward(q, k, v, out.reshape(BH, N, d), dout, lse.reshape(BH, N), P=P,
+                           causal=causal, layout=layout)
+            for a, b in zip(base, g):
+                assert np.abs(a - b).max() <= 1e-12
+
+
+def pin_backward_identical_keys_dv(O):
+    """Identical keys give uniform weights 1/N, so dV_j = mean_i dO_i."""
+    rng = np.random.default_rng(32)
+    BH, N, d = 1, 10, 3
+    q = rng.standard_normal((BH, N, d))
+    k = np.broadcast_to(rng.standard_normal((BH, 1, d)), (BH, N, d)).copy()
+    v = rng.standard_normal((BH, N, d))
+    dout = rng.standard_normal((BH, N, d))
+    out, lse = O.dense(q, k, v)
+    _, _, dv = O.backward(q, k, v, out.reshape(BH, N, d), dout, lse.reshape(BH, N), P=2)
+    assert np.abs(dv - dout.mean(axis=1, keepdims=True)).max() <= 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -11,7 +11,7 @@ import pytest
 import oracle_pins
 from oracle import ra_oracle
 
-MUTANTS = [1, 2, 3, 4, 5, 6, 7]
+MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
