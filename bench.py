@@ -32,6 +32,7 @@ sys.path.insert(0, str(ROOT))
 METRIC = "attention TFLOP/s (4·B·H·N²·d) at 1 GB300 and % of dense bf16 tensor peak"
 UNIT = "TFLOP/s"
 KERNEL_SOURCES = ["long_context_ra_gb300/csrc/ra_fold_sm103.cu",
+                  "long_context_ra_gb300/csrc/sm103_pipeline.cuh",
                   "long_context_ra_gb300/csrc/sm103_ptx.cuh"]
 
 

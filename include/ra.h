@@ -239,6 +239,30 @@ RA_API ra_status ra_forward_split_noalloc(const void* q, const void* k, const vo
                                           ra_stream_t stream);
 
 /*
+ * ra_backward -- gradients of ring attention ("Ring attention, explained",
+ * step 6: the backward runs on the same ring, the key-value blocks carrying
+ * their gradient accumulators).  For the loss L = sum(dout * out):
+ *     P = exp(tau q.k - lse)  (recomputed from the forward's lse)
+ *     dV = P^T dout;  dP = dout V^T;  dS = P * (dP - D),  D = rowsum(dout * out)
+ *     dQ = tau dS K;  dK = tau dS^T Q
+ * dK and dV of block j are accumulated while the block visits the query
+ * blocks (j + t) mod P; dQ of block i while it meets the key blocks
+ * (i - t) mod P.  No atomics: every gradient row is written once.
+ *   q, k, v, out, dout  [B, H, N, d] of `dtype` (out and lse from ra_forward).
+ *   lse         [B, H, N] fp32.
+ *   dq, dk, dv  [B, H, N, d] of `dtype` (written).
+ *   workspace   caller-owned fp32 scratch of 2 * B * H * N floats, 16-byte
+ *               aligned; receives D and -lse * log2(e).
+ * Size and alignment rules as ra_forward (bf16: d in {64, 128}, c % 128 == 0,
+ * 16-byte aligned tensors).  Non-causal.
+ * Errors: as ra_forward; RA_ERR_INVALID_ARG for a NULL buffer.
+ */
+RA_API ra_status ra_backward(const void* q, const void* k, const void* v, const void* out,
+                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                             float* workspace, int32_t B, int32_t H, int64_t N, int32_t d,
+                             int32_t P, ra_dtype dtype, ra_stream_t stream);
+
+/*
  * ra_state_init -- set a state to empty: m = -inf, l = 0, o = 0 ("Ring
  * Attention: the math", section "Accumulation math, step by step": "state = (m
  * = -inf, l = 0, o = 0)").

@@ -20,7 +20,7 @@ from ._native import RA_BF16, RA_F32, RA_MAX_PARTIALS, RaStateC
 
 __all__ = ["RaError", "RaState", "ra_forward", "ra_forward_causal", "ra_forward_partial",
            "ra_forward_partial_causal", "ra_forward_split", "ra_forward_split_workspace_bytes",
-           "ra_forward_split_segments", "ra_state_init", "ra_fold", "ra_merge",
+           "ra_forward_split_segments", "ra_backward", "ra_state_init", "ra_fold", "ra_merge",
            "ra_last_device_status", "new_state", "library_path"]
 
 
@@ -190,6 +190,22 @@ def ra_forward_split(q, k, v, P: int, G: int | None = None, workspace=None, out=
                                           _dtype_code(q), _stream(stream))
     _check(code, "ra_forward_split")
     return out, lse
+
+
+def ra_backward(q, k, v, out, dout, lse, P: int, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of L = sum(dout * out) for ra_forward's out/lse."""
+    B, H, N, d = q.shape
+    for t in (k, v, out, dout):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError("q, k, v, out, dout must share shape and dtype")
+    if workspace is None:
+        workspace = torch.empty(2 * B * H * N, device=q.device, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    code = _native.lib().ra_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), B, H, N, d, P,
+                                     _dtype_code(q), _stream(stream))
+    _check(code, "ra_backward")
+    return dq, dk, dv
 
 
 def ra_state_init(state: RaState, stream=None) -> RaState:

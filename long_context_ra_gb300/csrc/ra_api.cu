@@ -363,6 +363,54 @@ RA_API ra_status ra_forward_split(const void* q, const void* k, const void* v, v
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
+RA_API ra_status ra_backward(const void* q, const void* k, const void* v, const void* out,
+                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                             float* workspace, int32_t B, int32_t H, int64_t N, int32_t d,
+                             int32_t P, ra_dtype dtype, ra_stream_t stream) {
+  FoldArgs f;
+  ra_status st = check_attention(q, k, v, B, H, N, d, P, dtype, &f);
+  if (st != RA_OK) return st;
+  const int64_t rows = f.slices * f.nq;
+  if (rows == 0) return RA_OK;
+  if (!out || !dout || !lse || !dq || !dk || !dv || !workspace) return RA_ERR_INVALID_ARG;
+  const uintptr_t al = dtype == RA_BF16 ? 16 : 4;
+  if (!aligned(out, al) || !aligned(dout, al) || !aligned(dq, al) || !aligned(dk, al) ||
+      !aligned(dv, al) || !aligned(lse, 4) || !aligned(workspace, 16))
+    return RA_ERR_MISALIGNED;
+  DeviceInfo di;
+  if ((st = current_device(&di)) != RA_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  BackwardArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.dout = dout;
+  a.lse = lse;
+  a.delta = workspace;
+  a.nl = workspace + rows;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.slices = f.slices;
+  a.N = N;
+  a.d = d;
+  a.P = P;
+  a.tau = f.tau;
+  a.scale_log2 = f.scale_log2;
+  a.status = di.status;
+  if ((st = launched(launch_delta(out, dout, lse, workspace, workspace + rows, rows, d,
+                                  dtype == RA_BF16, s))) != RA_OK)
+    return st;
+  if (dtype == RA_F32) return launched(launch_backward_f32(a, s));
+  if ((st = get_encoder()) != RA_OK) return st;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((st = make_map(&tq, q, rows, d)) != RA_OK) return st;
+  if ((st = make_map(&tk, k, rows, d)) != RA_OK) return st;
+  if ((st = make_map(&tv, v, rows, d)) != RA_OK) return st;
+  if ((st = make_map(&tdo, dout, rows, d)) != RA_OK) return st;
+  return launched(launch_backward_sm103(a, tq, tk, tv, tdo, s));
+}
+
 RA_API ra_status ra_state_init(const ra_state* st, ra_stream_t stream) {
   if (!state_ok(st)) return RA_ERR_INVALID_ARG;
   if (!aligned(st->m, 4) || !aligned(st->l, 4) || !aligned(st->o, 4)) return RA_ERR_MISALIGNED;

@@ -1,0 +1,557 @@
+// Tensor-core backward kernels for bf16 inputs on sm_103a (GB300).
+//
+// The backward of ring attention runs on the same ring as the forward
+// ("Ring attention, explained", step 6): the key-value blocks travel with
+// their gradient accumulators.  For the loss L = sum(dO * out):
+//   P = exp(tau Q K^T - lse)   (recomputed from the forward's lse)
+//   dP = dO V^T;  dS = P * (dP - D),  D = rowsum(dO * out)
+//   dV = P^T dO;  dK = tau dS^T Q;  dQ = tau dS K
+// Two kernels, no atomics:
+//   dkv_kernel  one 128-key tile of block j per CTA; at ring step t the block
+//               is on device i = (j + t) mod P, so the CTA walks the query
+//               tiles of those blocks.  TMEM: S^T [0,128), dP^T [128,256),
+//               dV [256, 256+D), dK [256+D, 256+2D).  Per query tile:
+//               S^T = K Q^T and dP^T = V dO^T (SS MMAs), the elementwise
+//               warps turn them into P^T and dS^T (bf16, written over the
+//               first 64 columns of S^T and dP^T), then dV += P^T dO and
+//               dK += dS^T Q (A operand from TMEM).
+//   dq_kernel   one 128-query tile per CTA walking the key tiles in the
+//               forward's ring order (i - t) mod P.  TMEM: S [0,128),
+//               dP [128,256), dQ [256, 256+D).  S = Q K^T, dP = dO V^T,
+//               dS -> TMEM, dQ += dS K.
+// The row terms come precomputed per query row: D and nl = -lse * log2(e)
+// (so that p = exp2(s * tau * log2(e) + nl)).
+//
+// Warp roles (256 threads): warps 0-3 elementwise (thread = tile row = TMEM
+// lane), warp 4 TMA producer, warp 5 TMEM allocator and MMA issuer, warps 6-7
+// idle.  Every wait is bounded (see sm103_pipeline.cuh).
+
+#include <cmath>
+
+#include "ra_internal.h"
+#include "sm103_pipeline.cuh"
+#include "sm103_ptx.cuh"
+
+namespace ra {
+namespace {
+
+using namespace ptx;
+using namespace sm103;
+
+constexpr int kThreads = 256;
+constexpr int kLoadWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kStages = 2;
+
+template <int D>
+struct Tiles {
+  static constexpr int kBoxBytes = kBM * 128;  // 128 rows x 64 bf16
+  static constexpr int kTileBytes = kBM * D * 2;
+  static constexpr int kRowBytes = kBM * 4;  // one fp32 value per tile row
+};
+
+// 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+template <int D>
+__device__ __forceinline__ void load_tile2d(uint32_t dst, const CUtensorMap* map, int64_t row,
+                                            uint32_t bar) {
+#pragma unroll
+  for (int b = 0; b < D / 64; ++b)
+    tma_load_2d(dst + b * Tiles<D>::kBoxBytes, map, b * 64, static_cast<int32_t>(row), bar);
+}
+
+// D[tmem] = A B^T over d: 128 x 128 x D, both operands K-major in SMEM.
+template <int D>
+__device__ __forceinline__ void mma_nt(uint32_t d_tmem, uint64_t da, uint64_t db) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = desc_step((kk / 4) * Tiles<D>::kBoxBytes + (kk % 4) * 32);
+    mma_bf16_ss(d_tmem, da + off, db + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// D[tmem] (+)= A[tmem] B over 128 rows of B: A is 128 x 128 bf16 packed in
+// TMEM (8 columns per 16 values), B an MN-major 128 x D tile in SMEM.
+template <int D>
+__device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint64_t db,
+                                       uint32_t accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, true);
+  mma_bf16_ts(d_tmem, a_tmem, db, idesc, accumulate);
+#pragma unroll
+  for (int kk = 1; kk < kBN / 16; ++kk)
+    mma_bf16_ts(d_tmem, a_tmem + kk * 8, db + desc_step(kk * 16 * 128), idesc, 1u);
+}
+
+// Elementwise step on one tile row (this thread's TMEM lane): from the 128
+// scores s (TMEM columns of tS) and dp (columns of tP) make
+//   p = exp2(s * sl2 + nl),  ds = p * (dp - Dr)
+// where nl and Dr are per column (dkv kernel: per query, from SMEM) or per
+// row (dq kernel: scalars).  p (if kWriteP) and ds are rounded to bf16 pairs
+// and written over the first 64 columns of tS and tP.
+template <bool kPerColumn, bool kWriteP>
+__device__ __forceinline__ void elementwise(uint32_t tS, uint32_t tP, float sl2, const float* nl,
+                                            const float* dd, float nl_row, float d_row) {
+#pragma unroll
+  for (int c = 0; c < kBN; c += 32) {
+    uint32_t s[32], g[32];
+    tmem_ld32(tS + c, s);
+    tmem_ld32(tP + c, g);
+    tmem_ld_wait();
+    reg_fence(s, 32);
+    reg_fence(g, 32);
+    float ncol[kPerColumn ? 32 : 1], dcol[kPerColumn ? 32 : 1];
+    if (kPerColumn) {
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(nl + c + e);
+        const float4 y = *reinterpret_cast<const float4*>(dd + c + e);
+        ncol[e] = x.x, ncol[e + 1] = x.y, ncol[e + 2] = x.z, ncol[e + 3] = x.w;
+        dcol[e] = y.x, dcol[e + 1] = y.y, dcol[e + 2] = y.z, dcol[e + 3] = y.w;
+      }
+    }
+    uint32_t pk[16], dk[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      float n0 = nl_row, n1 = nl_row, d0 = d_row, d1 = d_row;
+      if (kPerColumn) {
+        n0 = ncol[e];
+        n1 = ncol[e + 1];
+        d0 = dcol[e];
+        d1 = dcol[e + 1];
+      }
+      const float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, n0));
+      const float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, n1));
+      const float ds0 = p0 * (__uint_as_float(g[e]) - d0);
+      const float ds1 = p1 * (__uint_as_float(g[e + 1]) - d1);
+      pk[e / 2] = pack_bf16x2(p0, p1);
+      dk[e / 2] = pack_bf16x2(ds0, ds1);
+    }
+    // columns [c/2, c/2 + 16) of tS / tP were read by this or an earlier chunk
+    if (kWriteP) tmem_st16(tS + c / 2, pk);
+    tmem_st16(tP + c / 2, dk);
+  }
+}
+
+// Store one TMEM row segment of 32 fp32 columns, times `scale`, as bf16.
+__device__ __forceinline__ void store_row_bf16(uint32_t taddr, uint16_t* dst, float scale) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+  tmem_ld_wait();
+  reg_fence(r, 32);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    uint4 w;
+    w.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * scale, __uint_as_float(r[8 * e + 1]) * scale);
+    w.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * scale, __uint_as_float(r[8 * e + 3]) * scale);
+    w.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * scale, __uint_as_float(r[8 * e + 5]) * scale);
+    w.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * scale, __uint_as_float(r[8 * e + 7]) * scale);
+    d4[e] = w;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dK, dV: one key tile per CTA
+// ---------------------------------------------------------------------------
+template <int D>
+struct DkvLayout {
+  using T = Tiles<D>;
+  static constexpr int kK = 0;
+  static constexpr int kV = T::kTileBytes;
+  static constexpr int kStage0 = 2 * T::kTileBytes;
+  // stage: Q tile, dO tile, nl[128], D[128]
+  static constexpr int kStageBytes = 2 * T::kTileBytes + 2 * T::kRowBytes;
+  static constexpr int kBar = kStage0 + kStages * kStageBytes;
+  // kv_full, stage_full[S], stage_empty[S], sp_full, p_full, o_full, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 4;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kSmem = kMisc + 16 + 1024;
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkv_kernel(const __grid_constant__ BackwardArgs a, const __grid_constant__ CUtensorMap tq,
+               const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+               const __grid_constant__ CUtensorMap tdo) {
+  using L = DkvLayout<D>;
+  using T = Tiles<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bar0 = base + L::kBar;
+  auto kv_full = [&]() { return bar0; };
+  auto st_full = [&](int s) { return bar0 + 8 * (1 + s); };
+  auto st_empty = [&](int s) { return bar0 + 8 * (1 + kStages + s); };
+  const uint32_t sp_full = bar0 + 8 * (1 + 2 * kStages);
+  const uint32_t p_full = sp_full + 8;
+  const uint32_t o_full = sp_full + 16;
+  const uint32_t drain = sp_full + 24;
+  volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + L::kMisc);
+  const Abort ab{tmem_holder + 1, a.status};
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  // unit: (slice, key block j, key tile kt); walk: t = 0..P-1 over the query
+  // blocks i = (j + t) mod P, each with its c/128 query tiles
+  const int64_t c = a.N / a.P;
+  const int tiles = static_cast<int>(c / kBN);
+  int64_t u = blockIdx.x;
+  const int kt = static_cast<int>(u % tiles);
+  u /= tiles;
+  const int j = static_cast<int>(u % a.P);
+  const int64_t slice = u / a.P;
+  const int64_t krow0 = slice * a.N + static_cast<int64_t>(j) * c + static_cast<int64_t>(kt) * kBM;
+  const int n_iter = a.P * tiles;
+  auto qrow = [&](int it) {
+    const int i = (j + it / tiles) % a.P;
+    return slice * a.N + static_cast<int64_t>(i) * c + static_cast<int64_t>(it % tiles) * kBM;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full(), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(st_full(s), 1);
+      mbar_init(st_empty(s), 1);
+    }
+    mbar_init(sp_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(o_full, 1);
+    mbar_init(drain, 1);
+    *ab.flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(base + L::kMisc, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full(), 2 * T::kTileBytes);
+      load_tile2d<D>(base + L::kK, &tk, krow0, kv_full());
+      load_tile2d<D>(base + L::kV, &tv, krow0, kv_full());
+      uint32_t issued = 0, last_parity = 0;
+      bool ok = true;
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
+        if (!wait1(st_empty(s), ph ^ 1u, ab)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sb = base + L::kStage0 + s * L::kStageBytes;
+        const int64_t r = qrow(it);
+        mbar_arrive_expect_tx(st_full(s), 2 * T::kTileBytes + 2 * T::kRowBytes);
+        load_tile2d<D>(sb, &tq, r, st_full(s));
+        load_tile2d<D>(sb + T::kTileBytes, &tdo, r, st_full(s));
+        bulk_load(sb + 2 * T::kTileBytes, a.nl + r, T::kRowBytes, st_full(s));
+        bulk_load(sb + 2 * T::kTileBytes + T::kRowBytes, a.delta + r, T::kRowBytes, st_full(s));
+        issued |= 1u << s;
+        last_parity = (last_parity & ~(1u << s)) | (ph << s);
+      }
+      if (!ok) {
+        wait_drain(kv_full(), 0);
+        for (int s = 0; s < kStages; ++s)
+          if (issued & (1u << s)) wait_drain(st_full(s), (last_parity >> s) & 1u);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      const uint64_t dK = desc_sw128(base + L::kK, 16, 1024);
+      const uint64_t dV = desc_sw128(base + L::kV, 16, 1024);
+      bool ok = wait1(kv_full(), 0, ab);
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const int s = it % kStages;
+        if (!wait1(st_full(s), static_cast<uint32_t>((it / kStages) & 1), ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sb = base + L::kStage0 + s * L::kStageBytes;
+        mma_nt<D>(tS, dK, desc_sw128(sb, 16, 1024));                  // S^T = K Q^T
+        mma_nt<D>(tP, dV, desc_sw128(sb + T::kTileBytes, 16, 1024));  // dP^T = V dO^T
+        mma_commit(sp_full);
+        if (!wait1(p_full, static_cast<uint32_t>(it & 1), ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc = it > 0 ? 1u : 0u;
+        mma_tn<D>(tdV, tS, desc_sw128(sb + T::kTileBytes, T::kBoxBytes, 1024), acc);  // P^T dO
+        mma_tn<D>(tdK, tP, desc_sw128(sb, T::kBoxBytes, 1024), acc);                 // dS^T Q
+        mma_commit(st_empty(s));
+      }
+      if (ok) {
+        mma_commit(o_full);
+      } else {
+        mma_commit(drain);
+        wait_drain(drain, 0);
+      }
+    }
+  } else if (warp < 4) {
+    const int row = warp * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      if (!wait_warp(sp_full, static_cast<uint32_t>(it & 1), ab)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int s = it % kStages;
+      const float* rows = reinterpret_cast<const float*>(gbase + L::kStage0 +
+                                                         s * L::kStageBytes + 2 * T::kTileBytes);
+      elementwise<true, true>(tS + lane_off, tP + lane_off, a.scale_log2, rows,
+                              rows + kBM, 0.f, 0.f);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && wait_warp(o_full, 0, ab)) {
+      tc_fence_after();
+      const int64_t r = krow0 + row;
+      uint16_t* dv = static_cast<uint16_t*>(a.dv) + r * D;
+      uint16_t* dk = static_cast<uint16_t*>(a.dk) + r * D;
+#pragma unroll
+      for (int cc = 0; cc < D; cc += 32) {
+        store_row_bf16(tdV + lane_off + cc, dv + cc, 1.f);
+        store_row_bf16(tdK + lane_off + cc, dk + cc, a.tau);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dQ: one query tile per CTA
+// ---------------------------------------------------------------------------
+template <int D>
+struct DqLayout {
+  using T = Tiles<D>;
+  static constexpr int kQ = 0;
+  static constexpr int kDO = T::kTileBytes;
+  static constexpr int kStage0 = 2 * T::kTileBytes;
+  static constexpr int kStageBytes = 2 * T::kTileBytes;  // K tile, V tile
+  static constexpr int kBar = kStage0 + kStages * kStageBytes;
+  // q_full, stage_full[S], stage_empty[S], sp_full, p_full, o_full, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 4;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kSmem = kMisc + 16 + 1024;
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_kernel(const __grid_constant__ BackwardArgs a, const __grid_constant__ CUtensorMap tq,
+              const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+              const __grid_constant__ CUtensorMap tdo) {
+  using L = DqLayout<D>;
+  using T = Tiles<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bar0 = base + L::kBar;
+  auto q_full = [&]() { return bar0; };
+  auto st_full = [&](int s) { return bar0 + 8 * (1 + s); };
+  auto st_empty = [&](int s) { return bar0 + 8 * (1 + kStages + s); };
+  const uint32_t sp_full = bar0 + 8 * (1 + 2 * kStages);
+  const uint32_t p_full = sp_full + 8;
+  const uint32_t o_full = sp_full + 16;
+  const uint32_t drain = sp_full + 24;
+  volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + L::kMisc);
+  const Abort ab{tmem_holder + 1, a.status};
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  // unit: (slice, query block i, query tile qt); walk: the forward's ring order
+  const int64_t c = a.N / a.P;
+  const int tiles = static_cast<int>(c / kBN);
+  int64_t u = blockIdx.x;
+  const int qt = static_cast<int>(u % tiles);
+  u /= tiles;
+  const int i = static_cast<int>(u % a.P);
+  const int64_t slice = u / a.P;
+  const int64_t qrow0 = slice * a.N + static_cast<int64_t>(i) * c + static_cast<int64_t>(qt) * kBM;
+  const int n_iter = a.P * tiles;
+  auto krow = [&](int it) {
+    int jj = (i - it / tiles) % a.P;
+    if (jj < 0) jj += a.P;
+    return slice * a.N + static_cast<int64_t>(jj) * c + static_cast<int64_t>(it % tiles) * kBM;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full(), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(st_full(s), 1);
+      mbar_init(st_empty(s), 1);
+    }
+    mbar_init(sp_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(o_full, 1);
+    mbar_init(drain, 1);
+    *ab.flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(base + L::kMisc, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tS = tmem, tP = tmem + 128, tdQ = tmem + 256;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full(), 2 * T::kTileBytes);
+      load_tile2d<D>(base + L::kQ, &tq, qrow0, q_full());
+      load_tile2d<D>(base + L::kDO, &tdo, qrow0, q_full());
+      uint32_t issued = 0, last_parity = 0;
+      bool ok = true;
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
+        if (!wait1(st_empty(s), ph ^ 1u, ab)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sb = base + L::kStage0 + s * L::kStageBytes;
+        const int64_t r = krow(it);
+        mbar_arrive_expect_tx(st_full(s), 2 * T::kTileBytes);
+        load_tile2d<D>(sb, &tk, r, st_full(s));
+        load_tile2d<D>(sb + T::kTileBytes, &tv, r, st_full(s));
+        issued |= 1u << s;
+        last_parity = (last_parity & ~(1u << s)) | (ph << s);
+      }
+      if (!ok) {
+        wait_drain(q_full(), 0);
+        for (int s = 0; s < kStages; ++s)
+          if (issued & (1u << s)) wait_drain(st_full(s), (last_parity >> s) & 1u);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      const uint64_t dQ = desc_sw128(base + L::kQ, 16, 1024);
+      const uint64_t dDO = desc_sw128(base + L::kDO, 16, 1024);
+      bool ok = wait1(q_full(), 0, ab);
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const int s = it % kStages;
+        if (!wait1(st_full(s), static_cast<uint32_t>((it / kStages) & 1), ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sb = base + L::kStage0 + s * L::kStageBytes;
+        mma_nt<D>(tS, dQ, desc_sw128(sb, 16, 1024));                    // S = Q K^T
+        mma_nt<D>(tP, dDO, desc_sw128(sb + T::kTileBytes, 16, 1024));   // dP = dO V^T
+        mma_commit(sp_full);
+        if (!wait1(p_full, static_cast<uint32_t>(it & 1), ab)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        mma_tn<D>(tdQ, tP, desc_sw128(sb, T::kBoxBytes, 1024), it > 0 ? 1u : 0u);  // dS K
+        mma_commit(st_empty(s));
+      }
+      if (ok) {
+        mma_commit(o_full);
+      } else {
+        mma_commit(drain);
+        wait_drain(drain, 0);
+      }
+    }
+  } else if (warp < 4) {
+    const int row = warp * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int64_t r = qrow0 + row;
+    const float nl_row = a.nl[r];  // the row terms were precomputed per query
+    const float d_row = a.delta[r];
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      if (!wait_warp(sp_full, static_cast<uint32_t>(it & 1), ab)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      elementwise<false, false>(tS + lane_off, tP + lane_off, a.scale_log2, nullptr, nullptr,
+                                nl_row, d_row);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && wait_warp(o_full, 0, ab)) {
+      tc_fence_after();
+      uint16_t* dq = static_cast<uint16_t*>(a.dq) + r * D;
+#pragma unroll
+      for (int cc = 0; cc < D; cc += 32) store_row_bf16(tdQ + lane_off + cc, dq + cc, a.tau);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const BackwardArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                     const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t s) {
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DkvLayout<D>::kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               DqLayout<D>::kSmem);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const unsigned grid = static_cast<unsigned>(a.slices * (a.N / kBM));
+  dkv_kernel<D><<<grid, kThreads, DkvLayout<D>::kSmem, s>>>(a, tq, tk, tv, tdo);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dq_kernel<D><<<grid, kThreads, DqLayout<D>::kSmem, s>>>(a, tq, tk, tv, tdo);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward_sm103(const BackwardArgs& a, const CUtensorMap& tq,
+                                  const CUtensorMap& tk, const CUtensorMap& tv,
+                                  const CUtensorMap& tdo, cudaStream_t s) {
+  if (a.d == 128) return launch_d<128>(a, tq, tk, tv, tdo, s);
+  if (a.d == 64) return launch_d<64>(a, tq, tk, tv, tdo, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ra

@@ -48,15 +48,15 @@
 #include <cmath>
 
 #include "ra_internal.h"
+#include "sm103_pipeline.cuh"
 #include "sm103_ptx.cuh"
 
 namespace ra {
 namespace {
 
 using namespace ptx;
+using namespace sm103;
 
-constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
-constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kThreads = 384;
 constexpr uint32_t kRegsSoftmax = 208;
 constexpr uint32_t kRegsOther = 88;
@@ -66,7 +66,6 @@ constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr long long kWaitLimit = 1ll << 31;  // SM cycles, about one second
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -99,55 +98,6 @@ struct Bars {
   __device__ uint32_t o_full(int t) const { return base + 8 * (5 + 2 * Layout<D>::kStages + t); }
   __device__ uint32_t drain() const { return base + 8 * (7 + 2 * Layout<D>::kStages); }
 };
-
-struct Abort {
-  volatile uint32_t* flag;
-  int* status;
-  __device__ void raise() const {
-    *flag = 1u;
-    atomicCAS(status, 0, kStatusTimeout);
-  }
-};
-
-// Single-thread bounded wait.
-__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const Abort& ab) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long start = clock64();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*ab.flag) return false;
-    if (clock64() - start > kWaitLimit) {
-      ab.raise();
-      return false;
-    }
-  }
-}
-
-// Bounded wait used while aborting (ignores the abort flag).
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
-  const long long start = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - start > kWaitLimit) return;
-  }
-}
-
-// Whole-warp bounded wait: every lane polls and the warp agrees on the
-// outcome, so the warp stays converged for the .sync.aligned TMEM accesses.
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Abort& ab) {
-  bool done = mbar_try_wait(bar, parity);
-  if (__all_sync(0xffffffffu, done)) return true;
-  const long long start = clock64();
-  while (true) {
-    done = done || mbar_try_wait(bar, parity);
-    if (__all_sync(0xffffffffu, done)) return true;
-    const bool timed_out = clock64() - start > kWaitLimit;
-    const bool give_up = (*ab.flag != 0u) || timed_out;
-    if (__any_sync(0xffffffffu, give_up)) {
-      if (__any_sync(0xffffffffu, timed_out) && (threadIdx.x % 32) == 0) ab.raise();
-      return false;
-    }
-  }
-}
 
 // The K/V tiles one work unit visits, in order: ring steps t = t0 .. t1-1
 // visit block j = (i - t) mod P ("Ring Attention: the math", "The ring
@@ -264,10 +214,6 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, 
   }
 }
 
-// The MMA thread builds each operand's shared-memory descriptor once and
-// moves it by adding (byte offset >> 4) to its start-address field; every
-// address here stays below 2^18 bytes, so the 14-bit field never carries.
-__device__ __forceinline__ constexpr uint64_t desc_step(uint32_t bytes) { return bytes >> 4; }
 
 // S[tmem] = Q K^T for one 128x128 tile: D/16 MMAs of K = 16 along d.  Q and K
 // are K-major (d contiguous) in 128-byte-swizzled boxes of 64 columns; the

@@ -64,6 +64,28 @@ struct FoldArgs {
   PartialPtrs part;  // partial mode
 };
 
+// Everything a backward launch needs besides the TMA descriptors.  Tensors
+// are [slices, N, d] in token order; lse and delta are [slices * N].
+struct BackwardArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dout;
+  const float* lse;    // the forward's log-sum-exp (natural log, scaled scores)
+  const float* nl;     // -lse * log2(e) (tensor path)
+  const float* delta;  // D = rowsum(dout * out)
+  void* dq;
+  void* dk;
+  void* dv;
+  int64_t slices;
+  int64_t N;
+  int32_t d;
+  int32_t P;
+  float tau;         // 1 / sqrt(d)
+  float scale_log2;  // tau * log2(e)
+  int* status;       // device watchdog word
+};
+
 struct MergeArgs {
   PartialPtrs part;
   int32_t G;
@@ -80,6 +102,13 @@ cudaError_t launch_fold_sm103(const FoldArgs& a, const CUtensorMap& tq, const CU
                               const CUtensorMap& tv, cudaStream_t s);
 cudaError_t launch_fold_f32(const FoldArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
+// delta[r] = rowsum(dout * out)[r] and nl[r] = -lse[r] * log2(e).
+cudaError_t launch_delta(const void* out, const void* dout, const float* lse, float* delta,
+                         float* nl, int64_t rows, int32_t d, bool bf16, cudaStream_t s);
+cudaError_t launch_backward_f32(const BackwardArgs& a, cudaStream_t s);
+cudaError_t launch_backward_sm103(const BackwardArgs& a, const CUtensorMap& tq,
+                                  const CUtensorMap& tk, const CUtensorMap& tv,
+                                  const CUtensorMap& tdo, cudaStream_t s);
 cudaError_t launch_state_init(float* m, float* l, float* o, int64_t rows, int32_t d,
                               cudaStream_t s);
 

@@ -527,6 +527,73 @@ int ora_backward(const void* q, const void* k, const void* v, int dtype, const d
   return 0;
 }
 
+// Gradient rows of the (non-causal) backward, for sampled rows of large
+// problems: the same formulas as ora_backward, organised per output row.
+//   qrows[Rq]: flat rows whose dQ is wanted (dq [Rq, d]);
+//   krows[Rk]: flat rows whose dK and dV are wanted (dk, dv [Rk, d]).
+//   out, dout: [BH, N, d] of `dtype` (the forward's output and the incoming
+//   gradient); lse: [BH*N] doubles.
+int ora_backward_rows(const void* q, const void* k, const void* v, int dtype, const void* out,
+                      const void* dout, const double* lse, int64_t BH, int64_t N, int d,
+                      const int64_t* qrows, int64_t Rq, double* dq, const int64_t* krows,
+                      int64_t Rk, double* dk, double* dv, int threads) {
+  if (!q || !k || !v || !out || !dout || !lse || BH < 0 || N < 1 || d < 1 || bad_dtype(dtype))
+    return 1;
+  if ((Rq > 0 && (!qrows || !dq)) || (Rk > 0 && (!krows || !dk || !dv))) return 1;
+  const double tau = 1.0 / std::sqrt(static_cast<double>(d));
+  auto row_D = [&](int64_t r, std::vector<double>& a, std::vector<double>& b) {
+    load_row(out, dtype, r, d, a.data());
+    load_row(dout, dtype, r, d, b.data());
+    double acc = 0.0;
+    for (int e = 0; e < d; ++e) acc += a[e] * b[e];
+    return acc;
+  };
+  parallel_for(Rq + Rk, threads, [&](int64_t x) {
+    std::vector<double> qa(d), ga(d), ka(d), va(d), oa(d), acc1(d, 0.0), acc2(d, 0.0);
+    if (x < Rq) {
+      const int64_t r = qrows[x], bh = r / N;
+      const double D = row_D(r, oa, ga);  // ga = dout_r
+      load_row(q, dtype, r, d, qa.data());
+      for (int64_t j = 0; j < N; ++j) {
+        load_row(k, dtype, bh * N + j, d, ka.data());
+        load_row(v, dtype, bh * N + j, d, va.data());
+        double s = 0.0, dp = 0.0;
+        for (int e = 0; e < d; ++e) {
+          s += qa[e] * ka[e];
+          dp += ga[e] * va[e];
+        }
+        const double ds = std::exp(s * tau - lse[r]) * (dp - D);
+        for (int e = 0; e < d; ++e) acc1[e] += tau * ds * ka[e];
+      }
+      for (int e = 0; e < d; ++e) dq[x * d + e] = acc1[e];
+    } else {
+      const int64_t xi = x - Rq, n = krows[xi], bh = n / N;
+      load_row(k, dtype, n, d, ka.data());
+      load_row(v, dtype, n, d, va.data());
+      for (int64_t r = bh * N; r < (bh + 1) * N; ++r) {
+        const double D = row_D(r, oa, ga);  // ga = dout_r
+        load_row(q, dtype, r, d, qa.data());
+        double s = 0.0, dp = 0.0;
+        for (int e = 0; e < d; ++e) {
+          s += qa[e] * ka[e];
+          dp += ga[e] * va[e];
+        }
+        const double p = std::exp(s * tau - lse[r]);
+        const double ds = p * (dp - D);
+        for (int e = 0; e < d; ++e) {
+          acc1[e] += tau * ds * qa[e];
+          acc2[e] += p * ga[e];
+        }
+      }
+      for (int e = 0; e < d; ++e) {
+        dk[xi * d + e] = acc1[e];
+        dv[xi * d + e] = acc2[e];
+      }
+    }
+  });
+  return 0;
+}
+
 // Build marker: lets a test confirm which variant it loaded.
 int ora_mutant(void) { return ORA_MUTANT; }
 

@@ -65,12 +65,14 @@ class Oracle:
         L.ora_ring.argtypes = [_P, _P, _P, _I32, _I64, _I64, _I32, _I64, _P, _I64, _I64,
                                _I64, _I32, _I32, _P, _I64, _P, _P, _P, _P, _P, _I32]
         L.ora_layout_positions.argtypes = [_I32, _I64, _I64, _P]
+        L.ora_backward_rows.argtypes = [_P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I32, _P,
+                                        _I64, _P, _P, _I64, _P, _P, _I32]
         L.ora_backward.argtypes = [_P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I32, _I64, _I32,
                                    _I32, _P, _P, _P, _I32]
         L.ora_fold.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I32, _I32]
         L.ora_merge.argtypes = [_P, _P, _P, _I64, _I64, _I32, _P, _P, _P, _P, _P]
         for f in (L.ora_ring_order, L.ora_dense, L.ora_ring, L.ora_fold, L.ora_merge,
-                  L.ora_layout_positions, L.ora_backward):
+                  L.ora_layout_positions, L.ora_backward, L.ora_backward_rows):
             f.restype = _I32
         L.ora_mutant.restype = _I32
         self.mutant = L.ora_mutant()
@@ -184,6 +186,28 @@ class Oracle:
                                    la.ctypes.data, BH, N, d, P, int(causal), LAYOUTS[layout],
                                    dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, self.threads)
         self._check(rc, "backward")
+        return dq, dk, dv
+
+    def backward_rows(self, q, k, v, out, dout, lse, qrows, krows, dtype="f64"):
+        """dq for flat rows `qrows`, (dk, dv) for flat rows `krows` (non-causal).
+        out and dout have q's dtype; lse is [BH*N]."""
+        BH, N, d = q.shape
+        qa, qp = self._arr(q, dtype)
+        ka, kp = self._arr(k, dtype)
+        va, vp = self._arr(v, dtype)
+        oa, op = self._arr(out, dtype)
+        ga, gp = self._arr(dout, dtype)
+        la = np.ascontiguousarray(lse, dtype=np.float64).reshape(-1)
+        qr = np.ascontiguousarray(qrows, dtype=np.int64)
+        kr = np.ascontiguousarray(krows, dtype=np.int64)
+        dq = np.empty((qr.size, d), np.float64)
+        dk = np.empty((kr.size, d), np.float64)
+        dv = np.empty((kr.size, d), np.float64)
+        rc = self.lib.ora_backward_rows(qp, kp, vp, _DTYPES[dtype], op, gp, la.ctypes.data, BH,
+                                        N, d, qr.ctypes.data, qr.size, dq.ctypes.data,
+                                        kr.ctypes.data, kr.size, dk.ctypes.data, dv.ctypes.data,
+                                        self.threads)
+        self._check(rc, "backward_rows")
         return dq, dk, dv
 
     def merge(self, m, l, o, state=False):

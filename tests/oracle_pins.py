@@ -523,4 +523,20 @@ def pin_backward_identical_keys_dv(O):
     assert np.abs(dv - dout.mean(axis=1, keepdims=True)).max() <= 1e-12
 
 
+def pin_backward_rows_match_full(O):
+    """The per-row backward used on sampled rows equals the full backward."""
+    rng = np.random.default_rng(33)
+    BH, N, d = 2, 10, 3
+    q, k, v = _rand(rng, BH, N, d, 1.5)
+    dout = rng.standard_normal((BH, N, d))
+    out, lse = O.dense(q, k, v)
+    out = out.reshape(BH, N, d)
+    dq, dk, dv = O.backward(q, k, v, out, dout, lse.reshape(BH, N), P=2)
+    rows = np.array([0, 7, 13, 19])
+    rq, rk, rv = O.backward_rows(q, k, v, out, dout, lse, rows, rows[::-1])
+    assert np.abs(rq - dq.reshape(-1, d)[rows]).max() <= 1e-12
+    assert np.abs(rk - dk.reshape(-1, d)[rows[::-1]]).max() <= 1e-12
+    assert np.abs(rv - dv.reshape(-1, d)[rows[::-1]]).max() <= 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,95 @@
+"""Backward pass (dQ, dK, dV) through the C ABI against the fp64 oracle.
+
+Tolerance: max-abs error <= tol * max(1, max|reference|) per gradient, with
+tol = 1e-5 on the fp32 path and 2e-2 on the bf16 path (the bf16 path rounds
+P and dS to bf16 before the tensor-core products and the gradients to bf16
+at the end; 2e-2 is the forward's bf16 bar)."""
+import numpy as np
+import pytest
+import torch
+
+import long_context_ra_gb300 as ra
+from gpu_util import to_oracle
+from long_context_ra_gb300 import synth
+from oracle import ra_oracle
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-2}
+
+
+@pytest.fixture(scope="module")
+def O():
+    return ra_oracle.get()
+
+
+def rnd(shape, seed, dtype, scale=1.0):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    return (torch.randn(shape, device=DEV, generator=g) * scale).to(dtype)
+
+
+def close(got, want, tol, what):
+    g = got.detach().double().cpu().numpy().reshape(want.shape)
+    err = np.abs(g - want).max()
+    bound = tol * max(1.0, np.abs(want).max())
+    assert err <= bound, f"{what}: max-abs error {err:.3e} > {bound:.3e}"
+    return err
+
+
+def full_check(O, q, k, v, P, dtype):
+    B, H, N, d = q.shape
+    out, lse = ra.ra_forward(q, k, v, P)
+    dout = rnd(q.shape, 999, dtype)
+    dq, dk, dv = ra.ra_backward(q, k, v, out, dout, lse, P)
+    torch.cuda.synchronize()
+    qa, tag = to_oracle(q)
+    ka, _ = to_oracle(k)
+    va, _ = to_oracle(v)
+    oa = out.double().reshape(B * H, N, d).cpu().numpy()
+    ga = dout.double().reshape(B * H, N, d).cpu().numpy()
+    la = lse.double().reshape(B * H, N).cpu().numpy()
+    wq, wk, wv = O.backward(qa, ka, va, oa, ga, la, P, dtype=tag)
+    for name, got, want in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv)):
+        close(got, want, TOL[dtype], name)
+    assert ra.ra_last_device_status() == 0
+
+
+@pytest.mark.parametrize("shape,P", [((1, 2, 40, 8), 4), ((2, 1, 33, 5), 3), ((1, 1, 64, 128), 1),
+                                     ((1, 2, 96, 64), 6)])
+def test_f32_backward(O, shape, P):
+    q, k, v = (rnd(shape, 10 + s, torch.float32, 1.3) for s in range(3))
+    full_check(O, q, k, v, P, torch.float32)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("B,H,N,P", [(1, 1, 256, 1), (1, 2, 512, 2), (2, 1, 768, 3),
+                                     (1, 2, 1024, 8)])
+def test_bf16_backward(O, d, B, H, N, P):
+    q, k, v = (rnd((B, H, N, d), 20 + N + d + s, torch.bfloat16) for s in range(3))
+    full_check(O, q, k, v, P, torch.bfloat16)
+
+
+def test_bf16_backward_workload2(O):
+    w = synth.WORKLOADS[2]
+    q, k, v = synth.make_inputs(w, DEV)
+    full_check(O, q, k, v, w.P, torch.bfloat16)
+
+
+def test_bf16_backward_workload4_sampled(O):
+    """The N = 131072, d = 128, P = 32 workload: gradients of sampled rows."""
+    w = synth.WORKLOADS[4]
+    q, k, v = synth.make_inputs(w, DEV)
+    out, lse = ra.ra_forward(q, k, v, w.P)
+    dout = rnd(q.shape, 4242, torch.bfloat16)
+    dq, dk, dv = ra.ra_backward(q, k, v, out, dout, lse, w.P)
+    torch.cuda.synchronize()
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+    rows = synth.sample_rows(w, 256, seed=5).numpy()
+    bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).cpu().view(torch.int16).numpy().view(np.uint16)
+    wq, wk, wv = O.backward_rows(bits(q), bits(k), bits(v), bits(out), bits(dout),
+                                 lse.double().cpu().numpy(), rows, rows, dtype="bf16")
+    idx = torch.as_tensor(rows, device=DEV)
+    for name, got, want in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv)):
+        close(got.reshape(-1, w.d).index_select(0, idx), want, TOL[torch.bfloat16], name)
+    assert ra.ra_last_device_status() == 0
