@@ -237,20 +237,30 @@ def run_ours(args, w) -> None:
     lse = torch.empty(w.B, w.H, w.N, device=dev, dtype=torch.float32)
     stream = torch.cuda.current_stream()
 
-    if args.split is not None:
+    if args.backward:
+        out0, lse0 = ra.ra_forward(q, k, v, w.P)
+        g = torch.Generator(device=dev).manual_seed(4242)
+        dout = torch.randn(q.shape, device=dev, generator=g).to(q.dtype)
+        ws = torch.empty(2 * w.rows, device=dev, dtype=torch.float32)
+
+        def step():
+            return ra.ra_backward(q, k, v, out0, dout, lse0, w.P, workspace=ws)
+    elif args.split is not None:
         G = args.split or ra.ra_forward_split_segments(w.B, w.H, w.N, w.d, w.P, w.dtype)
         ws = torch.empty(ra.ra_forward_split_workspace_bytes(w.B, w.H, w.N, w.d, G), device=dev,
                          dtype=torch.uint8)
 
         def step():
-            ra.ra_forward_split(q, k, v, w.P, G=G, workspace=ws, out=out, lse=lse)
+            return ra.ra_forward_split(q, k, v, w.P, G=G, workspace=ws, out=out, lse=lse)
     elif args.causal:
         def step():
-            ra.ra_forward_causal(q, k, v, w.P, layout=args.causal, out=out, lse=lse)
+            return ra.ra_forward_causal(q, k, v, w.P, layout=args.causal, out=out, lse=lse)
     else:
         def step():
-            ra.ra_forward(q, k, v, w.P, out=out, lse=lse)
+            return ra.ra_forward(q, k, v, w.P, out=out, lse=lse)
     flops = causal_flops(w) if args.causal else w.flops
+    if args.backward:
+        flops = 2.5 * w.flops  # five products of 2 N^2 d per head (dV, dP, dQ, dK, S)
 
     for _ in range(args.warmup):
         step()
@@ -281,19 +291,19 @@ def run_ours(args, w) -> None:
     ms_max = max_over_ranks(ms, dev, world)
     value = job_throughput(flops, world, ms_max)
 
-    # end to end through the C ABI: pinned host inputs -> device, forward,
-    # out and lse back to pinned host memory, every step
-    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
-    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    # end to end through the C ABI: the step's inputs from pinned host memory
+    # to the device, the call, its results back to pinned host memory, every
+    # step
+    dev_in = [q, k, v] + ([out0, dout, lse0] if args.backward else [])
+    host_in = [x.cpu().pin_memory() for x in dev_in]
+    results = step()
+    host_out = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results]
 
     def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        step()
-        hout.copy_(out, non_blocking=True)
-        hlse.copy_(lse, non_blocking=True)
+        for dst, src in zip(dev_in, host_in):
+            dst.copy_(src, non_blocking=True)
+        for dst, src in zip(host_out, step()):
+            dst.copy_(src, non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -309,12 +319,12 @@ def run_ours(args, w) -> None:
     ms_e2e = max(e0.elapsed_time(e1) / n_e2e, wall * 1e3)
     ms_e2e_max = max_over_ranks(ms_e2e, dev, world)
     e2e_value = job_throughput(flops, world, ms_e2e_max)
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
-    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
 
     peaks = load_peaks()
     achieved = flops / (ms * 1e-3) / 1e12  # one fold launch per step
-    traffic = None if args.causal else profiled_traffic(w.name)
+    traffic = None if (args.causal or args.backward) else profiled_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": UNIT,
                 "frac": achieved / peaks["bf16"], "traffic": traffic,
                 "kernel": "fold_sm103_kernel<128>",
@@ -324,7 +334,8 @@ def run_ours(args, w) -> None:
                 if peaks.get("bf16_sustained") else None}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.causal:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.causal \
+            and not args.backward:
         cpu, _, _ = cpu_oracle_baseline(w, q, k, v, args.cpu_seconds)
 
     if rank == 0:
@@ -335,12 +346,14 @@ def run_ours(args, w) -> None:
             "config": {**w.describe(), "parallelism": "replicas",
                        **({"causal": args.causal} if args.causal else {}),
                        **({"split_segments": G} if args.split is not None else {}),
+                       **({"pass": "backward"} if args.backward else {}),
                        "l2": "inputs larger than L2 (q+k+v = "
                              f"{3 * q.numel() * q.element_size() / 2**20:.0f} MiB)"},
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e_max},
-            "gpu_launches": args.steps * (2 if args.split is not None else 1), "clocks": clocks,
+            "gpu_launches": args.steps * (3 if args.backward else 2 if args.split is not None else 1),
+            "clocks": clocks,
             "pct_of_peak": 100.0 * achieved / peaks["bf16"],
             "exps_per_s": (flops / (4.0 * w.d)) / (ms * 1e-3),
         }
@@ -361,6 +374,8 @@ def main() -> None:
                     help="time ra_forward_causal with this layout instead of ra_forward")
     ap.add_argument("--split", type=int, default=None,
                     help="time ra_forward_split with G segments (0 = recommended)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time ra_backward (5 products per head counted: 10 B H N^2 d)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
