@@ -254,13 +254,26 @@ RA_API ra_status ra_forward_split_noalloc(const void* q, const void* k, const vo
  *   workspace   caller-owned fp32 scratch of 2 * B * H * N floats, 16-byte
  *               aligned; receives D and -lse * log2(e).
  * Size and alignment rules as ra_forward (bf16: d in {64, 128}, c % 128 == 0,
- * 16-byte aligned tensors).  Non-causal.
+ * 16-byte aligned tensors).
  * Errors: as ra_forward; RA_ERR_INVALID_ARG for a NULL buffer.
  */
 RA_API ra_status ra_backward(const void* q, const void* k, const void* v, const void* out,
                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
                              float* workspace, int32_t B, int32_t H, int64_t N, int32_t d,
                              int32_t P, ra_dtype dtype, ra_stream_t stream);
+
+/*
+ * ra_backward_causal -- ra_backward for ra_forward_causal: the mask and the
+ * layout as there (a query at position n sees key positions <= n).  Under the
+ * mask the key block j meets only the query tiles at or after its keys, the
+ * query block i only the key tiles at or before its queries.  Size rules as
+ * ra_forward_causal.
+ */
+RA_API ra_status ra_backward_causal(const void* q, const void* k, const void* v, const void* out,
+                                    const void* dout, const float* lse, void* dq, void* dk,
+                                    void* dv, float* workspace, int32_t B, int32_t H, int64_t N,
+                                    int32_t d, int32_t P, ra_layout layout, ra_dtype dtype,
+                                    ra_stream_t stream);
 
 /*
  * ra_state_init -- set a state to empty: m = -inf, l = 0, o = 0 ("Ring

@@ -20,7 +20,8 @@ from ._native import RA_BF16, RA_F32, RA_MAX_PARTIALS, RaStateC
 
 __all__ = ["RaError", "RaState", "ra_forward", "ra_forward_causal", "ra_forward_partial",
            "ra_forward_partial_causal", "ra_forward_split", "ra_forward_split_workspace_bytes",
-           "ra_forward_split_segments", "ra_backward", "ra_state_init", "ra_fold", "ra_merge",
+           "ra_forward_split_segments", "ra_backward", "ra_backward_causal", "ra_state_init",
+           "ra_fold", "ra_merge",
            "ra_last_device_status", "new_state", "library_path"]
 
 
@@ -192,8 +193,9 @@ def ra_forward_split(q, k, v, P: int, G: int | None = None, workspace=None, out=
     return out, lse
 
 
-def ra_backward(q, k, v, out, dout, lse, P: int, workspace=None, stream=None):
-    """Gradients (dq, dk, dv) of L = sum(dout * out) for ra_forward's out/lse."""
+def ra_backward(q, k, v, out, dout, lse, P: int, workspace=None, stream=None, causal=None):
+    """Gradients (dq, dk, dv) of L = sum(dout * out) for ra_forward's out/lse;
+    causal=<layout> for ra_forward_causal's."""
     B, H, N, d = q.shape
     for t in (k, v, out, dout):
         if t.shape != q.shape or t.dtype != q.dtype:
@@ -201,11 +203,22 @@ def ra_backward(q, k, v, out, dout, lse, P: int, workspace=None, stream=None):
     if workspace is None:
         workspace = torch.empty(2 * B * H * N, device=q.device, dtype=torch.float32)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    code = _native.lib().ra_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
-                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), B, H, N, d, P,
-                                     _dtype_code(q), _stream(stream))
+    ptrs = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+            _ptr(dv), _ptr(workspace))
+    if causal is None:
+        code = _native.lib().ra_backward(*ptrs, B, H, N, d, P, _dtype_code(q), _stream(stream))
+    else:
+        code = _native.lib().ra_backward_causal(*ptrs, B, H, N, d, P, _native.RA_LAYOUTS[causal],
+                                                _dtype_code(q), _stream(stream))
     _check(code, "ra_backward")
     return dq, dk, dv
+
+
+def ra_backward_causal(q, k, v, out, dout, lse, P: int, layout: str = "contiguous",
+                       workspace=None, stream=None):
+    """Gradients for ra_forward_causal (same mask and layout)."""
+    return ra_backward(q, k, v, out, dout, lse, P, workspace=workspace, stream=stream,
+                       causal=layout)
 
 
 def ra_state_init(state: RaState, stream=None) -> RaState:

@@ -363,13 +363,19 @@ RA_API ra_status ra_forward_split(const void* q, const void* k, const void* v, v
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
-RA_API ra_status ra_backward(const void* q, const void* k, const void* v, const void* out,
-                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
-                             float* workspace, int32_t B, int32_t H, int64_t N, int32_t d,
-                             int32_t P, ra_dtype dtype, ra_stream_t stream) {
+}  // extern "C"
+
+namespace ra {
+namespace {
+
+ra_status backward_impl(const void* q, const void* k, const void* v, const void* out,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        float* workspace, int32_t B, int32_t H, int64_t N, int32_t d, int32_t P,
+                        bool causal, ra_layout layout, ra_dtype dtype, ra_stream_t stream) {
   FoldArgs f;
   ra_status st = check_attention(q, k, v, B, H, N, d, P, dtype, &f);
   if (st != RA_OK) return st;
+  if (causal && (st = check_causal(N, P, layout, dtype, &f)) != RA_OK) return st;
   const int64_t rows = f.slices * f.nq;
   if (rows == 0) return RA_OK;
   if (!out || !dout || !lse || !dq || !dk || !dv || !workspace) return RA_ERR_INVALID_ARG;
@@ -395,20 +401,47 @@ RA_API ra_status ra_backward(const void* q, const void* k, const void* v, const 
   a.N = N;
   a.d = d;
   a.P = P;
+  a.causal = f.causal;
+  a.layout = f.layout;
   a.tau = f.tau;
   a.scale_log2 = f.scale_log2;
   a.status = di.status;
-  if ((st = launched(launch_delta(out, dout, lse, workspace, workspace + rows, rows, d,
-                                  dtype == RA_BF16, s))) != RA_OK)
+  if ((st = launched(launch_delta(out, dout, lse, workspace, workspace + rows, rows, d, N, P,
+                                  a.layout, dtype == RA_BF16, s))) != RA_OK)
     return st;
   if (dtype == RA_F32) return launched(launch_backward_f32(a, s));
   if ((st = get_encoder()) != RA_OK) return st;
   CUtensorMap tq, tk, tv, tdo;
-  if ((st = make_map(&tq, q, rows, d)) != RA_OK) return st;
-  if ((st = make_map(&tk, k, rows, d)) != RA_OK) return st;
-  if ((st = make_map(&tv, v, rows, d)) != RA_OK) return st;
-  if ((st = make_map(&tdo, dout, rows, d)) != RA_OK) return st;
+  const void* src[4] = {q, k, v, dout};
+  CUtensorMap* maps[4] = {&tq, &tk, &tv, &tdo};
+  for (int x = 0; x < 4; ++x) {
+    st = a.layout == kStriped ? make_map_striped(maps[x], src[x], rows, d, P)
+                              : make_map(maps[x], src[x], rows, d);
+    if (st != RA_OK) return st;
+  }
   return launched(launch_backward_sm103(a, tq, tk, tv, tdo, s));
+}
+
+}  // namespace
+}  // namespace ra
+
+extern "C" {
+
+RA_API ra_status ra_backward(const void* q, const void* k, const void* v, const void* out,
+                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                             float* workspace, int32_t B, int32_t H, int64_t N, int32_t d,
+                             int32_t P, ra_dtype dtype, ra_stream_t stream) {
+  return backward_impl(q, k, v, out, dout, lse, dq, dk, dv, workspace, B, H, N, d, P, false,
+                       RA_LAYOUT_CONTIGUOUS, dtype, stream);
+}
+
+RA_API ra_status ra_backward_causal(const void* q, const void* k, const void* v, const void* out,
+                                    const void* dout, const float* lse, void* dq, void* dk,
+                                    void* dv, float* workspace, int32_t B, int32_t H, int64_t N,
+                                    int32_t d, int32_t P, ra_layout layout, ra_dtype dtype,
+                                    ra_stream_t stream) {
+  return backward_impl(q, k, v, out, dout, lse, dq, dk, dv, workspace, B, H, N, d, P, true,
+                       layout, dtype, stream);
 }
 
 RA_API ra_status ra_state_init(const ra_state* st, ra_stream_t stream) {

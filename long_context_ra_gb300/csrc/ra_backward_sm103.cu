@@ -61,14 +61,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-template <int D>
-__device__ __forceinline__ void load_tile2d(uint32_t dst, const CUtensorMap* map, int64_t row,
-                                            uint32_t bar) {
-#pragma unroll
-  for (int b = 0; b < D / 64; ++b)
-    tma_load_2d(dst + b * Tiles<D>::kBoxBytes, map, b * 64, static_cast<int32_t>(row), bar);
-}
-
 // D[tmem] = A B^T over d: 128 x 128 x D, both operands K-major in SMEM.
 template <int D>
 __device__ __forceinline__ void mma_nt(uint32_t d_tmem, uint64_t da, uint64_t db) {
@@ -96,11 +88,13 @@ __device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // scores s (TMEM columns of tS) and dp (columns of tP) make
 //   p = exp2(s * sl2 + nl),  ds = p * (dp - Dr)
 // where nl and Dr are per column (dkv kernel: per query, from SMEM) or per
-// row (dq kernel: scalars).  p (if kWriteP) and ds are rounded to bf16 pairs
-// and written over the first 64 columns of tS and tP.
-template <bool kPerColumn, bool kWriteP>
+// row (dq kernel: scalars).  With kMask, columns outside [lo, hi) are masked
+// (their score is -inf, so p = ds = 0).  p (if kWriteP) and ds are rounded
+// to bf16 pairs and written over the first 64 columns of tS and tP.
+template <bool kPerColumn, bool kWriteP, bool kMask>
 __device__ __forceinline__ void elementwise(uint32_t tS, uint32_t tP, float sl2, const float* nl,
-                                            const float* dd, float nl_row, float d_row) {
+                                            const float* dd, float nl_row, float d_row, int lo,
+                                            int hi) {
 #pragma unroll
   for (int c = 0; c < kBN; c += 32) {
     uint32_t s[32], g[32];
@@ -109,6 +103,11 @@ __device__ __forceinline__ void elementwise(uint32_t tS, uint32_t tP, float sl2,
     tmem_ld_wait();
     reg_fence(s, 32);
     reg_fence(g, 32);
+    if (kMask) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (c + e < lo || c + e >= hi) s[e] = 0xff800000u;  // -inf
+    }
     float ncol[kPerColumn ? 32 : 1], dcol[kPerColumn ? 32 : 1];
     if (kPerColumn) {
 #pragma unroll
@@ -141,6 +140,67 @@ __device__ __forceinline__ void elementwise(uint32_t tS, uint32_t tP, float sl2,
     tmem_st16(tP + c / 2, dk);
   }
 }
+
+// The query tiles a key tile visits in the dK/dV kernel: ring steps t = 0 ..
+// P-1 bring query block i = (j + t) mod P (the key block is on device j + t
+// at step t); under the causal mask only query tiles holding a query at or
+// after the tile's first key take part, and in every layout these are a
+// suffix of the block's tiles.
+struct KWalk {
+  int j, P, tiles, layout;
+  int64_t c;
+  bool causal;
+  int64_t kfirst;  // first key position of the tile (striped: first local row)
+  int t, qt, n0;   // iteration state: step, query tile, first visible tile of the block
+
+  __device__ int block(int tt) const { return (j + tt) % P; }
+  __device__ int64_t pos(int i, int64_t r) const {
+    if (layout == kZigzag) {
+      const int64_t h = c / 2;
+      return r < h ? i * h + r : (2 * static_cast<int64_t>(P) - 1 - i) * h + (r - h);
+    }
+    if (layout == kStriped) return i + static_cast<int64_t>(P) * r;
+    return i * c + r;
+  }
+  // Leading tiles (of ntile, the first starting at `first`) whose last query
+  // comes before the tile's first key.
+  __device__ int hidden(int64_t first, int ntile) const {
+    const int64_t n = kfirst - first - (kBM - 1);  // tiles qt with first + qt*128 + 127 < kfirst
+    if (n <= 0) return 0;
+    const int64_t m = (n + kBM - 1) / kBM;
+    return m < ntile ? static_cast<int>(m) : ntile;
+  }
+  __device__ int first_visible(int i) const {
+    if (!causal) return 0;
+    if (layout == kStriped) return hidden(-static_cast<int64_t>(j > i ? 1 : 0), tiles);
+    if (layout == kZigzag) {
+      const int half = tiles / 2;
+      const int a = hidden(i * (c / 2), half);
+      return a < half ? a : half + hidden((2 * static_cast<int64_t>(P) - 1 - i) * (c / 2), half);
+    }
+    return hidden(i * c, tiles);
+  }
+  __device__ int total() const {
+    int n = 0;
+    for (int tt = 0; tt < P; ++tt) n += tiles - first_visible(block(tt));
+    return n;
+  }
+  __device__ void skip() {
+    while (t < P && qt >= tiles) {
+      ++t;
+      if (t < P) qt = n0 = first_visible(block(t));
+    }
+  }
+  __device__ void start() {
+    t = 0;
+    qt = n0 = first_visible(block(0));
+    skip();
+  }
+  __device__ void next() {
+    ++qt;
+    skip();
+  }
+};
 
 // Store one TMEM row segment of 32 fp32 columns, times `scale`, as bf16.
 __device__ __forceinline__ void store_row_bf16(uint32_t taddr, uint16_t* dst, float scale) {
@@ -179,7 +239,7 @@ struct DkvLayout {
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-template <int D>
+template <int D, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     dkv_kernel(const __grid_constant__ BackwardArgs a, const __grid_constant__ CUtensorMap tq,
                const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -202,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Abort ab{tmem_holder + 1, a.status};
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-  // unit: (slice, key block j, key tile kt); walk: t = 0..P-1 over the query
-  // blocks i = (j + t) mod P, each with its c/128 query tiles
+  // unit: (slice, key block j, key tile kt); walk: the query tiles of the
+  // blocks i = (j + t) mod P (see KWalk)
   const int64_t c = a.N / a.P;
   const int tiles = static_cast<int>(c / kBN);
   int64_t u = blockIdx.x;
@@ -211,12 +271,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   u /= tiles;
   const int j = static_cast<int>(u % a.P);
   const int64_t slice = u / a.P;
-  const int64_t krow0 = slice * a.N + static_cast<int64_t>(j) * c + static_cast<int64_t>(kt) * kBM;
-  const int n_iter = a.P * tiles;
-  auto qrow = [&](int it) {
-    const int i = (j + it / tiles) % a.P;
-    return slice * a.N + static_cast<int64_t>(i) * c + static_cast<int64_t>(it % tiles) * kBM;
-  };
+  const bool striped = a.layout == kStriped;
+  KWalk walk;
+  walk.j = j;
+  walk.P = a.P;
+  walk.tiles = tiles;
+  walk.layout = a.layout;
+  walk.c = c;
+  walk.causal = kCausal;
+  walk.kfirst = striped ? static_cast<int64_t>(kt) * kBM : walk.pos(j, static_cast<int64_t>(kt) * kBM);
+  const int n_iter = walk.total();
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full(), 1);
@@ -243,12 +307,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kLoadWarp) {
     if (lane == 0) {
+      const int64_t klr = static_cast<int64_t>(kt) * kBM;  // first local key row
       mbar_arrive_expect_tx(kv_full(), 2 * T::kTileBytes);
-      load_tile2d<D>(base + L::kK, &tk, krow0, kv_full());
-      load_tile2d<D>(base + L::kV, &tv, krow0, kv_full());
+      load_tile<D>(base + L::kK, &tk, striped, slice * a.N + walk.pos(j, klr), j,
+                   slice * c + klr, kv_full());
+      load_tile<D>(base + L::kV, &tv, striped, slice * a.N + walk.pos(j, klr), j,
+                   slice * c + klr, kv_full());
       uint32_t issued = 0, last_parity = 0;
       bool ok = true;
-      for (int it = 0; it < n_iter && ok; ++it) {
+      KWalk w = walk;
+      w.start();
+      for (int it = 0; it < n_iter && ok; ++it, w.next()) {
         const int s = it % kStages;
         const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
         if (!wait1(st_empty(s), ph ^ 1u, ab)) {
@@ -256,12 +325,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint32_t sb = base + L::kStage0 + s * L::kStageBytes;
-        const int64_t r = qrow(it);
+        const int i = w.block(w.t);
+        const int64_t qlr = static_cast<int64_t>(w.qt) * kBM;  // first local query row
+        const int64_t bm = slice * a.N + static_cast<int64_t>(i) * c + qlr;  // block-major
         mbar_arrive_expect_tx(st_full(s), 2 * T::kTileBytes + 2 * T::kRowBytes);
-        load_tile2d<D>(sb, &tq, r, st_full(s));
-        load_tile2d<D>(sb + T::kTileBytes, &tdo, r, st_full(s));
-        bulk_load(sb + 2 * T::kTileBytes, a.nl + r, T::kRowBytes, st_full(s));
-        bulk_load(sb + 2 * T::kTileBytes + T::kRowBytes, a.delta + r, T::kRowBytes, st_full(s));
+        load_tile<D>(sb, &tq, striped, slice * a.N + w.pos(i, qlr), i, slice * c + qlr,
+                     st_full(s));
+        load_tile<D>(sb + T::kTileBytes, &tdo, striped, slice * a.N + w.pos(i, qlr), i,
+                     slice * c + qlr, st_full(s));
+        bulk_load(sb + 2 * T::kTileBytes, a.nl + bm, T::kRowBytes, st_full(s));
+        bulk_load(sb + 2 * T::kTileBytes + T::kRowBytes, a.delta + bm, T::kRowBytes, st_full(s));
         issued |= 1u << s;
         last_parity = (last_parity & ~(1u << s)) | (ph << s);
       }
@@ -307,8 +380,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 4) {
     const int row = warp * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // this thread's key: position (striped: local row) for the mask
+    const int64_t kref = walk.kfirst + row;
+    KWalk w = walk;
+    w.start();
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
+      if (kCausal && it > 0) w.next();
       if (!wait_warp(sp_full, static_cast<uint32_t>(it & 1), ab)) {
         ok = false;
         break;
@@ -317,15 +395,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = it % kStages;
       const float* rows = reinterpret_cast<const float*>(gbase + L::kStage0 +
                                                          s * L::kStageBytes + 2 * T::kTileBytes);
-      elementwise<true, true>(tS + lane_off, tP + lane_off, a.scale_log2, rows,
-                              rows + kBM, 0.f, 0.f);
+      int lo = 0;
+      if (kCausal) {
+        // query columns before this key are masked: positions qfirst + col
+        const int i = w.block(w.t);
+        const int64_t qlr = static_cast<int64_t>(w.qt) * kBM;
+        const int64_t qref = striped ? qlr - (j > i ? 1 : 0) : w.pos(i, qlr);
+        const int64_t m = kref - qref;
+        lo = m < 0 ? 0 : (m > kBN ? kBN : static_cast<int>(m));
+      }
+      elementwise<true, true, kCausal>(tS + lane_off, tP + lane_off, a.scale_log2, rows,
+                                       rows + kBM, 0.f, 0.f, lo, kBN);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full);
     }
     if (ok && wait_warp(o_full, 0, ab)) {
       tc_fence_after();
-      const int64_t r = krow0 + row;
+      const int64_t r = slice * a.N + walk.pos(j, static_cast<int64_t>(kt) * kBM + row);
       uint16_t* dv = static_cast<uint16_t*>(a.dv) + r * D;
       uint16_t* dk = static_cast<uint16_t*>(a.dk) + r * D;
 #pragma unroll
@@ -363,7 +450,7 @@ struct DqLayout {
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-template <int D>
+template <int D, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ BackwardArgs a, const __grid_constant__ CUtensorMap tq,
               const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -386,21 +473,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Abort ab{tmem_holder + 1, a.status};
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-  // unit: (slice, query block i, query tile qt); walk: the forward's ring order
+  // unit: (slice, query block i, query tile qt); walk: the forward's ring
+  // order over key tiles (Walk), the heaviest units first under the mask
   const int64_t c = a.N / a.P;
   const int tiles = static_cast<int>(c / kBN);
   int64_t u = blockIdx.x;
-  const int qt = static_cast<int>(u % tiles);
+  int qt = static_cast<int>(u % tiles);
   u /= tiles;
-  const int i = static_cast<int>(u % a.P);
+  int i = static_cast<int>(u % a.P);
   const int64_t slice = u / a.P;
-  const int64_t qrow0 = slice * a.N + static_cast<int64_t>(i) * c + static_cast<int64_t>(qt) * kBM;
-  const int n_iter = a.P * tiles;
-  auto krow = [&](int it) {
-    int jj = (i - it / tiles) % a.P;
-    if (jj < 0) jj += a.P;
-    return slice * a.N + static_cast<int64_t>(jj) * c + static_cast<int64_t>(it % tiles) * kBM;
-  };
+  if (kCausal) {
+    qt = tiles - 1 - qt;
+    i = a.P - 1 - i;
+  }
+  const bool striped = a.layout == kStriped;
+  const int64_t qlr0 = static_cast<int64_t>(qt) * kBM;  // first local query row
+  Walk walk;
+  walk.slice = slice;
+  walk.N = a.N;
+  walk.c = c;
+  walk.i = i;
+  walk.P = a.P;
+  walk.t0 = 0;
+  walk.t1 = a.P;
+  walk.tiles = tiles;
+  walk.layout = a.layout;
+  walk.causal = kCausal;
+  walk.qlast = striped ? qlr0 + kBM - 1 : walk.pos(i, qlr0 + kBM - 1);
+  const int n_iter = walk.total();
 
   if (threadIdx.x == 0) {
     mbar_init(q_full(), 1);
@@ -428,11 +528,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kLoadWarp) {
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full(), 2 * T::kTileBytes);
-      load_tile2d<D>(base + L::kQ, &tq, qrow0, q_full());
-      load_tile2d<D>(base + L::kDO, &tdo, qrow0, q_full());
+      load_tile<D>(base + L::kQ, &tq, striped, slice * a.N + walk.pos(i, qlr0), i,
+                   slice * c + qlr0, q_full());
+      load_tile<D>(base + L::kDO, &tdo, striped, slice * a.N + walk.pos(i, qlr0), i,
+                   slice * c + qlr0, q_full());
       uint32_t issued = 0, last_parity = 0;
       bool ok = true;
-      for (int it = 0; it < n_iter && ok; ++it) {
+      Walk w = walk;
+      w.start();
+      for (int it = 0; it < n_iter && ok; ++it, w.next()) {
         const int s = it % kStages;
         const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
         if (!wait1(st_empty(s), ph ^ 1u, ab)) {
@@ -440,10 +544,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint32_t sb = base + L::kStage0 + s * L::kStageBytes;
-        const int64_t r = krow(it);
+        const int jb = w.block(w.t);
+        const int64_t row = slice * a.N + w.key_first();
+        const int64_t lrow = slice * c + static_cast<int64_t>(w.kt) * kBN;
         mbar_arrive_expect_tx(st_full(s), 2 * T::kTileBytes);
-        load_tile2d<D>(sb, &tk, r, st_full(s));
-        load_tile2d<D>(sb + T::kTileBytes, &tv, r, st_full(s));
+        load_tile<D>(sb, &tk, striped, row, jb, lrow, st_full(s));
+        load_tile<D>(sb + T::kTileBytes, &tv, striped, row, jb, lrow, st_full(s));
         issued |= 1u << s;
         last_parity = (last_parity & ~(1u << s)) | (ph << s);
       }
@@ -487,18 +593,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 4) {
     const int row = warp * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const int64_t r = qrow0 + row;
-    const float nl_row = a.nl[r];  // the row terms were precomputed per query
-    const float d_row = a.delta[r];
+    const int64_t lrow = qlr0 + row;
+    const int64_t qpos = walk.pos(i, lrow);
+    const int64_t r = slice * a.N + qpos;  // row of dq
+    const int64_t bm = slice * a.N + static_cast<int64_t>(i) * c + lrow;  // block-major
+    const float nl_row = a.nl[bm];  // the row terms were precomputed per query
+    const float d_row = a.delta[bm];
+    const int64_t qref = striped ? lrow : qpos;
+    Walk w = walk;
+    w.start();
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
+      if (kCausal && it > 0) w.next();
       if (!wait_warp(sp_full, static_cast<uint32_t>(it & 1), ab)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      elementwise<false, false>(tS + lane_off, tP + lane_off, a.scale_log2, nullptr, nullptr,
-                                nl_row, d_row);
+      int hi = kBN;
+      if (kCausal) {
+        // keys after this query are masked: first key reference of the tile
+        const int64_t first = w.key_first() + (striped && w.block(w.t) > i ? 1 : 0);
+        const int64_t n = qref - first + 1;
+        hi = n < 0 ? 0 : (n > kBN ? kBN : static_cast<int>(n));
+      }
+      elementwise<false, false, kCausal>(tS + lane_off, tP + lane_off, a.scale_log2, nullptr,
+                                         nullptr, nl_row, d_row, 0, hi);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full);
@@ -520,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kCausal>
 cudaError_t launch_d(const BackwardArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t s) {
   static thread_local int configured_device = -1;
@@ -528,19 +648,19 @@ cudaError_t launch_d(const BackwardArgs& a, const CUtensorMap& tq, const CUtenso
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(dkv_kernel<D, kCausal>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DkvLayout<D>::kSmem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               DqLayout<D>::kSmem);
+      e = cudaFuncSetAttribute(dq_kernel<D, kCausal>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::kSmem);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   const unsigned grid = static_cast<unsigned>(a.slices * (a.N / kBM));
-  dkv_kernel<D><<<grid, kThreads, DkvLayout<D>::kSmem, s>>>(a, tq, tk, tv, tdo);
+  dkv_kernel<D, kCausal><<<grid, kThreads, DkvLayout<D>::kSmem, s>>>(a, tq, tk, tv, tdo);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dq_kernel<D><<<grid, kThreads, DqLayout<D>::kSmem, s>>>(a, tq, tk, tv, tdo);
+  dq_kernel<D, kCausal><<<grid, kThreads, DqLayout<D>::kSmem, s>>>(a, tq, tk, tv, tdo);
   return cudaGetLastError();
 }
 
@@ -549,8 +669,13 @@ cudaError_t launch_d(const BackwardArgs& a, const CUtensorMap& tq, const CUtenso
 cudaError_t launch_backward_sm103(const BackwardArgs& a, const CUtensorMap& tq,
                                   const CUtensorMap& tk, const CUtensorMap& tv,
                                   const CUtensorMap& tdo, cudaStream_t s) {
-  if (a.d == 128) return launch_d<128>(a, tq, tk, tv, tdo, s);
-  if (a.d == 64) return launch_d<64>(a, tq, tk, tv, tdo, s);
+  if (a.causal) {
+    if (a.d == 128) return launch_d<128, true>(a, tq, tk, tv, tdo, s);
+    if (a.d == 64) return launch_d<64, true>(a, tq, tk, tv, tdo, s);
+  } else {
+    if (a.d == 128) return launch_d<128, false>(a, tq, tk, tv, tdo, s);
+    if (a.d == 64) return launch_d<64, false>(a, tq, tk, tv, tdo, s);
+  }
   return cudaErrorInvalidValue;
 }
 

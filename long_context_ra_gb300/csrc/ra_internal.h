@@ -81,6 +81,8 @@ struct BackwardArgs {
   int64_t N;
   int32_t d;
   int32_t P;
+  int32_t causal;    // 1: a query sees key positions <= its own
+  int32_t layout;    // Layout of the tokens over the blocks
   float tau;         // 1 / sqrt(d)
   float scale_log2;  // tau * log2(e)
   int* status;       // device watchdog word
@@ -102,9 +104,11 @@ cudaError_t launch_fold_sm103(const FoldArgs& a, const CUtensorMap& tq, const CU
                               const CUtensorMap& tv, cudaStream_t s);
 cudaError_t launch_fold_f32(const FoldArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
-// delta[r] = rowsum(dout * out)[r] and nl[r] = -lse[r] * log2(e).
+// D = rowsum(dout * out) and nl = -lse * log2(e) per query row, stored
+// block-major: (slice, block, local row) under `layout` (P blocks).
 cudaError_t launch_delta(const void* out, const void* dout, const float* lse, float* delta,
-                         float* nl, int64_t rows, int32_t d, bool bf16, cudaStream_t s);
+                         float* nl, int64_t rows, int32_t d, int64_t N, int32_t P,
+                         int32_t layout, bool bf16, cudaStream_t s);
 cudaError_t launch_backward_f32(const BackwardArgs& a, cudaStream_t s);
 cudaError_t launch_backward_sm103(const BackwardArgs& a, const CUtensorMap& tq,
                                   const CUtensorMap& tk, const CUtensorMap& tv,

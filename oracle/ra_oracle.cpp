@@ -527,16 +527,16 @@ int ora_backward(const void* q, const void* k, const void* v, int dtype, const d
   return 0;
 }
 
-// Gradient rows of the (non-causal) backward, for sampled rows of large
-// problems: the same formulas as ora_backward, organised per output row.
+// Gradient rows of the backward, for sampled rows of large problems: the same
+// formulas as ora_backward, organised per output row (causal: R12 mask).
 //   qrows[Rq]: flat rows whose dQ is wanted (dq [Rq, d]);
 //   krows[Rk]: flat rows whose dK and dV are wanted (dk, dv [Rk, d]).
 //   out, dout: [BH, N, d] of `dtype` (the forward's output and the incoming
 //   gradient); lse: [BH*N] doubles.
 int ora_backward_rows(const void* q, const void* k, const void* v, int dtype, const void* out,
                       const void* dout, const double* lse, int64_t BH, int64_t N, int d,
-                      const int64_t* qrows, int64_t Rq, double* dq, const int64_t* krows,
-                      int64_t Rk, double* dk, double* dv, int threads) {
+                      int causal, const int64_t* qrows, int64_t Rq, double* dq,
+                      const int64_t* krows, int64_t Rk, double* dk, double* dv, int threads) {
   if (!q || !k || !v || !out || !dout || !lse || BH < 0 || N < 1 || d < 1 || bad_dtype(dtype))
     return 1;
   if ((Rq > 0 && (!qrows || !dq)) || (Rk > 0 && (!krows || !dk || !dv))) return 1;
@@ -554,7 +554,8 @@ int ora_backward_rows(const void* q, const void* k, const void* v, int dtype, co
       const int64_t r = qrows[x], bh = r / N;
       const double D = row_D(r, oa, ga);  // ga = dout_r
       load_row(q, dtype, r, d, qa.data());
-      for (int64_t j = 0; j < N; ++j) {
+      const int64_t nk = causal ? r - bh * N + 1 : N;  // keys at or before the query (R12)
+      for (int64_t j = 0; j < nk; ++j) {
         load_row(k, dtype, bh * N + j, d, ka.data());
         load_row(v, dtype, bh * N + j, d, va.data());
         double s = 0.0, dp = 0.0;
@@ -570,7 +571,7 @@ int ora_backward_rows(const void* q, const void* k, const void* v, int dtype, co
       const int64_t xi = x - Rq, n = krows[xi], bh = n / N;
       load_row(k, dtype, n, d, ka.data());
       load_row(v, dtype, n, d, va.data());
-      for (int64_t r = bh * N; r < (bh + 1) * N; ++r) {
+      for (int64_t r = causal ? n : bh * N; r < (bh + 1) * N; ++r) {  // queries that see n
         const double D = row_D(r, oa, ga);  // ga = dout_r
         load_row(q, dtype, r, d, qa.data());
         double s = 0.0, dp = 0.0;

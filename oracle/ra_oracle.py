@@ -65,8 +65,8 @@ class Oracle:
         L.ora_ring.argtypes = [_P, _P, _P, _I32, _I64, _I64, _I32, _I64, _P, _I64, _I64,
                                _I64, _I32, _I32, _P, _I64, _P, _P, _P, _P, _P, _I32]
         L.ora_layout_positions.argtypes = [_I32, _I64, _I64, _P]
-        L.ora_backward_rows.argtypes = [_P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I32, _P,
-                                        _I64, _P, _P, _I64, _P, _P, _I32]
+        L.ora_backward_rows.argtypes = [_P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I32, _I32,
+                                        _P, _I64, _P, _P, _I64, _P, _P, _I32]
         L.ora_backward.argtypes = [_P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I32, _I64, _I32,
                                    _I32, _P, _P, _P, _I32]
         L.ora_fold.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I32, _I32]
@@ -188,8 +188,8 @@ class Oracle:
         self._check(rc, "backward")
         return dq, dk, dv
 
-    def backward_rows(self, q, k, v, out, dout, lse, qrows, krows, dtype="f64"):
-        """dq for flat rows `qrows`, (dk, dv) for flat rows `krows` (non-causal).
+    def backward_rows(self, q, k, v, out, dout, lse, qrows, krows, dtype="f64", causal=False):
+        """dq for flat rows `qrows`, (dk, dv) for flat rows `krows`.
         out and dout have q's dtype; lse is [BH*N]."""
         BH, N, d = q.shape
         qa, qp = self._arr(q, dtype)
@@ -204,7 +204,7 @@ class Oracle:
         dk = np.empty((kr.size, d), np.float64)
         dv = np.empty((kr.size, d), np.float64)
         rc = self.lib.ora_backward_rows(qp, kp, vp, _DTYPES[dtype], op, gp, la.ctypes.data, BH,
-                                        N, d, qr.ctypes.data, qr.size, dq.ctypes.data,
+                                        N, d, int(causal), qr.ctypes.data, qr.size, dq.ctypes.data,
                                         kr.ctypes.data, kr.size, dk.ctypes.data, dv.ctypes.data,
                                         self.threads)
         self._check(rc, "backward_rows")

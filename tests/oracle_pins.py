@@ -537,6 +537,14 @@ def pin_backward_rows_match_full(O):
     assert np.abs(rq - dq.reshape(-1, d)[rows]).max() <= 1e-12
     assert np.abs(rk - dk.reshape(-1, d)[rows[::-1]]).max() <= 1e-12
     assert np.abs(rv - dv.reshape(-1, d)[rows[::-1]]).max() <= 1e-12
+    # causal
+    out, lse = O.dense(q, k, v, causal=True)
+    out = out.reshape(BH, N, d)
+    dq, dk, dv = O.backward(q, k, v, out, dout, lse.reshape(BH, N), P=2, causal=True)
+    rq, rk, rv = O.backward_rows(q, k, v, out, dout, lse, rows, rows, causal=True)
+    assert np.abs(rq - dq.reshape(-1, d)[rows]).max() <= 1e-12
+    assert np.abs(rk - dk.reshape(-1, d)[rows]).max() <= 1e-12
+    assert np.abs(rv - dv.reshape(-1, d)[rows]).max() <= 1e-12
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

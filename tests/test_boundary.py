@@ -137,3 +137,14 @@ def test_noalloc_split_rejects_oversize_without_device(L):
         _native.RA_ERR_INVALID_ARG
     assert L.ra_forward_split_noalloc(A, A, A, A, A, 1, 2, 4096, 128, 8, 2, BF16, None) == \
         _native.RA_ERR_ARCH
+
+
+def test_backward_validation(L):
+    def fb(ws=A, N=1024, P=4, d=64, dt=BF16):
+        return L.ra_backward(A, A, A, A, A, A, A, A, A, ws, 1, 1, N, d, P, dt, None)
+    assert fb(ws=None) == _native.RA_ERR_INVALID_ARG
+    assert fb(ws=A + 4) == _native.RA_ERR_MISALIGNED
+    assert fb(N=1000) == _native.RA_ERR_UNSUPPORTED
+    assert fb() == _native.RA_ERR_ARCH
+    assert L.ra_backward_causal(A, A, A, A, A, A, A, A, A, A, 1, 1, 1024, 64, 4, 7, BF16,
+                                None) == _native.RA_ERR_INVALID_ARG

@@ -36,11 +36,14 @@ def close(got, want, tol, what):
     return err
 
 
-def full_check(O, q, k, v, P, dtype):
+def full_check(O, q, k, v, P, dtype, causal=None):
     B, H, N, d = q.shape
-    out, lse = ra.ra_forward(q, k, v, P)
+    if causal is None:
+        out, lse = ra.ra_forward(q, k, v, P)
+    else:
+        out, lse = ra.ra_forward_causal(q, k, v, P, layout=causal)
     dout = rnd(q.shape, 999, dtype)
-    dq, dk, dv = ra.ra_backward(q, k, v, out, dout, lse, P)
+    dq, dk, dv = ra.ra_backward(q, k, v, out, dout, lse, P, causal=causal)
     torch.cuda.synchronize()
     qa, tag = to_oracle(q)
     ka, _ = to_oracle(k)
@@ -48,7 +51,8 @@ def full_check(O, q, k, v, P, dtype):
     oa = out.double().reshape(B * H, N, d).cpu().numpy()
     ga = dout.double().reshape(B * H, N, d).cpu().numpy()
     la = lse.double().reshape(B * H, N).cpu().numpy()
-    wq, wk, wv = O.backward(qa, ka, va, oa, ga, la, P, dtype=tag)
+    wq, wk, wv = O.backward(qa, ka, va, oa, ga, la, P, dtype=tag, causal=causal is not None,
+                            layout=causal or "contiguous")
     for name, got, want in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv)):
         close(got, want, TOL[dtype], name)
     assert ra.ra_last_device_status() == 0
@@ -89,6 +93,45 @@ def test_bf16_backward_workload4_sampled(O):
     bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).cpu().view(torch.int16).numpy().view(np.uint16)
     wq, wk, wv = O.backward_rows(bits(q), bits(k), bits(v), bits(out), bits(dout),
                                  lse.double().cpu().numpy(), rows, rows, dtype="bf16")
+    idx = torch.as_tensor(rows, device=DEV)
+    for name, got, want in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv)):
+        close(got.reshape(-1, w.d).index_select(0, idx), want, TOL[torch.bfloat16], name)
+    assert ra.ra_last_device_status() == 0
+
+
+LAYOUTS = ["contiguous", "zigzag", "striped"]
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("shape,P", [((1, 2, 48, 8), 4), ((2, 1, 36, 33), 6), ((1, 1, 64, 64), 2)])
+def test_f32_backward_causal(O, layout, shape, P):
+    q, k, v = (rnd(shape, 40 + s, torch.float32, 1.3) for s in range(3))
+    full_check(O, q, k, v, P, torch.float32, causal=layout)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("B,H,N,P", [(1, 2, 1024, 4), (2, 1, 512, 2), (1, 1, 1536, 3),
+                                     (1, 1, 2048, 8)])
+def test_bf16_backward_causal(O, layout, d, B, H, N, P):
+    if layout == "zigzag" and (N // P) % 256:
+        pytest.skip("zigzag on the tensor path needs c % 256 == 0")
+    q, k, v = (rnd((B, H, N, d), 50 + N + d + s, torch.bfloat16) for s in range(3))
+    full_check(O, q, k, v, P, torch.bfloat16, causal=layout)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_bf16_backward_causal_workload4_sampled(O, layout):
+    w = synth.WORKLOADS[4]
+    q, k, v = synth.make_inputs(w, DEV)
+    out, lse = ra.ra_forward_causal(q, k, v, w.P, layout=layout)
+    dout = rnd(q.shape, 4343, torch.bfloat16)
+    dq, dk, dv = ra.ra_backward_causal(q, k, v, out, dout, lse, w.P, layout=layout)
+    torch.cuda.synchronize()
+    rows = synth.sample_rows(w, 128, seed=6).numpy()
+    bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).cpu().view(torch.int16).numpy().view(np.uint16)
+    wq, wk, wv = O.backward_rows(bits(q), bits(k), bits(v), bits(out), bits(dout),
+                                 lse.double().cpu().numpy(), rows, rows, dtype="bf16", causal=True)
     idx = torch.as_tensor(rows, device=DEV)
     for name, got, want in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv)):
         close(got.reshape(-1, w.d).index_select(0, idx), want, TOL[torch.bfloat16], name)
