@@ -238,13 +238,17 @@ def run_ours(args, w) -> None:
     stream = torch.cuda.current_stream()
 
     if args.backward:
-        out0, lse0 = ra.ra_forward(q, k, v, w.P)
+        if args.causal:
+            out0, lse0 = ra.ra_forward_causal(q, k, v, w.P, layout=args.causal)
+        else:
+            out0, lse0 = ra.ra_forward(q, k, v, w.P)
         g = torch.Generator(device=dev).manual_seed(4242)
         dout = torch.randn(q.shape, device=dev, generator=g).to(q.dtype)
         ws = torch.empty(2 * w.rows, device=dev, dtype=torch.float32)
 
         def step():
-            return ra.ra_backward(q, k, v, out0, dout, lse0, w.P, workspace=ws)
+            return ra.ra_backward(q, k, v, out0, dout, lse0, w.P, workspace=ws,
+                                  causal=args.causal)
     elif args.split is not None:
         G = args.split or ra.ra_forward_split_segments(w.B, w.H, w.N, w.d, w.P, w.dtype)
         ws = torch.empty(ra.ra_forward_split_workspace_bytes(w.B, w.H, w.N, w.d, G), device=dev,
@@ -260,7 +264,8 @@ def run_ours(args, w) -> None:
             return ra.ra_forward(q, k, v, w.P, out=out, lse=lse)
     flops = causal_flops(w) if args.causal else w.flops
     if args.backward:
-        flops = 2.5 * w.flops  # five products of 2 N^2 d per head (dV, dP, dQ, dK, S)
+        # five products of 2 N^2 d per head (S, dP, dV, dQ, dK)
+        flops = 2.5 * (causal_flops(w) if args.causal else w.flops)
 
     for _ in range(args.warmup):
         step()
