@@ -43,6 +43,10 @@ constexpr int kLoadWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStages = 2;
+// The elementwise pass over a tile's 128 columns is done in kParts parts; the
+// tensor-core products that read part h start as soon as part h is done.
+constexpr int kParts = 4;
+constexpr int kPartCols = kBN / kParts;
 
 template <int D>
 struct Tiles {
@@ -72,16 +76,17 @@ __device__ __forceinline__ void mma_nt(uint32_t d_tmem, uint64_t da, uint64_t db
   }
 }
 
-// D[tmem] (+)= A[tmem] B over 128 rows of B: A is 128 x 128 bf16 packed in
-// TMEM (8 columns per 16 values), B an MN-major 128 x D tile in SMEM.
-template <int D>
+// D[tmem] (+)= A[tmem] B over rows [16 k0, 16 k1) of B: A is 128 x 128 bf16
+// packed in TMEM (8 columns per 16 values), B an MN-major 128 x D tile in
+// SMEM.  `accumulate` applies to the first product only.
+template <int D, int k0, int k1>
 __device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint64_t db,
                                        uint32_t accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, true);
-  mma_bf16_ts(d_tmem, a_tmem, db, idesc, accumulate);
 #pragma unroll
-  for (int kk = 1; kk < kBN / 16; ++kk)
-    mma_bf16_ts(d_tmem, a_tmem + kk * 8, db + desc_step(kk * 16 * 128), idesc, 1u);
+  for (int kk = k0; kk < k1; ++kk)
+    mma_bf16_ts(d_tmem, a_tmem + kk * 8, db + desc_step(kk * 16 * 128), idesc,
+                kk == k0 ? accumulate : 1u);
 }
 
 // Elementwise step on one tile row (this thread's TMEM lane): from the 128
@@ -90,13 +95,15 @@ __device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // where nl and Dr are per column (dkv kernel: per query, from SMEM) or per
 // row (dq kernel: scalars).  With kMask, columns outside [lo, hi) are masked
 // (their score is -inf, so p = ds = 0).  p (if kWriteP) and ds are rounded
-// to bf16 pairs and written over the first 64 columns of tS and tP.
-template <bool kPerColumn, bool kWriteP, bool kMask>
+// to bf16 pairs and written over the first 64 columns of tS and tP.  One call
+// covers the columns [c0, c1): the tile is done in two halves, so that the
+// products over the first half can run while the second half is computed.
+template <bool kPerColumn, bool kWriteP, bool kMask, int c0, int c1>
 __device__ __forceinline__ void elementwise(uint32_t tS, uint32_t tP, float sl2, const float* nl,
                                             const float* dd, float nl_row, float d_row, int lo,
                                             int hi) {
 #pragma unroll
-  for (int c = 0; c < kBN; c += 32) {
+  for (int c = c0; c < c1; c += 32) {
     uint32_t s[32], g[32];
     tmem_ld32(tS + c, s);
     tmem_ld32(tP + c, g);
@@ -202,6 +209,32 @@ struct KWalk {
   }
 };
 
+// Part h of the elementwise pass: columns [h * kPartCols, (h + 1) * kPartCols).
+template <bool kPerColumn, bool kWriteP, bool kMask>
+__device__ __forceinline__ void elementwise_part(int h, uint32_t tS, uint32_t tP, float sl2,
+                                                 const float* nl, const float* dd, float nl_row,
+                                                 float d_row, int lo, int hi) {
+  static_assert(kPartCols == 32, "one 32-column chunk per part");
+  switch (h) {
+    case 0: elementwise<kPerColumn, kWriteP, kMask, 0, 32>(tS, tP, sl2, nl, dd, nl_row, d_row, lo, hi); break;
+    case 1: elementwise<kPerColumn, kWriteP, kMask, 32, 64>(tS, tP, sl2, nl, dd, nl_row, d_row, lo, hi); break;
+    case 2: elementwise<kPerColumn, kWriteP, kMask, 64, 96>(tS, tP, sl2, nl, dd, nl_row, d_row, lo, hi); break;
+    default: elementwise<kPerColumn, kWriteP, kMask, 96, 128>(tS, tP, sl2, nl, dd, nl_row, d_row, lo, hi); break;
+  }
+}
+
+// The products over part h: k-steps [2h, 2h + 2) (16 rows of B each).
+template <int D>
+__device__ __forceinline__ void mma_tn_part(uint32_t d_tmem, uint32_t a_tmem, uint64_t db, int h,
+                                            uint32_t accumulate) {
+  switch (h) {
+    case 0: mma_tn<D, 0, 2>(d_tmem, a_tmem, db, accumulate); break;
+    case 1: mma_tn<D, 2, 4>(d_tmem, a_tmem, db, accumulate); break;
+    case 2: mma_tn<D, 4, 6>(d_tmem, a_tmem, db, accumulate); break;
+    default: mma_tn<D, 6, 8>(d_tmem, a_tmem, db, accumulate); break;
+  }
+}
+
 // Store one TMEM row segment of 32 fp32 columns, times `scale`, as bf16.
 __device__ __forceinline__ void store_row_bf16(uint32_t taddr, uint16_t* dst, float scale) {
   uint32_t r[32];
@@ -232,8 +265,8 @@ struct DkvLayout {
   // stage: Q tile, dO tile, nl[128], D[128]
   static constexpr int kStageBytes = 2 * T::kTileBytes + 2 * T::kRowBytes;
   static constexpr int kBar = kStage0 + kStages * kStageBytes;
-  // kv_full, stage_full[S], stage_empty[S], sp_full, p_full, o_full, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 4;
+  // kv_full, stage_full[S], stage_empty[S], sp_full, p_full[2], o_full, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 3 + kParts;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kSmem = kMisc + 16 + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -255,9 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto st_full = [&](int s) { return bar0 + 8 * (1 + s); };
   auto st_empty = [&](int s) { return bar0 + 8 * (1 + kStages + s); };
   const uint32_t sp_full = bar0 + 8 * (1 + 2 * kStages);
-  const uint32_t p_full = sp_full + 8;
-  const uint32_t o_full = sp_full + 16;
-  const uint32_t drain = sp_full + 24;
+  auto p_full = [&](int h) { return sp_full + 8 * (1 + h); };  // part h of the tile done
+  const uint32_t o_full = sp_full + 8 * (1 + kParts);
+  const uint32_t drain = o_full + 8;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + L::kMisc);
   const Abort ab{tmem_holder + 1, a.status};
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -289,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(st_empty(s), 1);
     }
     mbar_init(sp_full, 1);
-    mbar_init(p_full, 128);
+    for (int h = 0; h < kParts; ++h) mbar_init(p_full(h), 128);
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
     *ab.flag = 0u;
@@ -360,14 +393,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_nt<D>(tS, dK, desc_sw128(sb, 16, 1024));                  // S^T = K Q^T
         mma_nt<D>(tP, dV, desc_sw128(sb + T::kTileBytes, 16, 1024));  // dP^T = V dO^T
         mma_commit(sp_full);
-        if (!wait1(p_full, static_cast<uint32_t>(it & 1), ab)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        const uint64_t dDOs = desc_sw128(sb + T::kTileBytes, T::kBoxBytes, 1024);
+        const uint64_t dQs = desc_sw128(sb, T::kBoxBytes, 1024);
         const uint32_t acc = it > 0 ? 1u : 0u;
-        mma_tn<D>(tdV, tS, desc_sw128(sb + T::kTileBytes, T::kBoxBytes, 1024), acc);  // P^T dO
-        mma_tn<D>(tdK, tP, desc_sw128(sb, T::kBoxBytes, 1024), acc);                 // dS^T Q
+        for (int h = 0; h < kParts && ok; ++h) {
+          if (!wait1(p_full(h), static_cast<uint32_t>(it & 1), ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // dV += P^T dO and dK += dS^T Q over the queries of part h
+          mma_tn_part<D>(tdV, tS, dDOs, h, h == 0 ? acc : 1u);
+          mma_tn_part<D>(tdK, tP, dQs, h, h == 0 ? acc : 1u);
+        }
+        if (!ok) break;
         mma_commit(st_empty(s));
       }
       if (ok) {
@@ -404,11 +443,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t m = kref - qref;
         lo = m < 0 ? 0 : (m > kBN ? kBN : static_cast<int>(m));
       }
-      elementwise<true, true, kCausal>(tS + lane_off, tP + lane_off, a.scale_log2, rows,
-                                       rows + kBM, 0.f, 0.f, lo, kBN);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(p_full);
+#pragma unroll
+      for (int h = 0; h < kParts; ++h) {
+        elementwise_part<true, true, kCausal>(h, tS + lane_off, tP + lane_off, a.scale_log2,
+                                              rows, rows + kBM, 0.f, 0.f, lo, kBN);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full(h));
+      }
     }
     if (ok && wait_warp(o_full, 0, ab)) {
       tc_fence_after();
@@ -443,8 +485,8 @@ struct DqLayout {
   static constexpr int kStage0 = 2 * T::kTileBytes;
   static constexpr int kStageBytes = 2 * T::kTileBytes;  // K tile, V tile
   static constexpr int kBar = kStage0 + kStages * kStageBytes;
-  // q_full, stage_full[S], stage_empty[S], sp_full, p_full, o_full, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 4;
+  // q_full, stage_full[S], stage_empty[S], sp_full, p_full[2], o_full, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 3 + kParts;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kSmem = kMisc + 16 + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -466,9 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto st_full = [&](int s) { return bar0 + 8 * (1 + s); };
   auto st_empty = [&](int s) { return bar0 + 8 * (1 + kStages + s); };
   const uint32_t sp_full = bar0 + 8 * (1 + 2 * kStages);
-  const uint32_t p_full = sp_full + 8;
-  const uint32_t o_full = sp_full + 16;
-  const uint32_t drain = sp_full + 24;
+  auto p_full = [&](int h) { return sp_full + 8 * (1 + h); };  // part h of the tile done
+  const uint32_t o_full = sp_full + 8 * (1 + kParts);
+  const uint32_t drain = o_full + 8;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + L::kMisc);
   const Abort ab{tmem_holder + 1, a.status};
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -509,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(st_empty(s), 1);
     }
     mbar_init(sp_full, 1);
-    mbar_init(p_full, 128);
+    for (int h = 0; h < kParts; ++h) mbar_init(p_full(h), 128);
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
     *ab.flag = 0u;
@@ -575,12 +617,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_nt<D>(tS, dQ, desc_sw128(sb, 16, 1024));                    // S = Q K^T
         mma_nt<D>(tP, dDO, desc_sw128(sb + T::kTileBytes, 16, 1024));   // dP = dO V^T
         mma_commit(sp_full);
-        if (!wait1(p_full, static_cast<uint32_t>(it & 1), ab)) {
-          ok = false;
-          break;
+        const uint64_t dKs = desc_sw128(sb, T::kBoxBytes, 1024);
+        for (int h = 0; h < kParts && ok; ++h) {
+          if (!wait1(p_full(h), static_cast<uint32_t>(it & 1), ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_tn_part<D>(tdQ, tP, dKs, h, (it > 0 || h > 0) ? 1u : 0u);  // dQ += dS K, part h
         }
-        tc_fence_after();
-        mma_tn<D>(tdQ, tP, desc_sw128(sb, T::kBoxBytes, 1024), it > 0 ? 1u : 0u);  // dS K
+        if (!ok) break;
         mma_commit(st_empty(s));
       }
       if (ok) {
@@ -617,11 +663,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t n = qref - first + 1;
         hi = n < 0 ? 0 : (n > kBN ? kBN : static_cast<int>(n));
       }
-      elementwise<false, false, kCausal>(tS + lane_off, tP + lane_off, a.scale_log2, nullptr,
-                                         nullptr, nl_row, d_row, 0, hi);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(p_full);
+#pragma unroll
+      for (int h = 0; h < kParts; ++h) {
+        elementwise_part<false, false, kCausal>(h, tS + lane_off, tP + lane_off, a.scale_log2,
+                                                nullptr, nullptr, nl_row, d_row, 0, hi);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full(h));
+      }
     }
     if (ok && wait_warp(o_full, 0, ab)) {
       tc_fence_after();
