@@ -239,6 +239,42 @@ RA_API ra_status ra_forward_split_noalloc(const void* q, const void* k, const vo
                                           ra_stream_t stream);
 
 /*
+ * ra_forward_host -- ra_forward (causal = 0) or ra_forward_causal
+ * (causal = 1, with `layout`) for inputs and results in HOST memory.  The
+ * pages have no counterpart: it is the same computation with the transfers
+ * folded in.  The B*H independent (batch, head) slices are cut into chunks.
+ * Chunk c's q, k, v are copied to the device while earlier chunks compute,
+ * and its out, lse are copied back while later chunks compute, so only the
+ * first chunk's upload and the last chunk's download are not hidden.
+ *   q, k, v    HOST [B, H, N, d] of `dtype`.  Page-locked (pinned) memory
+ *              lets the copies overlap the compute; pageable memory gives the
+ *              same results with the copies serialised.
+ *   out, lse   HOST [B, H, N, d] of `dtype` and [B, H, N] fp32 (written).
+ *   workspace  DEVICE scratch of at least ra_forward_host_workspace_bytes
+ *              bytes, 256-byte aligned, owned by the caller; it holds the
+ *              device copies of q, k, v, out and lse.
+ * The call is asynchronous on `stream` like the others: the host buffers
+ * must stay valid, and out/lse are complete, only once `stream` has reached
+ * the point of the call (e.g. after cudaStreamSynchronize).  The copies and
+ * half of the chunks run on streams the library creates once per device;
+ * `stream` waits for all of them before any later work.  Calls that may
+ * overlap on the GPU need workspaces of their own.
+ * Errors: as ra_forward / ra_forward_causal (checked before anything is
+ * queued); RA_ERR_INVALID_ARG for a NULL buffer or a workspace that is too
+ * small; RA_ERR_MISALIGNED for a workspace not 256-byte aligned.  A CUDA
+ * error after the first copy was queued returns RA_ERR_CUDA; `stream` still
+ * waits for the work already queued.
+ */
+RA_API ra_status ra_forward_host(const void* q, const void* k, const void* v, void* out,
+                                 float* lse, int32_t B, int32_t H, int64_t N, int32_t d,
+                                 int32_t P, int32_t causal, ra_layout layout, ra_dtype dtype,
+                                 void* workspace, int64_t workspace_bytes, ra_stream_t stream);
+
+/* Device scratch bytes ra_forward_host needs (-1 for invalid sizes). */
+RA_API int64_t ra_forward_host_workspace_bytes(int32_t B, int32_t H, int64_t N, int32_t d,
+                                               ra_dtype dtype);
+
+/*
  * ra_backward -- gradients of ring attention ("Ring attention, explained",
  * step 6: the backward runs on the same ring, the key-value blocks carrying
  * their gradient accumulators).  For the loss L = sum(dout * out):

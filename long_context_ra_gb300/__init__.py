@@ -20,7 +20,8 @@ from ._native import RA_BF16, RA_F32, RA_MAX_PARTIALS, RaStateC
 
 __all__ = ["RaError", "RaState", "ra_forward", "ra_forward_causal", "ra_forward_partial",
            "ra_forward_partial_causal", "ra_forward_split", "ra_forward_split_workspace_bytes",
-           "ra_forward_split_segments", "ra_backward", "ra_backward_causal", "ra_state_init",
+           "ra_forward_split_segments", "ra_forward_host", "ra_forward_host_workspace_bytes",
+           "ra_backward", "ra_backward_causal", "ra_state_init",
            "ra_fold", "ra_merge",
            "ra_last_device_status", "new_state", "library_path"]
 
@@ -190,6 +191,48 @@ def ra_forward_split(q, k, v, P: int, G: int | None = None, workspace=None, out=
                                           N, d, P, G, _ptr(workspace), workspace.numel(),
                                           _dtype_code(q), _stream(stream))
     _check(code, "ra_forward_split")
+    return out, lse
+
+
+def _host_ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    if t.is_cuda:
+        raise ValueError("ra_forward_host takes host (CPU) tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def ra_forward_host_workspace_bytes(B: int, H: int, N: int, d: int, dtype) -> int:
+    code = RA_BF16 if dtype == torch.bfloat16 else RA_F32
+    return int(_native.lib().ra_forward_host_workspace_bytes(B, H, N, d, code))
+
+
+def ra_forward_host(q, k, v, P: int, out=None, lse=None, workspace=None, causal=None,
+                    stream=None):
+    """Forward for HOST tensors q, k, v ([B,H,N,d], pinned for overlap): the
+    library uploads, computes and downloads in overlapped chunks of (batch,
+    head) slices.  causal=<layout> for the causal forward.  `workspace` is a
+    CUDA uint8 tensor of ra_forward_host_workspace_bytes bytes (allocated on
+    the current device when not given).  Returns host (out, lse); the call
+    is asynchronous on `stream`, so synchronize before reading them."""
+    B, H, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share shape and dtype")
+    pinned = q.is_pinned()
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=pinned)
+    if lse is None:
+        lse = torch.empty(B, H, N, dtype=torch.float32, pin_memory=pinned)
+    nbytes = ra_forward_host_workspace_bytes(B, H, N, d, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), device=torch.cuda.current_device(),
+                                dtype=torch.uint8)
+    layout = _native.RA_LAYOUTS[causal] if causal is not None else 0
+    code = _native.lib().ra_forward_host(_host_ptr(q), _host_ptr(k), _host_ptr(v), _host_ptr(out),
+                                         _host_ptr(lse), B, H, N, d, P,
+                                         0 if causal is None else 1, layout, _dtype_code(q),
+                                         _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(code, "ra_forward_host")
     return out, lse
 
 

@@ -44,6 +44,9 @@ PROTOTYPES = {
     "ra_forward_split_noalloc": (_I32, [_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32,
                                         _I32, _P]),
     "ra_forward_split_segments": (_I32, [_I32, _I32, _I64, _I32, _I32, _I32]),
+    "ra_forward_host": (_I32, [_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32, _I32, _I32,
+                               _P, _I64, _P]),
+    "ra_forward_host_workspace_bytes": (_I64, [_I32, _I32, _I64, _I32, _I32]),
     "ra_backward": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _I32,
                            _I32, _P]),
     "ra_backward_causal": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I64, _I32,

@@ -111,6 +111,20 @@ ra_status launched(cudaError_t e) { return e == cudaSuccess ? RA_OK : RA_ERR_CUD
 
 constexpr int64_t kMaxRows = (int64_t{1} << 31) - 1;  // TMA coordinates are int32
 
+// Size rules of the attention-shaped calls (the arguments themselves are
+// already known to be in range).
+ra_status check_sizes(int64_t rows, int64_t N, int32_t d, int32_t P, ra_dtype dt) {
+  if (N % P != 0) return RA_ERR_UNSUPPORTED;
+  if (rows > kMaxRows) return RA_ERR_UNSUPPORTED;
+  if (dt == RA_BF16) {
+    if (d != 64 && d != 128) return RA_ERR_UNSUPPORTED;
+    if ((N / P) % 128 != 0) return RA_ERR_UNSUPPORTED;
+  } else if (d > 256) {
+    return RA_ERR_UNSUPPORTED;
+  }
+  return RA_OK;
+}
+
 // Shared checks of the attention-shaped calls; fills the fold arguments.
 ra_status check_attention(const void* q, const void* k, const void* v, int32_t B, int32_t H,
                           int64_t N, int32_t d, int32_t P, ra_dtype dt, FoldArgs* a) {
@@ -118,17 +132,10 @@ ra_status check_attention(const void* q, const void* k, const void* v, int32_t B
   if (dt != RA_F32 && dt != RA_BF16) return RA_ERR_INVALID_ARG;
   const int64_t rows = static_cast<int64_t>(B) * H * N;
   if (rows != 0 && (!q || !k || !v)) return RA_ERR_INVALID_ARG;
-  if (N % P != 0) return RA_ERR_UNSUPPORTED;
-  if (rows > kMaxRows) return RA_ERR_UNSUPPORTED;
-  const int64_t c = N / P;
-  if (dt == RA_BF16) {
-    if (d != 64 && d != 128) return RA_ERR_UNSUPPORTED;
-    if (c % 128 != 0) return RA_ERR_UNSUPPORTED;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return RA_ERR_MISALIGNED;
-  } else {
-    if (d > 256) return RA_ERR_UNSUPPORTED;
-    if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4)) return RA_ERR_MISALIGNED;
-  }
+  const ra_status sz = check_sizes(rows, N, d, P, dt);
+  if (sz != RA_OK) return sz;
+  const uintptr_t al = dt == RA_BF16 ? 16 : 4;
+  if (!aligned(q, al) || !aligned(k, al) || !aligned(v, al)) return RA_ERR_MISALIGNED;
   *a = FoldArgs{};
   a->q = q;
   a->k = k;
@@ -201,6 +208,20 @@ ra_status check_causal(int64_t N, int32_t P, ra_layout layout, ra_dtype dt, Fold
   a->layout = static_cast<int32_t>(layout);
   return RA_OK;
 }
+
+}  // namespace
+
+ra_status check_forward_args(int32_t B, int32_t H, int64_t N, int32_t d, int32_t P, bool causal,
+                             ra_layout layout, ra_dtype dtype) {
+  if (B < 0 || H < 0 || N < 0 || d < 1 || P < 1) return RA_ERR_INVALID_ARG;
+  if (dtype != RA_F32 && dtype != RA_BF16) return RA_ERR_INVALID_ARG;
+  const ra_status st = check_sizes(static_cast<int64_t>(B) * H * N, N, d, P, dtype);
+  if (st != RA_OK) return st;
+  FoldArgs a{};
+  return causal ? check_causal(N, P, layout, dtype, &a) : RA_OK;
+}
+
+namespace {
 
 ra_status forward_impl(const void* q, const void* k, const void* v, void* out, float* lse,
                        int32_t B, int32_t H, int64_t N, int32_t d, int32_t P, bool causal,

@@ -126,6 +126,12 @@ constexpr int kStatusTimeout = 1;
 // Number of SMs of the current device (cached).
 int device_sm_count();
 
+// The argument and size checks of ra_forward / ra_forward_causal, without
+// the buffers: the status those calls would return for a valid set of
+// buffers.
+ra_status check_forward_args(int32_t B, int32_t H, int64_t N, int32_t d, int32_t P, bool causal,
+                             ra_layout layout, ra_dtype dtype);
+
 // Bytes of scratch for G partial states of `rows` rows of width d: per
 // segment m [rows], l [rows], o [rows, d] fp32, each 256-byte aligned.
 int64_t split_workspace_bytes(int64_t rows, int32_t d, int32_t G);

@@ -148,3 +148,29 @@ def test_backward_validation(L):
     assert fb() == _native.RA_ERR_ARCH
     assert L.ra_backward_causal(A, A, A, A, A, A, A, A, A, A, 1, 1, 1024, 64, 4, 7, BF16,
                                 None) == _native.RA_ERR_INVALID_ARG
+
+
+def test_host_forward_validation(L):
+    rows, d = 2 * 1024, 64
+    up = lambda x: (x + 255) // 256 * 256
+    need = L.ra_forward_host_workspace_bytes(1, 2, 1024, d, BF16)
+    assert need == 4 * up(rows * d * 2) + up(rows * 4)
+    assert L.ra_forward_host_workspace_bytes(1, 2, 1024, d, F32) == 4 * up(rows * d * 4) + up(rows * 4)
+    assert L.ra_forward_host_workspace_bytes(-1, 2, 1024, d, BF16) == -1
+    assert L.ra_forward_host_workspace_bytes(1, 2, 1024, d, 9) == -1
+
+    def fh(q=A, out=A, ws=A, nbytes=need, N=1024, P=4, dd=d, causal=0, layout=0, dt=BF16, H=2):
+        return L.ra_forward_host(q, A, A, out, A, 1, H, N, dd, P, causal, layout, dt, ws, nbytes,
+                                 None)
+    assert fh(q=None) == _native.RA_ERR_INVALID_ARG
+    assert fh(out=None) == _native.RA_ERR_INVALID_ARG
+    assert fh(ws=None) == _native.RA_ERR_INVALID_ARG
+    assert fh(nbytes=need - 1) == _native.RA_ERR_INVALID_ARG
+    assert fh(ws=A + 16) == _native.RA_ERR_MISALIGNED       # workspace: 256-byte alignment
+    assert fh(causal=2) == _native.RA_ERR_INVALID_ARG
+    assert fh(causal=1, layout=5) == _native.RA_ERR_INVALID_ARG
+    assert fh(N=1000) == _native.RA_ERR_UNSUPPORTED          # P does not divide N
+    assert fh(dd=96) == _native.RA_ERR_UNSUPPORTED           # bf16 head dim
+    assert fh(causal=1, layout=1, N=1536, P=4) == _native.RA_ERR_UNSUPPORTED  # zigzag c % 256
+    assert fh(H=0, q=None, ws=None) == _native.RA_OK        # nothing to do
+    assert fh() == _native.RA_ERR_ARCH                      # valid; no device here
