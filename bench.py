@@ -160,9 +160,18 @@ def cpu_oracle_baseline(w, q, k, v, target_s: float):
     t0 = time.perf_counter()
     O.ring(qa, ka, va, w.P, dtype="bf16", rows=rows)
     dt = time.perf_counter() - t0
+    # the same oracle on one core, on a sample sized for about 3 s
+    O1 = ra_oracle.Oracle(threads=1)
+    n1 = int(min(n, max(4, 3.0 * n / (max(dt, 1e-6) * O.threads))))
+    rows1 = rows[np.linspace(0, len(rows) - 1, n1).astype(np.int64)]
+    t0 = time.perf_counter()
+    O1.ring(qa, ka, va, w.P, dtype="bf16", rows=rows1)
+    dt1 = time.perf_counter() - t0
     return {"value": n * per_row / dt / 1e12, "unit": UNIT, "cores": O.threads, "kind": "oracle",
             "sample": f"{n} seeded query rows of {w.name} (ring recurrence, fp64), {dt:.1f} s; "
-                      f"value = rows x 4*N*d flops / time"}, n, dt
+                      f"value = rows x 4*N*d flops / time",
+            "value_1core": n1 * per_row / dt1 / 1e12,
+            "sample_1core": f"{n1} of those rows on one core, {dt1:.1f} s"}, n, dt
 
 
 def run_reference(args, w) -> None:
