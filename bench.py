@@ -171,7 +171,8 @@ def cpu_oracle_baseline(w, q, k, v, target_s: float):
             "sample": f"{n} seeded query rows of {w.name} (ring recurrence, fp64), {dt:.1f} s; "
                       f"value = rows x 4*N*d flops / time",
             "value_1core": n1 * per_row / dt1 / 1e12,
-            "sample_1core": f"{n1} of those rows on one core, {dt1:.1f} s"}, n, dt
+            "sample_1core": f"{n1} of those rows on one core, {dt1:.1f} s",
+            "projected_full_s": dt * w.rows / n}, n, dt
 
 
 def run_reference(args, w) -> None:
