@@ -12,9 +12,10 @@
 //               tiles of those blocks.  TMEM: S^T [0,128), dP^T [128,256),
 //               dV [256, 256+D), dK [256+D, 256+2D).  Per query tile:
 //               S^T = K Q^T and dP^T = V dO^T (SS MMAs), the elementwise
-//               warps turn them into P^T and dS^T (bf16, written over the
-//               first 64 columns of S^T and dP^T), then dV += P^T dO and
-//               dK += dS^T Q (A operand from TMEM).
+//               warps turn them into P^T and dS^T (bf16; the 16 values of
+//               each k-step packed over the first 8 of their own 16 columns
+//               of S^T and dP^T), then dV += P^T dO and dK += dS^T Q (A
+//               operand from TMEM).
 //   dq_kernel   one 128-query tile per CTA walking the key tiles in the
 //               forward's ring order (i - t) mod P.  TMEM: S [0,128),
 //               dP [128,256), dQ [256, 256+D).  S = Q K^T, dP = dO V^T,
@@ -22,9 +23,9 @@
 // The row terms come precomputed per query row: D and nl = -lse * log2(e)
 // (so that p = exp2(s * tau * log2(e) + nl)).
 //
-// Warp roles (256 threads): warps 0-3 elementwise (thread = tile row = TMEM
-// lane), warp 4 TMA producer, warp 5 TMEM allocator and MMA issuer, warps 6-7
-// idle.  Every wait is bounded (see sm103_pipeline.cuh).
+// Warp roles (320 threads): warps 0-7 elementwise, two warpgroups (thread =
+// tile row = TMEM lane), warp 8 TMA producer, warp 9 TMEM allocator and MMA
+// issuer.  Every wait is bounded (see sm103_pipeline.cuh).
 
 #include <cmath>
 
@@ -38,15 +39,37 @@ namespace {
 using namespace ptx;
 using namespace sm103;
 
-constexpr int kThreads = 256;
-constexpr int kLoadWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStages = 2;
-// The elementwise pass over a tile's 128 columns is done in kParts parts; the
-// tensor-core products that read part h start as soon as part h is done.
+// The elementwise pass over a tile's 128 columns is done in kParts parts of
+// 32 columns, which are k-steps 2h and 2h + 1 of the TMEM-operand products;
+// warpgroup g takes k-step 2h + g, so both warpgroups work on every part.
+// The products that read part h start as soon as part h is done.
 constexpr int kParts = 4;
-constexpr int kPartCols = kBN / kParts;
+constexpr int kPartThreads = 256;  // arrivals per part: both warpgroups
+
+// 8 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::
+                   "r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+               "r"(r[7])
+               : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
 
 template <int D>
 struct Tiles {
@@ -77,15 +100,16 @@ __device__ __forceinline__ void mma_nt(uint32_t d_tmem, uint64_t da, uint64_t db
 }
 
 // D[tmem] (+)= A[tmem] B over rows [16 k0, 16 k1) of B: A is 128 x 128 bf16
-// packed in TMEM (8 columns per 16 values), B an MN-major 128 x D tile in
-// SMEM.  `accumulate` applies to the first product only.
+// in TMEM, the 16 values of k-step kk packed into the 8 columns at 16 kk; B
+// an MN-major 128 x D tile in SMEM.  `accumulate` applies to the first
+// product only.
 template <int D, int k0, int k1>
 __device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint64_t db,
                                        uint32_t accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, true);
 #pragma unroll
   for (int kk = k0; kk < k1; ++kk)
-    mma_bf16_ts(d_tmem, a_tmem + kk * 8, db + desc_step(kk * 16 * 128), idesc,
+    mma_bf16_ts(d_tmem, a_tmem + kk * 16, db + desc_step(kk * 16 * 128), idesc,
                 kk == k0 ? accumulate : 1u);
 }
 
@@ -95,39 +119,38 @@ __device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // where nl and Dr are per column (dkv kernel: per query, from SMEM) or per
 // row (dq kernel: scalars).  With kMask, columns outside [lo, hi) are masked
 // (their score is -inf, so p = ds = 0).  p (if kWriteP) and ds are rounded
-// to bf16 pairs and written over the first 64 columns of tS and tP.  One call
-// covers the columns [c0, c1): the tile is done in two halves, so that the
-// products over the first half can run while the second half is computed.
-template <bool kPerColumn, bool kWriteP, bool kMask, int c0, int c1>
-__device__ __forceinline__ void elementwise(uint32_t tS, uint32_t tP, float sl2, const float* nl,
-                                            const float* dd, float nl_row, float d_row, int lo,
-                                            int hi) {
-#pragma unroll
-  for (int c = c0; c < c1; c += 32) {
-    uint32_t s[32], g[32];
-    tmem_ld32(tS + c, s);
-    tmem_ld32(tP + c, g);
+// to bf16 pairs and written over the first 8 of these 16 columns of tS and
+// tP (columns this warp has just read).  One call covers the 16 columns
+// [c, c + 16), one k-step of the products that read them.
+template <bool kPerColumn, bool kWriteP, bool kMask>
+__device__ __forceinline__ void elementwise(int c, uint32_t tS, uint32_t tP, float sl2,
+                                            const float* nl, const float* dd, float nl_row,
+                                            float d_row, int lo, int hi) {
+  {
+    uint32_t s[16], g[16];
+    tmem_ld16(tS + c, s);
+    tmem_ld16(tP + c, g);
     tmem_ld_wait();
-    reg_fence(s, 32);
-    reg_fence(g, 32);
+    reg_fence(s, 16);
+    reg_fence(g, 16);
     if (kMask) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
+      for (int e = 0; e < 16; ++e)
         if (c + e < lo || c + e >= hi) s[e] = 0xff800000u;  // -inf
     }
-    float ncol[kPerColumn ? 32 : 1], dcol[kPerColumn ? 32 : 1];
+    float ncol[kPerColumn ? 16 : 1], dcol[kPerColumn ? 16 : 1];
     if (kPerColumn) {
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) {
+      for (int e = 0; e < 16; e += 4) {
         const float4 x = *reinterpret_cast<const float4*>(nl + c + e);
         const float4 y = *reinterpret_cast<const float4*>(dd + c + e);
         ncol[e] = x.x, ncol[e + 1] = x.y, ncol[e + 2] = x.z, ncol[e + 3] = x.w;
         dcol[e] = y.x, dcol[e + 1] = y.y, dcol[e + 2] = y.z, dcol[e + 3] = y.w;
       }
     }
-    uint32_t pk[16], dk[16];
+    uint32_t pk[8], dk[8];
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) {
+    for (int e = 0; e < 16; e += 2) {
       float n0 = nl_row, n1 = nl_row, d0 = d_row, d1 = d_row;
       if (kPerColumn) {
         n0 = ncol[e];
@@ -142,9 +165,8 @@ __device__ __forceinline__ void elementwise(uint32_t tS, uint32_t tP, float sl2,
       pk[e / 2] = pack_bf16x2(p0, p1);
       dk[e / 2] = pack_bf16x2(ds0, ds1);
     }
-    // columns [c/2, c/2 + 16) of tS / tP were read by this or an earlier chunk
-    if (kWriteP) tmem_st16(tS + c / 2, pk);
-    tmem_st16(tP + c / 2, dk);
+    if (kWriteP) tmem_st8(tS + c, pk);
+    tmem_st8(tP + c, dk);
   }
 }
 
@@ -209,18 +231,13 @@ struct KWalk {
   }
 };
 
-// Part h of the elementwise pass: columns [h * kPartCols, (h + 1) * kPartCols).
+// Warpgroup g's share of part h: the 16 columns of k-step 2h + g.
 template <bool kPerColumn, bool kWriteP, bool kMask>
-__device__ __forceinline__ void elementwise_part(int h, uint32_t tS, uint32_t tP, float sl2,
-                                                 const float* nl, const float* dd, float nl_row,
-                                                 float d_row, int lo, int hi) {
-  static_assert(kPartCols == 32, "one 32-column chunk per part");
-  switch (h) {
-    case 0: elementwise<kPerColumn, kWriteP, kMask, 0, 32>(tS, tP, sl2, nl, dd, nl_row, d_row, lo, hi); break;
-    case 1: elementwise<kPerColumn, kWriteP, kMask, 32, 64>(tS, tP, sl2, nl, dd, nl_row, d_row, lo, hi); break;
-    case 2: elementwise<kPerColumn, kWriteP, kMask, 64, 96>(tS, tP, sl2, nl, dd, nl_row, d_row, lo, hi); break;
-    default: elementwise<kPerColumn, kWriteP, kMask, 96, 128>(tS, tP, sl2, nl, dd, nl_row, d_row, lo, hi); break;
-  }
+__device__ __forceinline__ void elementwise_part(int h, int g, uint32_t tS, uint32_t tP,
+                                                 float sl2, const float* nl, const float* dd,
+                                                 float nl_row, float d_row, int lo, int hi) {
+  elementwise<kPerColumn, kWriteP, kMask>(16 * (2 * h + g), tS, tP, sl2, nl, dd, nl_row, d_row,
+                                          lo, hi);
 }
 
 // The products over part h: k-steps [2h, 2h + 2) (16 rows of B each).
@@ -322,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(st_empty(s), 1);
     }
     mbar_init(sp_full, 1);
-    for (int h = 0; h < kParts; ++h) mbar_init(p_full(h), 128);
+    for (int h = 0; h < kParts; ++h) mbar_init(p_full(h), kPartThreads);
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
     *ab.flag = 0u;
@@ -416,9 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_drain(drain, 0);
       }
     }
-  } else if (warp < 4) {
-    const int row = warp * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  } else if (warp < 8) {
+    const int wg = warp / 4;  // warpgroup: k-step 2h + wg of every part h
+    const int row = (warp % 4) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
     // this thread's key: position (striped: local row) for the mask
     const int64_t kref = walk.kfirst + row;
     KWalk w = walk;
@@ -445,8 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
-        elementwise_part<true, true, kCausal>(h, tS + lane_off, tP + lane_off, a.scale_log2,
-                                              rows, rows + kBM, 0.f, 0.f, lo, kBN);
+        elementwise_part<true, true, kCausal>(h, wg, tS + lane_off, tP + lane_off,
+                                              a.scale_log2, rows, rows + kBM, 0.f, 0.f, lo, kBN);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(p_full(h));
@@ -458,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint16_t* dv = static_cast<uint16_t*>(a.dv) + r * D;
       uint16_t* dk = static_cast<uint16_t*>(a.dk) + r * D;
 #pragma unroll
-      for (int cc = 0; cc < D; cc += 32) {
+      for (int cc = wg * (D / 2); cc < (wg + 1) * (D / 2); cc += 32) {
         store_row_bf16(tdV + lane_off + cc, dv + cc, 1.f);
         store_row_bf16(tdK + lane_off + cc, dk + cc, a.tau);
       }
@@ -551,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(st_empty(s), 1);
     }
     mbar_init(sp_full, 1);
-    for (int h = 0; h < kParts; ++h) mbar_init(p_full(h), 128);
+    for (int h = 0; h < kParts; ++h) mbar_init(p_full(h), kPartThreads);
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
     *ab.flag = 0u;
@@ -636,9 +654,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_drain(drain, 0);
       }
     }
-  } else if (warp < 4) {
-    const int row = warp * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  } else if (warp < 8) {
+    const int wg = warp / 4;  // warpgroup: k-step 2h + wg of every part h
+    const int row = (warp % 4) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const int64_t lrow = qlr0 + row;
     const int64_t qpos = walk.pos(i, lrow);
     const int64_t r = slice * a.N + qpos;  // row of dq
@@ -665,8 +684,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
-        elementwise_part<false, false, kCausal>(h, tS + lane_off, tP + lane_off, a.scale_log2,
-                                                nullptr, nullptr, nl_row, d_row, 0, hi);
+        elementwise_part<false, false, kCausal>(h, wg, tS + lane_off, tP + lane_off,
+                                                a.scale_log2, nullptr, nullptr, nl_row, d_row, 0,
+                                                hi);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(p_full(h));
@@ -676,7 +696,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint16_t* dq = static_cast<uint16_t*>(a.dq) + r * D;
 #pragma unroll
-      for (int cc = 0; cc < D; cc += 32) store_row_bf16(tdQ + lane_off + cc, dq + cc, a.tau);
+      for (int cc = wg * (D / 2); cc < (wg + 1) * (D / 2); cc += 32)
+        store_row_bf16(tdQ + lane_off + cc, dq + cc, a.tau);
     }
   }
 
