@@ -66,6 +66,10 @@ constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
+// Every p is >= 0, so a tile whose row sum of p is at most 2^kRescaleLog2
+// has no p above 2^kRescaleLog2.
+constexpr float kFastSumBound = 256.0f;
+static_assert(kFastSumBound == (1 << static_cast<int>(kRescaleLog2)), "2^kRescaleLog2");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -150,6 +154,37 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 #pragma unroll
   for (int kk = 1; kk < kBN / 16; ++kk)
     mma_bf16_ts(d_tmem, p_tmem + kk * 8, dv + desc_step(kk * 16 * 128), idesc, 1u);
+}
+
+// p = exp2(s * sl2 + neg) for the 128 scores of this row, two per FMA; p is
+// rounded to bf16 pairs and written over the first 64 columns of S (tS),
+// where the P V product reads it.  Returns the row sum of p (four
+// independent pair sums).
+__device__ __forceinline__ float exp_store(const uint32_t (&s)[kBN], uint64_t scale2,
+                                           uint64_t neg2, uint32_t tS) {
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const int j = half * 64 + 2 * jj;
+      const uint64_t x =
+          fma_f32x2(pack_f32x2(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), scale2, neg2);
+      float x0, x1;
+      unpack_f32x2(x, x0, x1);
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      acc[jj & 3] = add_f32x2(acc[jj & 3], pack_f32x2(p0, p1));
+      pk[jj] = pack_bf16x2(p0, p1);
+    }
+    tmem_st32(tS + static_cast<uint32_t>(half * 32), pk);
+  }
+  float a0, a1, a2, a3, a4, a5, a6, a7;
+  unpack_f32x2(acc[0], a0, a1);
+  unpack_f32x2(acc[1], a2, a3);
+  unpack_f32x2(acc[2], a4, a5);
+  unpack_f32x2(acc[3], a6, a7);
+  return ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
 }
 
 template <int D, bool kCausal>
@@ -451,74 +486,68 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 
-        // Row max: eight independent chains of three-input maxima.
-        float mx[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(__uint_as_float(s[e]), __uint_as_float(s[e + 8]));
-#pragma unroll
-        for (int j = 16; j < kBN; j += 16) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            mx[e] = fmax3(mx[e], __uint_as_float(s[j + e]), __uint_as_float(s[j + 8 + e]));
-        }
-        const float rmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                 fmaxf(mx[6], mx[7]));
-        const float m_new = rmax * sl2;
-        m_true = fmaxf(m_true, m_new);
-        const bool need = m_new > m_ref + kRescaleLog2;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? ex2(m_ref - m_new) : 1.f;
-          if (o_valid) {
-#pragma unroll
-            for (int c = 0; c < D; c += 32) {
-              uint32_t r[32];
-              tmem_ld32(tO + c, r);
-              tmem_ld_wait();
-              reg_fence(r, 32);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-              tmem_st32(tO + c, r);
-            }
-            tmem_st_wait();
-          }
-          if (need) {
-            l *= alpha;
-            m_ref = m_new;
-          }
-        }
-
-        // p = exp2(s * tau * log2(e) - m_ref), two scores per FMA; the row
-        // sum runs in four independent pairs.  p is rounded to bf16 pairs and
-        // written over the first 64 columns of S, where the P V product reads
-        // it.
         const uint64_t scale2 = pack_f32x2(sl2, sl2);
-        // a row that has seen no visible key yet keeps m_ref = -inf; its
-        // masked scores must still give p = 0 rather than NaN
-        const float neg = (kCausal && m_ref == -INFINITY) ? 0.f : -m_ref;
-        const uint64_t neg2 = pack_f32x2(neg, neg);
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int j = half * 64 + 2 * jj;
-            const uint64_t x = fma_f32x2(
-                pack_f32x2(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), scale2, neg2);
-            float x0, x1;
-            unpack_f32x2(x, x0, x1);
-            const float p0 = ex2(x0), p1 = ex2(x1);
-            acc[jj & 3] = add_f32x2(acc[jj & 3], pack_f32x2(p0, p1));
-            pk[jj] = pack_bf16x2(p0, p1);
+        // Fast path (the forward, once the reference is set): the row max is
+        // needed only to move the reference, which must move when some p
+        // against it would exceed 2^kRescaleLog2.  A row sum of p at most
+        // kFastSumBound rules that out (every p >= 0), so the exponentials
+        // come first and the max is skipped.  If a row's sum is over the
+        // bound (rarely: p is mostly well below 1), the warp redoes the tile
+        // through the exact path below.  A unit's first tile goes there
+        // directly.  Any reference gives the same l and o, so both paths are
+        // exact.  The partial and fold modes always take the exact path,
+        // since they report the true running max.
+        bool redo = true;
+        if (a.mode == kForward && __all_sync(0xffffffffu, m_ref != -INFINITY)) {
+          const float lt = exp_store(s, scale2, pack_f32x2(-m_ref, -m_ref), tS);
+          if (!__any_sync(0xffffffffu, lt > kFastSumBound)) {
+            l += lt;
+            redo = false;
+          } else {
+            tmem_st_wait();  // the redo's stores land after these
           }
-          tmem_st32(tS + static_cast<uint32_t>(half * 32), pk);
         }
-        float a0, a1, a2, a3, a4, a5, a6, a7;
-        unpack_f32x2(acc[0], a0, a1);
-        unpack_f32x2(acc[1], a2, a3);
-        unpack_f32x2(acc[2], a4, a5);
-        unpack_f32x2(acc[3], a6, a7);
-        l += ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
+        if (redo) {
+          // Row max: eight independent chains of three-input maxima.
+          float mx[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx[e] = fmaxf(__uint_as_float(s[e]), __uint_as_float(s[e + 8]));
+#pragma unroll
+          for (int j = 16; j < kBN; j += 16) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              mx[e] = fmax3(mx[e], __uint_as_float(s[j + e]), __uint_as_float(s[j + 8 + e]));
+          }
+          const float rmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                   fmaxf(mx[6], mx[7]));
+          const float m_new = rmax * sl2;
+          m_true = fmaxf(m_true, m_new);
+          const bool need = m_new > m_ref + kRescaleLog2;
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ex2(m_ref - m_new) : 1.f;
+            if (o_valid) {
+#pragma unroll
+              for (int c = 0; c < D; c += 32) {
+                uint32_t r[32];
+                tmem_ld32(tO + c, r);
+                tmem_ld_wait();
+                reg_fence(r, 32);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                tmem_st32(tO + c, r);
+              }
+              tmem_st_wait();
+            }
+            if (need) {
+              l *= alpha;
+              m_ref = m_new;
+            }
+          }
+          // a row that has seen no visible key yet keeps m_ref = -inf; its
+          // masked scores must still give p = 0 rather than NaN
+          const float neg = (kCausal && m_ref == -INFINITY) ? 0.f : -m_ref;
+          l += exp_store(s, scale2, pack_f32x2(neg, neg), tS);
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bars.p_full(t));
