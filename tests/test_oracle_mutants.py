@@ -3,7 +3,8 @@
 The mistakes are compiled into separate copies of the oracle via the
 ``ORA_MUTANT`` switch: o not rescaled (1), l not rescaled (2), per-block
 normalise-then-average (3), 1/d instead of 1/sqrt(d) (4), sign flip in the
-exponent (5), K used in place of V (6).
+exponent (5), K used in place of V (6), a strict causal mask that hides the
+query's own key (7), the backward's row term D dropped from dS (8).
 """
 import numpy as np
 import pytest
