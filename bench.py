@@ -196,7 +196,7 @@ def run_reference(args, w) -> None:
     t0 = time.perf_counter()
     O.ring(qa, ka, va, w.P, dtype="bf16", rows=probe)
     t_probe = (time.perf_counter() - t0) / len(probe)
-    budget = 120.0 / max(1, args.steps + args.warmup)  # whole run within ~2 minutes
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)  # whole run ~2 minutes
     n = int(max(4, min(4096, budget / max(t_probe, 1e-6))))
     times = []
     for s in range(args.warmup + args.steps):
@@ -404,6 +404,8 @@ def main() -> None:
                     help="time ra_backward (5 products per head counted: 10 B H N^2 d)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="CPU time of the whole --impl reference run (default 120 s)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # timing rule: at least 3 warm-up steps
     from long_context_ra_gb300 import synth
