@@ -174,3 +174,17 @@ def test_host_forward_validation(L):
     assert fh(causal=1, layout=1, N=1536, P=4) == _native.RA_ERR_UNSUPPORTED  # zigzag c % 256
     assert fh(H=0, q=None, ws=None) == _native.RA_OK        # nothing to do
     assert fh() == _native.RA_ERR_ARCH                      # valid; no device here
+
+
+def test_largest_sizes(L):
+    # TMA coordinates are int32: B*H*N rows must stay below 2^31
+    big = 1 << 31
+    assert fwd(L, N=big, P=1 << 14, d=128) == _native.RA_ERR_UNSUPPORTED
+    assert fwd(L, B=2, H=1 << 14, N=1 << 16, P=1 << 9, d=128) == _native.RA_ERR_UNSUPPORTED
+    # one row less than the limit passes the size rules (then stops at the device check)
+    assert fwd(L, B=1, H=(1 << 14) - 1, N=1 << 17, P=1 << 10, d=128) == _native.RA_ERR_ARCH
+    # the causal bf16 path keeps one step-table entry per ring step: P <= 1024
+    assert L.ra_forward_causal(A, A, A, A, A, 1, 1, 1024 * 128, 128, 1024, 0, BF16, None) == \
+        _native.RA_ERR_ARCH
+    assert L.ra_forward_causal(A, A, A, A, A, 1, 1, 1025 * 128, 128, 1025, 0, BF16, None) == \
+        _native.RA_ERR_UNSUPPORTED
