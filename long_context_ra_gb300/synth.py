@@ -114,24 +114,40 @@ def make_inputs(w: Workload, device="cuda", seed: int | None = None, shape=None)
 
 
 def sample_rows(w: Workload, count: int, seed: int = 7, shape=None) -> torch.Tensor:
-    """Flat query-row indices into [B*H*N] for sampled parity checks.
+    """Flat query-row indices into [B*H*N] for sampled parity checks (CPU
+    int64 tensor, sorted, unique, `count` of them when there are enough rows).
 
-    Covers every (b, h) and every query block: the first and last row of each
-    block, then seeded uniform rows until `count` (CPU int64 tensor, sorted,
-    unique)."""
+    Strata, in order: the first and last row of every (b, h, query block);
+    then, up to half of the remaining count, the first and last row of seeded
+    128-row query tiles (every head in turn, the tiles of a head drawn without
+    replacement), which are the lanes 0 and 127 of the kernel's tiles; then
+    seeded uniform rows.  If the block boundaries alone exceed `count`, a
+    seeded subset of them is returned."""
     B, H, N, d = shape if shape is not None else (w.B, w.H, w.N, w.d)
     c = N // w.P
+    g = torch.Generator().manual_seed(seed)
     rows = []
     for bh in range(B * H):
         for i in range(w.P):
             rows.append(bh * N + i * c)
             rows.append(bh * N + i * c + c - 1)
     allr = torch.unique(torch.tensor(rows, dtype=torch.int64))
-    g = torch.Generator().manual_seed(seed)
     if allr.numel() > count:
         keep = torch.randperm(allr.numel(), generator=g)[:count]
         return torch.unique(allr[keep])
     count = min(count, B * H * N)
+    tiles = N // 128
+    want_tiles = (count - allr.numel()) // 2
+    if tiles > 0 and want_tiles > 0:
+        orders = [torch.randperm(tiles, generator=g) for _ in range(B * H)]
+        picked, r = [], 0
+        while len(picked) < want_tiles and r < tiles:
+            for bh in range(B * H):
+                t = int(orders[bh][r])
+                picked += [bh * N + t * 128, bh * N + t * 128 + 127]
+            r += 1
+        picked = torch.tensor(picked[:want_tiles], dtype=torch.int64)
+        allr = torch.unique(torch.cat([allr, picked]))
     while allr.numel() < count:
         extra = torch.randint(0, B * H * N, (count - allr.numel(),), generator=g)
         allr = torch.unique(torch.cat([allr, extra]))

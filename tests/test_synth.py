@@ -54,6 +54,14 @@ def test_sample_rows_cover_blocks():
     assert int(rows.max()) < w.rows
     blocks = set(((rows // w.N) * w.P + (rows % w.N) // w.c).tolist())
     assert len(blocks) == w.B * w.H * w.P  # every (b, h, query block)
+    # tile boundaries (lanes 0 and 127) of many tiles in every head, and
+    # interior rows too
+    lane = (rows % w.N) % 128
+    assert (lane == 0).sum() > 900 and (lane == 127).sum() > 900
+    for bh in range(w.B * w.H):
+        mine = rows[(rows // w.N) == bh]
+        assert ((mine % w.N) % 128 == 0).sum() >= 100
+    assert ((lane > 0) & (lane < 127)).sum() > 1500
 
 
 def test_workload_sizes():
