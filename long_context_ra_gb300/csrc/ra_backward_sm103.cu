@@ -170,6 +170,73 @@ __device__ __forceinline__ void elementwise(int c, uint32_t tS, uint32_t tP, flo
   }
 }
 
+// 8 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+
+// The elementwise work of the dK/dV kernel in two passes, so that each
+// overlaps a product on the tensor cores.  Pass A (needs only S^T) makes
+//   p = exp2(s * sl2 + nl)        (nl per column, from SMEM)
+// for the 16 columns [c, c + 16), masked to 0 outside [lo, hi), and stores p
+// as bf16 pairs over the first 8 of these columns of tS (read by the dV
+// product and by pass B).
+template <bool kMask>
+__device__ __forceinline__ void pass_p(int c, uint32_t tS, float sl2, const float* nl, int lo,
+                                       int hi) {
+  uint32_t s[16];
+  tmem_ld16(tS + c, s);
+  float ncol[16];
+#pragma unroll
+  for (int e = 0; e < 16; e += 4) {
+    const float4 x = *reinterpret_cast<const float4*>(nl + c + e);
+    ncol[e] = x.x, ncol[e + 1] = x.y, ncol[e + 2] = x.z, ncol[e + 3] = x.w;
+  }
+  tmem_ld_wait();
+  reg_fence(s, 16);
+  if (kMask) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if (c + e < lo || c + e >= hi) s[e] = 0xff800000u;  // -inf
+  }
+  uint32_t pk[8];
+#pragma unroll
+  for (int e = 0; e < 16; e += 2)
+    pk[e / 2] = pack_bf16x2(ex2(fmaf(__uint_as_float(s[e]), sl2, ncol[e])),
+                            ex2(fmaf(__uint_as_float(s[e + 1]), sl2, ncol[e + 1])));
+  tmem_st8(tS + c, pk);
+}
+
+// Pass B (needs dP^T and pass A): ds = p * (dp - Dr) on the same 16 columns,
+// with p read back as the bf16 pairs pass A stored (the same p the dV product
+// uses), stored as bf16 pairs over the first 8 of these columns of tP.
+__device__ __forceinline__ void pass_ds(int c, uint32_t tS, uint32_t tP, const float* dd) {
+  uint32_t g[16], pk[8];
+  tmem_ld16(tP + c, g);
+  tmem_ld8(tS + c, pk);
+  float dcol[16];
+#pragma unroll
+  for (int e = 0; e < 16; e += 4) {
+    const float4 y = *reinterpret_cast<const float4*>(dd + c + e);
+    dcol[e] = y.x, dcol[e + 1] = y.y, dcol[e + 2] = y.z, dcol[e + 3] = y.w;
+  }
+  tmem_ld_wait();
+  reg_fence(g, 16);
+  reg_fence(pk, 8);
+  uint32_t dk[8];
+#pragma unroll
+  for (int e = 0; e < 16; e += 2) {
+    const float p0 = __uint_as_float(pk[e / 2] << 16);
+    const float p1 = __uint_as_float(pk[e / 2] & 0xffff0000u);
+    dk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(g[e]) - dcol[e]),
+                            p1 * (__uint_as_float(g[e + 1]) - dcol[e + 1]));
+  }
+  tmem_st8(tP + c, dk);
+}
+
 // The query tiles a key tile visits in the dK/dV kernel: ring steps t = 0 ..
 // P-1 bring query block i = (j + t) mod P (the key block is on device j + t
 // at step t); under the causal mask only query tiles holding a query at or
@@ -282,8 +349,9 @@ struct DkvLayout {
   // stage: Q tile, dO tile, nl[128], D[128]
   static constexpr int kStageBytes = 2 * T::kTileBytes + 2 * T::kRowBytes;
   static constexpr int kBar = kStage0 + kStages * kStageBytes;
-  // kv_full, stage_full[S], stage_empty[S], sp_full, p_full[2], o_full, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 3 + kParts;
+  // kv_full, stage_full[S], stage_empty[S], s_full, dp_full, pa[kParts],
+  // pb[kParts], o_full, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2 * kParts;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kSmem = kMisc + 16 + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -304,9 +372,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto kv_full = [&]() { return bar0; };
   auto st_full = [&](int s) { return bar0 + 8 * (1 + s); };
   auto st_empty = [&](int s) { return bar0 + 8 * (1 + kStages + s); };
-  const uint32_t sp_full = bar0 + 8 * (1 + 2 * kStages);
-  auto p_full = [&](int h) { return sp_full + 8 * (1 + h); };  // part h of the tile done
-  const uint32_t o_full = sp_full + 8 * (1 + kParts);
+  const uint32_t s_full = bar0 + 8 * (1 + 2 * kStages);  // S^T of the tile done
+  const uint32_t dp_full = s_full + 8;                      // dP^T of the tile done
+  auto pa = [&](int h) { return dp_full + 8 * (1 + h); };  // pass A, part h done
+  auto pb = [&](int h) { return dp_full + 8 * (1 + kParts + h); };  // pass B, part h done
+  const uint32_t o_full = dp_full + 8 * (1 + 2 * kParts);
   const uint32_t drain = o_full + 8;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + L::kMisc);
   const Abort ab{tmem_holder + 1, a.status};
@@ -338,8 +408,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(st_full(s), 1);
       mbar_init(st_empty(s), 1);
     }
-    mbar_init(sp_full, 1);
-    for (int h = 0; h < kParts; ++h) mbar_init(p_full(h), kPartThreads);
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    for (int h = 0; h < kParts; ++h) {
+      mbar_init(pa(h), kPartThreads);
+      mbar_init(pb(h), kPartThreads);
+    }
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
     *ab.flag = 0u;
@@ -396,35 +470,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
+      // Per tile, in pipe order: dP^T; dV over the parts of pass A as they
+      // land; dK over the parts of pass B; then the next tile's S^T (issued
+      // at the end of the previous iteration).  Pass A runs while dP^T is on
+      // the tensor cores and pass B while dV is.  The next S^T overwrites the
+      // p that pass B reads, so it waits for all of pass B.
       const uint64_t dK = desc_sw128(base + L::kK, 16, 1024);
       const uint64_t dV = desc_sw128(base + L::kV, 16, 1024);
       bool ok = wait1(kv_full(), 0, ab);
+      if (ok && n_iter > 0) ok = wait1(st_full(0), 0, ab);
+      if (ok && n_iter > 0) {
+        tc_fence_after();
+        mma_nt<D>(tS, dK, desc_sw128(base + L::kStage0, 16, 1024));  // S^T = K Q^T
+        mma_commit(s_full);
+      }
       for (int it = 0; it < n_iter && ok; ++it) {
         const int s = it % kStages;
-        if (!wait1(st_full(s), static_cast<uint32_t>((it / kStages) & 1), ab)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
         const uint32_t sb = base + L::kStage0 + s * L::kStageBytes;
-        mma_nt<D>(tS, dK, desc_sw128(sb, 16, 1024));                  // S^T = K Q^T
+        const uint32_t par = static_cast<uint32_t>(it & 1);
         mma_nt<D>(tP, dV, desc_sw128(sb + T::kTileBytes, 16, 1024));  // dP^T = V dO^T
-        mma_commit(sp_full);
+        mma_commit(dp_full);
         const uint64_t dDOs = desc_sw128(sb + T::kTileBytes, T::kBoxBytes, 1024);
         const uint64_t dQs = desc_sw128(sb, T::kBoxBytes, 1024);
         const uint32_t acc = it > 0 ? 1u : 0u;
         for (int h = 0; h < kParts && ok; ++h) {
-          if (!wait1(p_full(h), static_cast<uint32_t>(it & 1), ab)) {
+          if (!wait1(pa(h), par, ab)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // dV += P^T dO and dK += dS^T Q over the queries of part h
-          mma_tn_part<D>(tdV, tS, dDOs, h, h == 0 ? acc : 1u);
-          mma_tn_part<D>(tdK, tP, dQs, h, h == 0 ? acc : 1u);
+          mma_tn_part<D>(tdV, tS, dDOs, h, h == 0 ? acc : 1u);  // dV += P^T dO, part h
+        }
+        for (int h = 0; h < kParts && ok; ++h) {
+          if (!wait1(pb(h), par, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_tn_part<D>(tdK, tP, dQs, h, h == 0 ? acc : 1u);  // dK += dS^T Q, part h
         }
         if (!ok) break;
         mma_commit(st_empty(s));
+        if (it + 1 < n_iter) {
+          const int s1 = (it + 1) % kStages;
+          if (!wait1(st_full(s1), static_cast<uint32_t>(((it + 1) / kStages) & 1), ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_nt<D>(tS, dK, desc_sw128(base + L::kStage0 + s1 * L::kStageBytes, 16, 1024));
+          mma_commit(s_full);
+        }
       }
       if (ok) {
         mma_commit(o_full);
@@ -444,7 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       if (kCausal && it > 0) w.next();
-      if (!wait_warp(sp_full, static_cast<uint32_t>(it & 1), ab)) {
+      const uint32_t par = static_cast<uint32_t>(it & 1);
+      if (!wait_warp(s_full, par, ab)) {
         ok = false;
         break;
       }
@@ -461,13 +558,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t m = kref - qref;
         lo = m < 0 ? 0 : (m > kBN ? kBN : static_cast<int>(m));
       }
+      // pass A: p, feeding dV (warpgroup wg takes k-step 2h + wg of part h)
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
-        elementwise_part<true, true, kCausal>(h, wg, tS + lane_off, tP + lane_off,
-                                              a.scale_log2, rows, rows + kBM, 0.f, 0.f, lo, kBN);
+        pass_p<kCausal>(16 * (2 * h + wg), tS + lane_off, a.scale_log2, rows, lo, kBN);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full(h));
+        mbar_arrive(pa(h));
+      }
+      // pass B: dS, feeding dK
+      if (!wait_warp(dp_full, par, ab)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < kParts; ++h) {
+        pass_ds(16 * (2 * h + wg), tS + lane_off, tP + lane_off, rows + kBM);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(pb(h));
       }
     }
     if (ok && wait_warp(o_full, 0, ab)) {
