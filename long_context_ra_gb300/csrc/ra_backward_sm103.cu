@@ -203,10 +203,15 @@ __device__ __forceinline__ void pass_p(int c, uint32_t tS, float sl2, const floa
       if (c + e < lo || c + e >= hi) s[e] = 0xff800000u;  // -inf
   }
   uint32_t pk[8];
+  const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
 #pragma unroll
-  for (int e = 0; e < 16; e += 2)
-    pk[e / 2] = pack_bf16x2(ex2(fmaf(__uint_as_float(s[e]), sl2, ncol[e])),
-                            ex2(fmaf(__uint_as_float(s[e + 1]), sl2, ncol[e + 1])));
+  for (int e = 0; e < 16; e += 2) {
+    const uint64_t x = fma_f32x2(pack_f32x2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),
+                                 sl2x2, pack_f32x2(ncol[e], ncol[e + 1]));
+    float x0, x1;
+    unpack_f32x2(x, x0, x1);
+    pk[e / 2] = pack_bf16x2(ex2(x0), ex2(x1));
+  }
   tmem_st8(tS + c, pk);
 }
 
@@ -227,12 +232,18 @@ __device__ __forceinline__ void pass_ds(int c, uint32_t tS, uint32_t tP, const f
   reg_fence(g, 16);
   reg_fence(pk, 8);
   uint32_t dk[8];
+  const uint64_t minus1 = pack_f32x2(-1.f, -1.f);
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
-    const float p0 = __uint_as_float(pk[e / 2] << 16);
-    const float p1 = __uint_as_float(pk[e / 2] & 0xffff0000u);
-    dk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(g[e]) - dcol[e]),
-                            p1 * (__uint_as_float(g[e + 1]) - dcol[e + 1]));
+    const uint64_t p = pack_f32x2(__uint_as_float(pk[e / 2] << 16),
+                                  __uint_as_float(pk[e / 2] & 0xffff0000u));
+    // dp - Dr, then times p, two columns per instruction
+    const uint64_t diff =
+        fma_f32x2(pack_f32x2(dcol[e], dcol[e + 1]), minus1,
+                  pack_f32x2(__uint_as_float(g[e]), __uint_as_float(g[e + 1])));
+    float d0, d1;
+    unpack_f32x2(mul_f32x2(p, diff), d0, d1);
+    dk[e / 2] = pack_bf16x2(d0, d1);
   }
   tmem_st8(tP + c, dk);
 }
