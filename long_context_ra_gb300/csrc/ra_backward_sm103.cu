@@ -184,16 +184,22 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
 // for the 16 columns [c, c + 16), masked to 0 outside [lo, hi), and stores p
 // as bf16 pairs over the first 8 of these columns of tS (read by the dV
 // product and by pass B).
-template <bool kMask>
-__device__ __forceinline__ void pass_p(int c, uint32_t tS, float sl2, const float* nl, int lo,
-                                       int hi) {
+// In the dQ kernel the row term is one scalar per thread (kPerColumn false:
+// nl_row, and the mask keeps the columns below hi).
+template <bool kPerColumn, bool kMask>
+__device__ __forceinline__ void pass_p(int c, uint32_t tS, float sl2, const float* nl,
+                                       float nl_row, int lo, int hi) {
   uint32_t s[16];
   tmem_ld16(tS + c, s);
   float ncol[16];
 #pragma unroll
   for (int e = 0; e < 16; e += 4) {
-    const float4 x = *reinterpret_cast<const float4*>(nl + c + e);
-    ncol[e] = x.x, ncol[e + 1] = x.y, ncol[e + 2] = x.z, ncol[e + 3] = x.w;
+    if (kPerColumn) {
+      const float4 x = *reinterpret_cast<const float4*>(nl + c + e);
+      ncol[e] = x.x, ncol[e + 1] = x.y, ncol[e + 2] = x.z, ncol[e + 3] = x.w;
+    } else {
+      ncol[e] = ncol[e + 1] = ncol[e + 2] = ncol[e + 3] = nl_row;
+    }
   }
   tmem_ld_wait();
   reg_fence(s, 16);
@@ -218,15 +224,21 @@ __device__ __forceinline__ void pass_p(int c, uint32_t tS, float sl2, const floa
 // Pass B (needs dP^T and pass A): ds = p * (dp - Dr) on the same 16 columns,
 // with p read back as the bf16 pairs pass A stored (the same p the dV product
 // uses), stored as bf16 pairs over the first 8 of these columns of tP.
-__device__ __forceinline__ void pass_ds(int c, uint32_t tS, uint32_t tP, const float* dd) {
+template <bool kPerColumn>
+__device__ __forceinline__ void pass_ds(int c, uint32_t tS, uint32_t tP, const float* dd,
+                                        float d_row) {
   uint32_t g[16], pk[8];
   tmem_ld16(tP + c, g);
   tmem_ld8(tS + c, pk);
   float dcol[16];
 #pragma unroll
   for (int e = 0; e < 16; e += 4) {
-    const float4 y = *reinterpret_cast<const float4*>(dd + c + e);
-    dcol[e] = y.x, dcol[e + 1] = y.y, dcol[e + 2] = y.z, dcol[e + 3] = y.w;
+    if (kPerColumn) {
+      const float4 y = *reinterpret_cast<const float4*>(dd + c + e);
+      dcol[e] = y.x, dcol[e + 1] = y.y, dcol[e + 2] = y.z, dcol[e + 3] = y.w;
+    } else {
+      dcol[e] = dcol[e + 1] = dcol[e + 2] = dcol[e + 3] = d_row;
+    }
   }
   tmem_ld_wait();
   reg_fence(g, 16);
@@ -572,7 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // pass A: p, feeding dV (warpgroup wg takes k-step 2h + wg of part h)
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
-        pass_p<kCausal>(16 * (2 * h + wg), tS + lane_off, a.scale_log2, rows, lo, kBN);
+        pass_p<true, kCausal>(16 * (2 * h + wg), tS + lane_off, a.scale_log2, rows, 0.f, lo,
+                              kBN);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(pa(h));
@@ -585,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
-        pass_ds(16 * (2 * h + wg), tS + lane_off, tP + lane_off, rows + kBM);
+        pass_ds<true>(16 * (2 * h + wg), tS + lane_off, tP + lane_off, rows + kBM, 0.f);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(pb(h));
@@ -619,18 +632,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 struct DqLayout {
   using T = Tiles<D>;
+  static constexpr int kKStages = 3;  // K is read by S (one tile ahead) and by dQ
+  static constexpr int kVStages = 2;  // V only by dP
   static constexpr int kQ = 0;
   static constexpr int kDO = T::kTileBytes;
-  static constexpr int kStage0 = 2 * T::kTileBytes;
-  static constexpr int kStageBytes = 2 * T::kTileBytes;  // K tile, V tile
-  static constexpr int kBar = kStage0 + kStages * kStageBytes;
-  // q_full, stage_full[S], stage_empty[S], sp_full, p_full[2], o_full, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 3 + kParts;
+  static constexpr int kK0 = 2 * T::kTileBytes;
+  static constexpr int kV0 = kK0 + kKStages * T::kTileBytes;
+  static constexpr int kBar = kV0 + kVStages * T::kTileBytes;
+  // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], dp_full,
+  // pb[kParts], o_full, drain
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 3 + kParts + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kSmem = kMisc + 16 + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
+// dQ: one query tile per CTA.  TMEM: S in two buffers [0,128) and [128,256),
+// dP [256,384), dQ [384, 384+D).  In pipe order, per key tile it: dQ(it) over
+// the parts of pass B as they land, dP(it+1), then S(it+2) into the buffer
+// S(it) used.  Pass A (p from S) of a tile runs while the tensor cores work
+// on the previous tile's dQ and on its own dP; pass B (dS) while they work on
+// the next S.
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ BackwardArgs a, const __grid_constant__ CUtensorMap tq,
@@ -643,12 +665,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bar0 = base + L::kBar;
-  auto q_full = [&]() { return bar0; };
-  auto st_full = [&](int s) { return bar0 + 8 * (1 + s); };
-  auto st_empty = [&](int s) { return bar0 + 8 * (1 + kStages + s); };
-  const uint32_t sp_full = bar0 + 8 * (1 + 2 * kStages);
-  auto p_full = [&](int h) { return sp_full + 8 * (1 + h); };  // part h of the tile done
-  const uint32_t o_full = sp_full + 8 * (1 + kParts);
+  const uint32_t q_full = bar0;
+  auto k_full = [&](int s) { return bar0 + 8 * (1 + s); };
+  auto k_empty = [&](int s) { return bar0 + 8 * (1 + L::kKStages + s); };
+  auto v_full = [&](int s) { return bar0 + 8 * (1 + 2 * L::kKStages + s); };
+  auto v_empty = [&](int s) { return bar0 + 8 * (1 + 2 * L::kKStages + L::kVStages + s); };
+  const uint32_t bar_s = bar0 + 8 * (1 + 2 * L::kKStages + 2 * L::kVStages);
+  auto s_full = [&](int b) { return bar_s + 8 * b; };  // S of the tile in buffer b done
+  const uint32_t dp_full = bar_s + 16;
+  auto pb = [&](int h) { return dp_full + 8 * (1 + h); };  // pass B, part h done
+  const uint32_t o_full = dp_full + 8 * (1 + kParts);
   const uint32_t drain = o_full + 8;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + L::kMisc);
   const Abort ab{tmem_holder + 1, a.status};
@@ -684,13 +710,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_iter = walk.total();
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full(), 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(st_full(s), 1);
-      mbar_init(st_empty(s), 1);
+    mbar_init(q_full, 1);
+    for (int s = 0; s < L::kKStages; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
     }
-    mbar_init(sp_full, 1);
-    for (int h = 0; h < kParts; ++h) mbar_init(p_full(h), kPartThreads);
+    for (int s = 0; s < L::kVStages; ++s) {
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
+    }
+    mbar_init(s_full(0), 1);
+    mbar_init(s_full(1), 1);
+    mbar_init(dp_full, 1);
+    for (int h = 0; h < kParts; ++h) mbar_init(pb(h), kPartThreads);
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
     *ab.flag = 0u;
@@ -704,61 +736,95 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tS = tmem, tP = tmem + 128, tdQ = tmem + 256;
+  const uint32_t tP = tmem + 256, tdQ = tmem + 384;
+  auto tS = [&](int it) { return tmem + static_cast<uint32_t>((it & 1) * 128); };
 
   if (warp == kLoadWarp) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full(), 2 * T::kTileBytes);
+      mbar_arrive_expect_tx(q_full, 2 * T::kTileBytes);
       load_tile<D>(base + L::kQ, &tq, striped, slice * a.N + walk.pos(i, qlr0), i,
-                   slice * c + qlr0, q_full());
+                   slice * c + qlr0, q_full);
       load_tile<D>(base + L::kDO, &tdo, striped, slice * a.N + walk.pos(i, qlr0), i,
-                   slice * c + qlr0, q_full());
-      uint32_t issued = 0, last_parity = 0;
+                   slice * c + qlr0, q_full);
+      // per ring, the stages with a load in flight and their last parity
+      uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
       bool ok = true;
       Walk w = walk;
       w.start();
       for (int it = 0; it < n_iter && ok; ++it, w.next()) {
-        const int s = it % kStages;
-        const uint32_t ph = static_cast<uint32_t>((it / kStages) & 1);
-        if (!wait1(st_empty(s), ph ^ 1u, ab)) {
-          ok = false;
-          break;
-        }
-        const uint32_t sb = base + L::kStage0 + s * L::kStageBytes;
         const int jb = w.block(w.t);
         const int64_t row = slice * a.N + w.key_first();
         const int64_t lrow = slice * c + static_cast<int64_t>(w.kt) * kBN;
-        mbar_arrive_expect_tx(st_full(s), 2 * T::kTileBytes);
-        load_tile<D>(sb, &tk, striped, row, jb, lrow, st_full(s));
-        load_tile<D>(sb + T::kTileBytes, &tv, striped, row, jb, lrow, st_full(s));
-        issued |= 1u << s;
-        last_parity = (last_parity & ~(1u << s)) | (ph << s);
+        const int ks = it % L::kKStages;
+        const uint32_t kph = static_cast<uint32_t>((it / L::kKStages) & 1);
+        if (!wait1(k_empty(ks), kph ^ 1u, ab)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(k_full(ks), T::kTileBytes);
+        load_tile<D>(base + L::kK0 + ks * T::kTileBytes, &tk, striped, row, jb, lrow, k_full(ks));
+        k_issued |= 1u << ks;
+        k_par = (k_par & ~(1u << ks)) | (kph << ks);
+        const int vs = it % L::kVStages;
+        const uint32_t vph = static_cast<uint32_t>((it / L::kVStages) & 1);
+        if (!wait1(v_empty(vs), vph ^ 1u, ab)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(v_full(vs), T::kTileBytes);
+        load_tile<D>(base + L::kV0 + vs * T::kTileBytes, &tv, striped, row, jb, lrow, v_full(vs));
+        v_issued |= 1u << vs;
+        v_par = (v_par & ~(1u << vs)) | (vph << vs);
       }
       if (!ok) {
-        wait_drain(q_full(), 0);
-        for (int s = 0; s < kStages; ++s)
-          if (issued & (1u << s)) wait_drain(st_full(s), (last_parity >> s) & 1u);
+        wait_drain(q_full, 0);
+        for (int s = 0; s < L::kKStages; ++s)
+          if (k_issued & (1u << s)) wait_drain(k_full(s), (k_par >> s) & 1u);
+        for (int s = 0; s < L::kVStages; ++s)
+          if (v_issued & (1u << s)) wait_drain(v_full(s), (v_par >> s) & 1u);
       }
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       const uint64_t dQ = desc_sw128(base + L::kQ, 16, 1024);
       const uint64_t dDO = desc_sw128(base + L::kDO, 16, 1024);
-      bool ok = wait1(q_full(), 0, ab);
-      for (int it = 0; it < n_iter && ok; ++it) {
-        const int s = it % kStages;
-        if (!wait1(st_full(s), static_cast<uint32_t>((it / kStages) & 1), ab)) {
-          ok = false;
-          break;
-        }
+      auto kdesc = [&](int it, uint32_t lbo) {
+        return desc_sw128(base + L::kK0 + (it % L::kKStages) * T::kTileBytes, lbo, 1024);
+      };
+      auto wait_k = [&](int it) {
+        return wait1(k_full(it % L::kKStages),
+                     static_cast<uint32_t>((it / L::kKStages) & 1), ab);
+      };
+      // S(it) = Q K(it)^T into buffer it % 2, then signal it
+      auto issue_s = [&](int it) {
         tc_fence_after();
-        const uint32_t sb = base + L::kStage0 + s * L::kStageBytes;
-        mma_nt<D>(tS, dQ, desc_sw128(sb, 16, 1024));                    // S = Q K^T
-        mma_nt<D>(tP, dDO, desc_sw128(sb + T::kTileBytes, 16, 1024));   // dP = dO V^T
-        mma_commit(sp_full);
-        const uint64_t dKs = desc_sw128(sb, T::kBoxBytes, 1024);
+        mma_nt<D>(tS(it), dQ, kdesc(it, 16));
+        mma_commit(s_full(it & 1));
+      };
+      // dP(it) = dO V(it)^T, then signal it and free V(it)
+      auto issue_dp = [&](int it) {
+        const int vs = it % L::kVStages;
+        if (!wait1(v_full(vs), static_cast<uint32_t>((it / L::kVStages) & 1), ab)) return false;
+        tc_fence_after();
+        mma_nt<D>(tP, dDO, desc_sw128(base + L::kV0 + vs * T::kTileBytes, 16, 1024));
+        mma_commit(dp_full);
+        mma_commit(v_empty(vs));
+        return true;
+      };
+      bool ok = wait1(q_full, 0, ab);
+      if (ok && n_iter > 0) {
+        ok = wait_k(0);
+        if (ok) issue_s(0);
+        if (ok) ok = issue_dp(0);
+        if (ok && n_iter > 1) {
+          ok = wait_k(1);
+          if (ok) issue_s(1);
+        }
+      }
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const uint64_t dKs = kdesc(it, T::kBoxBytes);
         for (int h = 0; h < kParts && ok; ++h) {
-          if (!wait1(p_full(h), static_cast<uint32_t>(it & 1), ab)) {
+          if (!wait1(pb(h), static_cast<uint32_t>(it & 1), ab)) {
             ok = false;
             break;
           }
@@ -766,7 +832,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_tn_part<D>(tdQ, tP, dKs, h, (it > 0 || h > 0) ? 1u : 0u);  // dQ += dS K, part h
         }
         if (!ok) break;
-        mma_commit(st_empty(s));
+        mma_commit(k_empty(it % L::kKStages));
+        // dP(it+1) overwrites dS(it) (read by the dQ products above, earlier
+        // in the pipe) and dP(it) (read by pass B, complete); S(it+2) goes to
+        // the buffer of S(it), whose p pass B has read too.
+        if (it + 1 < n_iter && !issue_dp(it + 1)) {
+          ok = false;
+          break;
+        }
+        if (it + 2 < n_iter) {
+          if (!wait_k(it + 2)) {
+            ok = false;
+            break;
+          }
+          issue_s(it + 2);
+        }
       }
       if (ok) {
         mma_commit(o_full);
@@ -791,7 +871,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       if (kCausal && it > 0) w.next();
-      if (!wait_warp(sp_full, static_cast<uint32_t>(it & 1), ab)) {
+      // pass A: p into the S buffer of this tile
+      if (!wait_warp(s_full(it & 1), static_cast<uint32_t>((it >> 1) & 1), ab)) {
         ok = false;
         break;
       }
@@ -803,14 +884,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t n = qref - first + 1;
         hi = n < 0 ? 0 : (n > kBN ? kBN : static_cast<int>(n));
       }
+      const uint32_t tSt = tS(it) + lane_off;
+#pragma unroll
+      for (int h = 0; h < kParts; ++h)
+        pass_p<false, kCausal>(16 * (2 * h + wg), tSt, a.scale_log2, nullptr, nl_row, 0, hi);
+      tmem_st_wait();  // pass B reads these p back
+      // pass B: dS into dP's columns, feeding dQ
+      if (!wait_warp(dp_full, static_cast<uint32_t>(it & 1), ab)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
-        elementwise_part<false, false, kCausal>(h, wg, tS + lane_off, tP + lane_off,
-                                                a.scale_log2, nullptr, nullptr, nl_row, d_row, 0,
-                                                hi);
+        pass_ds<false>(16 * (2 * h + wg), tSt, tP + lane_off, nullptr, d_row);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full(h));
+        mbar_arrive(pb(h));
       }
     }
     if (ok && wait_warp(o_full, 0, ab)) {
