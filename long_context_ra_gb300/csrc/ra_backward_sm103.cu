@@ -23,9 +23,11 @@
 // The row terms come precomputed per query row: D and nl = -lse * log2(e)
 // (so that p = exp2(s * tau * log2(e) + nl)).
 //
-// Warp roles (320 threads): warps 0-7 elementwise, two warpgroups (thread =
-// tile row = TMEM lane), warp 8 TMA producer, warp 9 TMEM allocator and MMA
-// issuer.  Every wait is bounded (see sm103_pipeline.cuh).
+// Warp roles (G elementwise warpgroups; 128 G + 64 threads): warps 0 .. 4G-1
+// elementwise (thread = tile row = TMEM lane), warp 4G TMA producer, warp
+// 4G+1 TMEM allocator and MMA issuer.  G = 4 where the kernel's registers
+// allow it (the plain kernels), else 2 (the causal ones, whose walk state
+// needs more).  Every wait is bounded (see sm103_pipeline.cuh).
 
 #include <cmath>
 
@@ -39,17 +41,23 @@ namespace {
 using namespace ptx;
 using namespace sm103;
 
-constexpr int kThreads = 320;
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+template <int G>
+struct Roles {
+  static constexpr int kThreads = 128 * G + 64;
+  static constexpr int kLoadWarp = 4 * G;
+  static constexpr int kMmaWarp = 4 * G + 1;
+  static constexpr int kParts = 8 / G;          // parts of a tile's 128 columns
+  static constexpr int kPartThreads = 128 * G;  // arrivals per part: every warpgroup
+};
+template <bool kCausal>
+constexpr int groups_for() { return kCausal ? 2 : 4; }
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStages = 2;
-// The elementwise pass over a tile's 128 columns is done in kParts parts of
-// 32 columns, which are k-steps 2h and 2h + 1 of the TMEM-operand products;
-// warpgroup g takes k-step 2h + g, so both warpgroups work on every part.
+// The elementwise pass over a tile's 128 columns is done in 8/G parts of 16G
+// columns, which are k-steps [G h, G h + G) of the TMEM-operand products;
+// warpgroup g takes k-step G h + g, so every warpgroup works on every part.
 // The products that read part h start as soon as part h is done.
-constexpr int kParts = 4;
-constexpr int kPartThreads = 256;  // arrivals per part: both warpgroups
+constexpr int kMaxParts = 4;
 
 // 8 consecutive 32-bit columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
@@ -330,15 +338,16 @@ __device__ __forceinline__ void elementwise_part(int h, int g, uint32_t tS, uint
                                           lo, hi);
 }
 
-// The products over part h: k-steps [2h, 2h + 2) (16 rows of B each).
-template <int D>
+// The products over part h: k-steps [G h, G h + G) (16 rows of B each).
+template <int D, int G>
 __device__ __forceinline__ void mma_tn_part(uint32_t d_tmem, uint32_t a_tmem, uint64_t db, int h,
                                             uint32_t accumulate) {
-  switch (h) {
-    case 0: mma_tn<D, 0, 2>(d_tmem, a_tmem, db, accumulate); break;
-    case 1: mma_tn<D, 2, 4>(d_tmem, a_tmem, db, accumulate); break;
-    case 2: mma_tn<D, 4, 6>(d_tmem, a_tmem, db, accumulate); break;
-    default: mma_tn<D, 6, 8>(d_tmem, a_tmem, db, accumulate); break;
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, true);
+#pragma unroll
+  for (int e = 0; e < G; ++e) {
+    const int kk = G * h + e;
+    mma_bf16_ts(d_tmem, a_tmem + kk * 16, db + desc_step(kk * 16 * 128), idesc,
+                e == 0 ? accumulate : 1u);
   }
 }
 
@@ -372,21 +381,25 @@ struct DkvLayout {
   // stage: Q tile, dO tile, nl[128], D[128]
   static constexpr int kStageBytes = 2 * T::kTileBytes + 2 * T::kRowBytes;
   static constexpr int kBar = kStage0 + kStages * kStageBytes;
-  // kv_full, stage_full[S], stage_empty[S], s_full, dp_full, pa[kParts],
-  // pb[kParts], o_full, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2 * kParts;
+  // kv_full, stage_full[S], stage_empty[S], s_full, dp_full, pa[kMaxParts],
+  // pb[kMaxParts], o_full, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2 * kMaxParts;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kSmem = kMisc + 16 + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-template <int D, bool kCausal>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool kCausal, int G = groups_for<kCausal>()>
+__global__ void __launch_bounds__(Roles<G>::kThreads, 1)
     dkv_kernel(const __grid_constant__ BackwardArgs a, const __grid_constant__ CUtensorMap tq,
                const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                const __grid_constant__ CUtensorMap tdo) {
   using L = DkvLayout<D>;
   using T = Tiles<D>;
+  constexpr int kLoadWarp = Roles<G>::kLoadWarp;
+  constexpr int kMmaWarp = Roles<G>::kMmaWarp;
+  constexpr int kParts = Roles<G>::kParts;
+  constexpr int kPartThreads = Roles<G>::kPartThreads;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -398,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_full = bar0 + 8 * (1 + 2 * kStages);  // S^T of the tile done
   const uint32_t dp_full = s_full + 8;                      // dP^T of the tile done
   auto pa = [&](int h) { return dp_full + 8 * (1 + h); };  // pass A, part h done
-  auto pb = [&](int h) { return dp_full + 8 * (1 + kParts + h); };  // pass B, part h done
-  const uint32_t o_full = dp_full + 8 * (1 + 2 * kParts);
+  auto pb = [&](int h) { return dp_full + 8 * (1 + kMaxParts + h); };  // pass B, part h done
+  const uint32_t o_full = dp_full + 8 * (1 + 2 * kMaxParts);
   const uint32_t drain = o_full + 8;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + L::kMisc);
   const Abort ab{tmem_holder + 1, a.status};
@@ -522,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          mma_tn_part<D>(tdV, tS, dDOs, h, h == 0 ? acc : 1u);  // dV += P^T dO, part h
+          mma_tn_part<D, G>(tdV, tS, dDOs, h, h == 0 ? acc : 1u);  // dV += P^T dO, part h
         }
         for (int h = 0; h < kParts && ok; ++h) {
           if (!wait1(pb(h), par, ab)) {
@@ -530,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          mma_tn_part<D>(tdK, tP, dQs, h, h == 0 ? acc : 1u);  // dK += dS^T Q, part h
+          mma_tn_part<D, G>(tdK, tP, dQs, h, h == 0 ? acc : 1u);  // dK += dS^T Q, part h
         }
         if (!ok) break;
         mma_commit(st_empty(s));
@@ -552,8 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_drain(drain, 0);
       }
     }
-  } else if (warp < 8) {
-    const int wg = warp / 4;  // warpgroup: k-step 2h + wg of every part h
+  } else if (warp < 4 * G) {
+    const int wg = warp / 4;  // warpgroup: k-step G h + wg of every part h
     const int row = (warp % 4) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
     // this thread's key: position (striped: local row) for the mask
@@ -584,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // pass A: p, feeding dV (warpgroup wg takes k-step 2h + wg of part h)
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
-        pass_p<true, kCausal>(16 * (2 * h + wg), tS + lane_off, a.scale_log2, rows, 0.f, lo,
+        pass_p<true, kCausal>(16 * (G * h + wg), tS + lane_off, a.scale_log2, rows, 0.f, lo,
                               kBN);
         tmem_st_wait();
         tc_fence_before();
@@ -598,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
-        pass_ds<true>(16 * (2 * h + wg), tS + lane_off, tP + lane_off, rows + kBM, 0.f);
+        pass_ds<true>(16 * (G * h + wg), tS + lane_off, tP + lane_off, rows + kBM, 0.f);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(pb(h));
@@ -610,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint16_t* dv = static_cast<uint16_t*>(a.dv) + r * D;
       uint16_t* dk = static_cast<uint16_t*>(a.dk) + r * D;
 #pragma unroll
-      for (int cc = wg * (D / 2); cc < (wg + 1) * (D / 2); cc += 32) {
+      for (int cc = 32 * wg; cc < D; cc += 32 * G) {
         store_row_bf16(tdV + lane_off + cc, dv + cc, 1.f);
         store_row_bf16(tdK + lane_off + cc, dk + cc, a.tau);
       }
@@ -640,8 +653,8 @@ struct DqLayout {
   static constexpr int kV0 = kK0 + kKStages * T::kTileBytes;
   static constexpr int kBar = kV0 + kVStages * T::kTileBytes;
   // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], dp_full,
-  // pb[kParts], o_full, drain
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 3 + kParts + 2;
+  // pb[kMaxParts], o_full, drain
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 3 + kMaxParts + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kSmem = kMisc + 16 + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -653,13 +666,17 @@ struct DqLayout {
 // S(it) used.  Pass A (p from S) of a tile runs while the tensor cores work
 // on the previous tile's dQ and on its own dP; pass B (dS) while they work on
 // the next S.
-template <int D, bool kCausal>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool kCausal, int G = groups_for<kCausal>()>
+__global__ void __launch_bounds__(Roles<G>::kThreads, 1)
     dq_kernel(const __grid_constant__ BackwardArgs a, const __grid_constant__ CUtensorMap tq,
               const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
               const __grid_constant__ CUtensorMap tdo) {
   using L = DqLayout<D>;
   using T = Tiles<D>;
+  constexpr int kLoadWarp = Roles<G>::kLoadWarp;
+  constexpr int kMmaWarp = Roles<G>::kMmaWarp;
+  constexpr int kParts = Roles<G>::kParts;
+  constexpr int kPartThreads = Roles<G>::kPartThreads;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -674,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto s_full = [&](int b) { return bar_s + 8 * b; };  // S of the tile in buffer b done
   const uint32_t dp_full = bar_s + 16;
   auto pb = [&](int h) { return dp_full + 8 * (1 + h); };  // pass B, part h done
-  const uint32_t o_full = dp_full + 8 * (1 + kParts);
+  const uint32_t o_full = dp_full + 8 * (1 + kMaxParts);
   const uint32_t drain = o_full + 8;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + L::kMisc);
   const Abort ab{tmem_holder + 1, a.status};
@@ -829,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          mma_tn_part<D>(tdQ, tP, dKs, h, (it > 0 || h > 0) ? 1u : 0u);  // dQ += dS K, part h
+          mma_tn_part<D, G>(tdQ, tP, dKs, h, (it > 0 || h > 0) ? 1u : 0u);  // dQ += dS K, part h
         }
         if (!ok) break;
         mma_commit(k_empty(it % L::kKStages));
@@ -855,8 +872,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_drain(drain, 0);
       }
     }
-  } else if (warp < 8) {
-    const int wg = warp / 4;  // warpgroup: k-step 2h + wg of every part h
+  } else if (warp < 4 * G) {
+    const int wg = warp / 4;  // warpgroup: k-step G h + wg of every part h
     const int row = (warp % 4) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const int64_t lrow = qlr0 + row;
@@ -887,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tSt = tS(it) + lane_off;
 #pragma unroll
       for (int h = 0; h < kParts; ++h)
-        pass_p<false, kCausal>(16 * (2 * h + wg), tSt, a.scale_log2, nullptr, nl_row, 0, hi);
+        pass_p<false, kCausal>(16 * (G * h + wg), tSt, a.scale_log2, nullptr, nl_row, 0, hi);
       tmem_st_wait();  // pass B reads these p back
       // pass B: dS into dP's columns, feeding dQ
       if (!wait_warp(dp_full, static_cast<uint32_t>(it & 1), ab)) {
@@ -897,7 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
-        pass_ds<false>(16 * (2 * h + wg), tSt, tP + lane_off, nullptr, d_row);
+        pass_ds<false>(16 * (G * h + wg), tSt, tP + lane_off, nullptr, d_row);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(pb(h));
@@ -907,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint16_t* dq = static_cast<uint16_t*>(a.dq) + r * D;
 #pragma unroll
-      for (int cc = wg * (D / 2); cc < (wg + 1) * (D / 2); cc += 32)
+      for (int cc = 32 * wg; cc < D; cc += 32 * G)
         store_row_bf16(tdQ + lane_off + cc, dq + cc, a.tau);
     }
   }
@@ -938,6 +955,7 @@ cudaError_t launch_d(const BackwardArgs& a, const CUtensorMap& tq, const CUtenso
     configured_device = dev;
   }
   const unsigned grid = static_cast<unsigned>(a.slices * (a.N / kBM));
+  constexpr int kThreads = Roles<groups_for<kCausal>()>::kThreads;
   dkv_kernel<D, kCausal><<<grid, kThreads, DkvLayout<D>::kSmem, s>>>(a, tq, tk, tv, tdo);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
