@@ -6,20 +6,25 @@
 //   P = exp(tau Q K^T - lse)   (recomputed from the forward's lse)
 //   dP = dO V^T;  dS = P * (dP - D),  D = rowsum(dO * out)
 //   dV = P^T dO;  dK = tau dS^T Q;  dQ = tau dS K
-// Two kernels, no atomics:
+// Two kernels, no atomics.  In both, the elementwise work runs in two
+// passes: pass A makes p (needs S), pass B makes dS from the bf16 p (needs
+// dP), and each overlaps a product on the tensor cores.
 //   dkv_kernel  one 128-key tile of block j per CTA; at ring step t the block
 //               is on device i = (j + t) mod P, so the CTA walks the query
 //               tiles of those blocks.  TMEM: S^T [0,128), dP^T [128,256),
-//               dV [256, 256+D), dK [256+D, 256+2D).  Per query tile:
-//               S^T = K Q^T and dP^T = V dO^T (SS MMAs), the elementwise
-//               warps turn them into P^T and dS^T (bf16; the 16 values of
-//               each k-step packed over the first 8 of their own 16 columns
-//               of S^T and dP^T), then dV += P^T dO and dK += dS^T Q (A
-//               operand from TMEM).
+//               dV [256, 256+D), dK [256+D, 256+2D).  Pipe order per query
+//               tile: dP^T = V dO^T (pass A runs meanwhile), dV += P^T dO
+//               over pass A's parts (pass B runs meanwhile), dK += dS^T Q
+//               over pass B's parts, then the next S^T = K Q^T.  P^T and
+//               dS^T are bf16, the 16 values of each k-step packed over the
+//               first 8 of their own 16 columns of S^T and dP^T (the A
+//               operands of the dV and dK products).
 //   dq_kernel   one 128-query tile per CTA walking the key tiles in the
-//               forward's ring order (i - t) mod P.  TMEM: S [0,128),
-//               dP [128,256), dQ [256, 256+D).  S = Q K^T, dP = dO V^T,
-//               dS -> TMEM, dQ += dS K.
+//               forward's ring order (i - t) mod P.  TMEM: S in two buffers
+//               [0,128) and [128,256), dP [256,384), dQ [384, 384+D).  S is
+//               computed a tile ahead; pipe order per key tile: dQ += dS K
+//               over pass B's parts, the next dP = dO V^T, then S = Q K^T two
+//               tiles ahead.  K and V stream through separate rings.
 // The row terms come precomputed per query row: D and nl = -lse * log2(e)
 // (so that p = exp2(s * tau * log2(e) + nl)).
 //
@@ -119,63 +124,6 @@ __device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint64_
   for (int kk = k0; kk < k1; ++kk)
     mma_bf16_ts(d_tmem, a_tmem + kk * 16, db + desc_step(kk * 16 * 128), idesc,
                 kk == k0 ? accumulate : 1u);
-}
-
-// Elementwise step on one tile row (this thread's TMEM lane): from the 128
-// scores s (TMEM columns of tS) and dp (columns of tP) make
-//   p = exp2(s * sl2 + nl),  ds = p * (dp - Dr)
-// where nl and Dr are per column (dkv kernel: per query, from SMEM) or per
-// row (dq kernel: scalars).  With kMask, columns outside [lo, hi) are masked
-// (their score is -inf, so p = ds = 0).  p (if kWriteP) and ds are rounded
-// to bf16 pairs and written over the first 8 of these 16 columns of tS and
-// tP (columns this warp has just read).  One call covers the 16 columns
-// [c, c + 16), one k-step of the products that read them.
-template <bool kPerColumn, bool kWriteP, bool kMask>
-__device__ __forceinline__ void elementwise(int c, uint32_t tS, uint32_t tP, float sl2,
-                                            const float* nl, const float* dd, float nl_row,
-                                            float d_row, int lo, int hi) {
-  {
-    uint32_t s[16], g[16];
-    tmem_ld16(tS + c, s);
-    tmem_ld16(tP + c, g);
-    tmem_ld_wait();
-    reg_fence(s, 16);
-    reg_fence(g, 16);
-    if (kMask) {
-#pragma unroll
-      for (int e = 0; e < 16; ++e)
-        if (c + e < lo || c + e >= hi) s[e] = 0xff800000u;  // -inf
-    }
-    float ncol[kPerColumn ? 16 : 1], dcol[kPerColumn ? 16 : 1];
-    if (kPerColumn) {
-#pragma unroll
-      for (int e = 0; e < 16; e += 4) {
-        const float4 x = *reinterpret_cast<const float4*>(nl + c + e);
-        const float4 y = *reinterpret_cast<const float4*>(dd + c + e);
-        ncol[e] = x.x, ncol[e + 1] = x.y, ncol[e + 2] = x.z, ncol[e + 3] = x.w;
-        dcol[e] = y.x, dcol[e + 1] = y.y, dcol[e + 2] = y.z, dcol[e + 3] = y.w;
-      }
-    }
-    uint32_t pk[8], dk[8];
-#pragma unroll
-    for (int e = 0; e < 16; e += 2) {
-      float n0 = nl_row, n1 = nl_row, d0 = d_row, d1 = d_row;
-      if (kPerColumn) {
-        n0 = ncol[e];
-        n1 = ncol[e + 1];
-        d0 = dcol[e];
-        d1 = dcol[e + 1];
-      }
-      const float p0 = ex2(fmaf(__uint_as_float(s[e]), sl2, n0));
-      const float p1 = ex2(fmaf(__uint_as_float(s[e + 1]), sl2, n1));
-      const float ds0 = p0 * (__uint_as_float(g[e]) - d0);
-      const float ds1 = p1 * (__uint_as_float(g[e + 1]) - d1);
-      pk[e / 2] = pack_bf16x2(p0, p1);
-      dk[e / 2] = pack_bf16x2(ds0, ds1);
-    }
-    if (kWriteP) tmem_st8(tS + c, pk);
-    tmem_st8(tP + c, dk);
-  }
 }
 
 // 8 consecutive 32-bit columns of this thread's TMEM lane.
@@ -328,15 +276,6 @@ struct KWalk {
     skip();
   }
 };
-
-// Warpgroup g's share of part h: the 16 columns of k-step 2h + g.
-template <bool kPerColumn, bool kWriteP, bool kMask>
-__device__ __forceinline__ void elementwise_part(int h, int g, uint32_t tS, uint32_t tP,
-                                                 float sl2, const float* nl, const float* dd,
-                                                 float nl_row, float d_row, int lo, int hi) {
-  elementwise<kPerColumn, kWriteP, kMask>(16 * (2 * h + g), tS, tP, sl2, nl, dd, nl_row, d_row,
-                                          lo, hi);
-}
 
 // The products over part h: k-steps [G h, G h + G) (16 rows of B each).
 template <int D, int G>
