@@ -51,17 +51,20 @@ struct Roles {
   static constexpr int kThreads = 128 * G + 64;
   static constexpr int kLoadWarp = 4 * G;
   static constexpr int kMmaWarp = 4 * G + 1;
-  static constexpr int kParts = 8 / G;          // parts of a tile's 128 columns
+  static constexpr int kParts = 2;               // parts of a tile's 128 columns
+  static constexpr int kStepsPerPart = 8 / kParts;
+  static constexpr int kStepsPerGroup = kStepsPerPart / G;  // k-steps of one warpgroup per part
   static constexpr int kPartThreads = 128 * G;  // arrivals per part: every warpgroup
 };
 template <bool kCausal>
 constexpr int groups_for() { return kCausal ? 2 : 4; }
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStages = 2;
-// The elementwise pass over a tile's 128 columns is done in 8/G parts of 16G
-// columns, which are k-steps [G h, G h + G) of the TMEM-operand products;
-// warpgroup g takes k-step G h + g, so every warpgroup works on every part.
-// The products that read part h start as soon as part h is done.
+// Each elementwise pass over a tile's 128 columns is done in two parts of 64
+// columns, which are k-steps [4h, 4h + 4) of the TMEM-operand products;
+// warpgroup g takes the k-steps 4h + g + G m, so every warpgroup works on
+// every part.  The products that read part h start as soon as part h is
+// done.  (Two parts measured faster than one, or than one per k-step pair.)
 constexpr int kMaxParts = 4;
 
 // 8 consecutive 32-bit columns of this thread's TMEM lane.
@@ -277,14 +280,15 @@ struct KWalk {
   }
 };
 
-// The products over part h: k-steps [G h, G h + G) (16 rows of B each).
+// The products over part h: k-steps [4h, 4h + 4) (16 rows of B each).
 template <int D, int G>
 __device__ __forceinline__ void mma_tn_part(uint32_t d_tmem, uint32_t a_tmem, uint64_t db, int h,
                                             uint32_t accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, true);
+  constexpr int S = Roles<G>::kStepsPerPart;
 #pragma unroll
-  for (int e = 0; e < G; ++e) {
-    const int kk = G * h + e;
+  for (int e = 0; e < S; ++e) {
+    const int kk = S * h + e;
     mma_bf16_ts(d_tmem, a_tmem + kk * 16, db + desc_step(kk * 16 * 128), idesc,
                 e == 0 ? accumulate : 1u);
   }
@@ -505,7 +509,7 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
       }
     }
   } else if (warp < 4 * G) {
-    const int wg = warp / 4;  // warpgroup: k-step G h + wg of every part h
+    const int wg = warp / 4;  // warpgroup: k-steps 4h + wg + G m of every part h
     const int row = (warp % 4) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
     // this thread's key: position (striped: local row) for the mask
@@ -533,11 +537,13 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
         const int64_t m = kref - qref;
         lo = m < 0 ? 0 : (m > kBN ? kBN : static_cast<int>(m));
       }
-      // pass A: p, feeding dV (warpgroup wg takes k-step 2h + wg of part h)
+      // pass A: p, feeding dV (warpgroup wg takes k-steps 4h + wg + G m of part h)
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
-        pass_p<true, kCausal>(16 * (G * h + wg), tS + lane_off, a.scale_log2, rows, 0.f, lo,
-                              kBN);
+#pragma unroll
+        for (int m = 0; m < Roles<G>::kStepsPerGroup; ++m)
+          pass_p<true, kCausal>(16 * (Roles<G>::kStepsPerPart * h + wg + G * m), tS + lane_off,
+                                a.scale_log2, rows, 0.f, lo, kBN);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(pa(h));
@@ -550,7 +556,10 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
-        pass_ds<true>(16 * (G * h + wg), tS + lane_off, tP + lane_off, rows + kBM, 0.f);
+#pragma unroll
+        for (int m = 0; m < Roles<G>::kStepsPerGroup; ++m)
+          pass_ds<true>(16 * (Roles<G>::kStepsPerPart * h + wg + G * m), tS + lane_off,
+                        tP + lane_off, rows + kBM, 0.f);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(pb(h));
@@ -812,7 +821,7 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
       }
     }
   } else if (warp < 4 * G) {
-    const int wg = warp / 4;  // warpgroup: k-step G h + wg of every part h
+    const int wg = warp / 4;  // warpgroup: k-steps 4h + wg + G m of every part h
     const int row = (warp % 4) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const int64_t lrow = qlr0 + row;
@@ -843,7 +852,10 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
       const uint32_t tSt = tS(it) + lane_off;
 #pragma unroll
       for (int h = 0; h < kParts; ++h)
-        pass_p<false, kCausal>(16 * (G * h + wg), tSt, a.scale_log2, nullptr, nl_row, 0, hi);
+#pragma unroll
+        for (int m = 0; m < Roles<G>::kStepsPerGroup; ++m)
+          pass_p<false, kCausal>(16 * (Roles<G>::kStepsPerPart * h + wg + G * m), tSt,
+                                 a.scale_log2, nullptr, nl_row, 0, hi);
       tmem_st_wait();  // pass B reads these p back
       // pass B: dS into dP's columns, feeding dQ
       if (!wait_warp(dp_full, static_cast<uint32_t>(it & 1), ab)) {
@@ -853,7 +865,10 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
-        pass_ds<false>(16 * (G * h + wg), tSt, tP + lane_off, nullptr, d_row);
+#pragma unroll
+        for (int m = 0; m < Roles<G>::kStepsPerGroup; ++m)
+          pass_ds<false>(16 * (Roles<G>::kStepsPerPart * h + wg + G * m), tSt, tP + lane_off,
+                         nullptr, d_row);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(pb(h));
