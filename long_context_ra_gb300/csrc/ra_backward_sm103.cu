@@ -58,6 +58,7 @@ struct Roles {
 };
 template <bool kCausal>
 constexpr int groups_for() { return kCausal ? 2 : 4; }
+
 constexpr uint32_t kTmemCols = 512;
 constexpr int kStages = 2;
 // Each elementwise pass over a tile's 128 columns is done in two parts of 64
@@ -147,7 +148,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
 // nl_row, and the mask keeps the columns below hi).
 template <bool kPerColumn, bool kMask>
 __device__ __forceinline__ void pass_p(int c, uint32_t tS, float sl2, const float* nl,
-                                       float nl_row, int lo, int hi) {
+                                       float nl_row, int lo, int hi, uint32_t (&pk)[8]) {
   uint32_t s[16];
   tmem_ld16(tS + c, s);
   float ncol[16];
@@ -167,7 +168,6 @@ __device__ __forceinline__ void pass_p(int c, uint32_t tS, float sl2, const floa
     for (int e = 0; e < 16; ++e)
       if (c + e < lo || c + e >= hi) s[e] = 0xff800000u;  // -inf
   }
-  uint32_t pk[8];
   const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
@@ -181,14 +181,15 @@ __device__ __forceinline__ void pass_p(int c, uint32_t tS, float sl2, const floa
 }
 
 // Pass B (needs dP^T and pass A): ds = p * (dp - Dr) on the same 16 columns,
-// with p read back as the bf16 pairs pass A stored (the same p the dV product
-// uses), stored as bf16 pairs over the first 8 of these columns of tP.
-template <bool kPerColumn>
+// with p as the bf16 pairs pass A made (the same p the dV product uses):
+// kept in registers (dK/dV kernel) or read back from tS (dQ kernel); ds is
+// stored as bf16 pairs over the first 8 of these columns of tP.
+template <bool kPerColumn, bool kPFromTmem>
 __device__ __forceinline__ void pass_ds(int c, uint32_t tS, uint32_t tP, const float* dd,
-                                        float d_row) {
-  uint32_t g[16], pk[8];
+                                        float d_row, uint32_t (&pk)[8]) {
+  uint32_t g[16];
   tmem_ld16(tP + c, g);
-  tmem_ld8(tS + c, pk);
+  if (kPFromTmem) tmem_ld8(tS + c, pk);
   float dcol[16];
 #pragma unroll
   for (int e = 0; e < 16; e += 4) {
@@ -201,7 +202,7 @@ __device__ __forceinline__ void pass_ds(int c, uint32_t tS, uint32_t tP, const f
   }
   tmem_ld_wait();
   reg_fence(g, 16);
-  reg_fence(pk, 8);
+  if (kPFromTmem) reg_fence(pk, 8);
   uint32_t dk[8];
   const uint64_t minus1 = pack_f32x2(-1.f, -1.f);
 #pragma unroll
@@ -339,6 +340,11 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
                const __grid_constant__ CUtensorMap tdo) {
   using L = DkvLayout<D>;
   using T = Tiles<D>;
+  // Where the next tile's S^T goes.  Early (between dV and dK; pass B then
+  // keeps p in registers, since S^T overwrites them in tS) measured 3.6 %
+  // faster with two warpgroups and 2.2 % slower with four, so the causal
+  // kernels issue it early and the plain ones after dK.
+  constexpr bool kEarlyS = kCausal;
   constexpr int kLoadWarp = Roles<G>::kLoadWarp;
   constexpr int kMmaWarp = Roles<G>::kMmaWarp;
   constexpr int kParts = Roles<G>::kParts;
@@ -450,10 +456,10 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       // Per tile, in pipe order: dP^T; dV over the parts of pass A as they
-      // land; dK over the parts of pass B; then the next tile's S^T (issued
-      // at the end of the previous iteration).  Pass A runs while dP^T is on
-      // the tensor cores and pass B while dV is.  The next S^T overwrites the
-      // p that pass B reads, so it waits for all of pass B.
+      // land; dK over the parts of pass B; the next tile's S^T either before
+      // dK (kEarlyS) or after it.  Pass A runs while dP^T is on the tensor
+      // cores and pass B while dV is (and, with kEarlyS, the next pass A
+      // while dK is).
       const uint64_t dK = desc_sw128(base + L::kK, 16, 1024);
       const uint64_t dV = desc_sw128(base + L::kV, 16, 1024);
       bool ok = wait1(kv_full(), 0, ab);
@@ -480,6 +486,18 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
           tc_fence_after();
           mma_tn_part<D, G>(tdV, tS, dDOs, h, h == 0 ? acc : 1u);  // dV += P^T dO, part h
         }
+        // the next tile's S^T, early: it overwrites the p in tS, which the dV
+        // products before it have read and pass B holds in registers
+        if (kEarlyS && ok && it + 1 < n_iter) {
+          const int s1 = (it + 1) % kStages;
+          if (!wait1(st_full(s1), static_cast<uint32_t>(((it + 1) / kStages) & 1), ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_nt<D>(tS, dK, desc_sw128(base + L::kStage0 + s1 * L::kStageBytes, 16, 1024));
+          mma_commit(s_full);
+        }
         for (int h = 0; h < kParts && ok; ++h) {
           if (!wait1(pb(h), par, ab)) {
             ok = false;
@@ -490,7 +508,8 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
         }
         if (!ok) break;
         mma_commit(st_empty(s));
-        if (it + 1 < n_iter) {
+        // the next tile's S^T, late: after pass B has read the p in tS
+        if (!kEarlyS && it + 1 < n_iter) {
           const int s1 = (it + 1) % kStages;
           if (!wait1(st_full(s1), static_cast<uint32_t>(((it + 1) / kStages) & 1), ab)) {
             ok = false;
@@ -537,13 +556,17 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
         const int64_t m = kref - qref;
         lo = m < 0 ? 0 : (m > kBN ? kBN : static_cast<int>(m));
       }
-      // pass A: p, feeding dV (warpgroup wg takes k-steps 4h + wg + G m of part h)
+      // pass A: p, feeding dV (warpgroup wg takes k-steps 4h + wg + G m of part h);
+      // with the early next S^T, this thread's p stay in registers for pass B
+      // (S^T overwrites them in tS as soon as the dV products have read it);
+      // otherwise pass B reads them back from tS
+      uint32_t pkeep[kParts][Roles<G>::kStepsPerGroup][8];
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
 #pragma unroll
         for (int m = 0; m < Roles<G>::kStepsPerGroup; ++m)
           pass_p<true, kCausal>(16 * (Roles<G>::kStepsPerPart * h + wg + G * m), tS + lane_off,
-                                a.scale_log2, rows, 0.f, lo, kBN);
+                                a.scale_log2, rows, 0.f, lo, kBN, pkeep[h][m]);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(pa(h));
@@ -558,8 +581,9 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
       for (int h = 0; h < kParts; ++h) {
 #pragma unroll
         for (int m = 0; m < Roles<G>::kStepsPerGroup; ++m)
-          pass_ds<true>(16 * (Roles<G>::kStepsPerPart * h + wg + G * m), tS + lane_off,
-                        tP + lane_off, rows + kBM, 0.f);
+          pass_ds<true, !kEarlyS>(16 * (Roles<G>::kStepsPerPart * h + wg + G * m),
+                                                  tS + lane_off, tP + lane_off, rows + kBM, 0.f,
+                                                  pkeep[h][m]);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(pb(h));
@@ -853,9 +877,11 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
 #pragma unroll
       for (int h = 0; h < kParts; ++h)
 #pragma unroll
-        for (int m = 0; m < Roles<G>::kStepsPerGroup; ++m)
+        for (int m = 0; m < Roles<G>::kStepsPerGroup; ++m) {
+          uint32_t pk[8];
           pass_p<false, kCausal>(16 * (Roles<G>::kStepsPerPart * h + wg + G * m), tSt,
-                                 a.scale_log2, nullptr, nl_row, 0, hi);
+                                 a.scale_log2, nullptr, nl_row, 0, hi, pk);
+        }
       tmem_st_wait();  // pass B reads these p back
       // pass B: dS into dP's columns, feeding dQ
       if (!wait_warp(dp_full, static_cast<uint32_t>(it & 1), ab)) {
@@ -866,9 +892,11 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
 #pragma unroll
-        for (int m = 0; m < Roles<G>::kStepsPerGroup; ++m)
-          pass_ds<false>(16 * (Roles<G>::kStepsPerPart * h + wg + G * m), tSt, tP + lane_off,
-                         nullptr, d_row);
+        for (int m = 0; m < Roles<G>::kStepsPerGroup; ++m) {
+          uint32_t pk[8];
+          pass_ds<false, true>(16 * (Roles<G>::kStepsPerPart * h + wg + G * m), tSt,
+                               tP + lane_off, nullptr, d_row, pk);
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(pb(h));
