@@ -99,6 +99,27 @@ def test_bf16_backward_workload4_sampled(O):
     assert ra.ra_last_device_status() == 0
 
 
+def test_bf16_backward_workload5_sampled(O):
+    """The largest workload (N = 1048576, P = 64): gradients of sampled rows."""
+    w = synth.WORKLOADS[5]
+    q, k, v = synth.make_inputs(w, DEV)
+    out, lse = ra.ra_forward(q, k, v, w.P)
+    dout = rnd(q.shape, 4545, torch.bfloat16)
+    dq, dk, dv = ra.ra_backward(q, k, v, out, dout, lse, w.P)
+    torch.cuda.synchronize()
+    assert ra.ra_last_device_status() == 0
+    rows = synth.sample_rows(w, 64, seed=8).numpy()
+    idx = torch.as_tensor(rows, device=DEV)
+    got = [t.reshape(-1, w.d).index_select(0, idx) for t in (dq, dk, dv)]
+    del dq, dk, dv
+    bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).cpu().view(torch.int16).numpy().view(np.uint16)
+    wq, wk, wv = O.backward_rows(bits(q), bits(k), bits(v), bits(out), bits(dout),
+                                 lse.double().cpu().numpy(), rows, rows, dtype="bf16")
+    for name, g, want in zip(("dq", "dk", "dv"), got, (wq, wk, wv)):
+        assert torch.isfinite(g.float()).all()
+        close(g, want, TOL[torch.bfloat16], name)
+
+
 LAYOUTS = ["contiguous", "zigzag", "striped"]
 
 
