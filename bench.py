@@ -132,6 +132,49 @@ def causal_flops(w) -> float:
     return 4.0 * w.B * w.H * w.d * w.N * (w.N + 1) / 2.0
 
 
+def l2_note(w) -> str:
+    """How the timed steps avoid an L2-resident working set (both arms)."""
+    esize = 2 if "bf16" in w.name else 4
+    return f"inputs larger than L2 (q+k+v = {3 * w.rows * w.d * esize / 2**20:.0f} MiB)"
+
+
+def host_pipeline_stages(host_in, host_out, dev_in, results, w, stream) -> dict:
+    """The parts of ra_forward_host's pipeline that the compute cannot hide:
+    the upload of its first chunk and the download of its last (each timed
+    alone with CUDA events), next to the whole device-resident call."""
+    import torch
+
+    slices = w.B * w.H
+    chunks = min(slices, 8)  # ra_forward_host's chunk count
+    first = slices // chunks  # slices in the first chunk
+    last = slices - (chunks - 1) * slices // chunks
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, reps=5):
+        fn()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def up():
+        for dst, src in zip(dev_in, host_in):
+            n = src.numel() // slices * first
+            dst.view(-1)[:n].copy_(src.view(-1)[:n], non_blocking=True)
+
+    def down():
+        for dst, src in zip(host_out, results):
+            n = src.numel() // slices * last
+            dst.view(-1)[-n:].copy_(src.view(-1)[-n:], non_blocking=True)
+
+    return {"first_chunk_upload": timed(up), "last_chunk_download": timed(down),
+            "chunks": chunks}
+
+
 def job_throughput(flops_per_replica: float, world: int, ms_max: float) -> float:
     """Whole-job TFLOP/s: every replica's work over the slowest replica's time."""
     return world * flops_per_replica / (ms_max * 1e-3) / 1e12
@@ -212,7 +255,8 @@ def run_reference(args, w) -> None:
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {**w.describe(), "parallelism": "replicas"},
+        "data": "synthetic", "config": {**w.describe(), "parallelism": "replicas",
+                                        "l2": l2_note(w)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -333,7 +377,7 @@ def run_ours(args, w) -> None:
 
     e2e_step()
     torch.cuda.synchronize()
-    n_e2e = max(1, min(args.steps, 5))
+    n_e2e = args.steps  # the same step count as the device leg
     barrier()
     w0 = time.perf_counter()
     e0.record(stream)
@@ -347,6 +391,9 @@ def run_ours(args, w) -> None:
     e2e_value = job_throughput(flops, world, ms_e2e_max)
     h2d = sum(x.numel() * x.element_size() for x in host_in)
     d2h = sum(x.numel() * x.element_size() for x in host_out)
+    stages = None
+    if e2e_path == "ra_forward_host":
+        stages = host_pipeline_stages(host_in, host_out, dev_in, results, w, stream)
 
     peaks = load_peaks()
     achieved = flops / (ms * 1e-3) / 1e12  # one fold launch per step
@@ -373,11 +420,12 @@ def run_ours(args, w) -> None:
                        **({"causal": args.causal} if args.causal else {}),
                        **({"split_segments": G} if args.split is not None else {}),
                        **({"pass": "backward"} if args.backward else {}),
-                       "l2": "inputs larger than L2 (q+k+v = "
-                             f"{3 * q.numel() * q.element_size() / 2**20:.0f} MiB)"},
+                       "l2": l2_note(w)},
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e_max, "path": e2e_path},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e_max, "path": e2e_path,
+                    "steps": n_e2e, "of_device_value": e2e_value / value,
+                    **({"stages_ms": stages} if stages else {})},
             "gpu_launches": args.steps * (3 if args.backward else 2 if args.split is not None else 1),
             "clocks": clocks,
             "pct_of_peak": 100.0 * achieved / peaks["bf16"],

@@ -221,14 +221,21 @@ RA_API int32_t ra_forward_split_segments(int32_t B, int32_t H, int64_t N, int32_
  * live in one library-owned device array of RA_SPLIT_NOALLOC_SCRATCH_BYTES
  * that every GPU which loads the library holds until the process exits.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The array is part of the library's device code: every process that
+ *     loads the library's kernels on a GPU holds its 32 MiB there (at module
+ *     load under CUDA_MODULE_LOADING=EAGER, else when the module is first
+ *     used), whether or not this entry point is ever called.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     stream capture.  A cudaDeviceReset invalidates the cached address:
+ *     call no entry point of this library after resetting a device it used.
  *   - Every call on a device shares the array: calls that overlap on the GPU
  *     (other streams, unordered host threads) race and corrupt each other.
  *     Nothing in it needs to start at zero; each call writes all it reads.
  * Arguments as ra_forward_split, without the workspace.
- * Errors: as ra_forward_split; RA_ERR_UNSUPPORTED when the partial states
+ * Errors: as ra_forward_split (the arguments are checked first, so a bad
+ * argument gives RA_ERR_INVALID_ARG or RA_ERR_MISALIGNED whatever the
+ * size); then RA_ERR_UNSUPPORTED when the partial states
  * (ra_forward_split_workspace_bytes(B, H, N, d, G)) exceed
  * RA_SPLIT_NOALLOC_SCRATCH_BYTES -- nothing is launched then; use
  * ra_forward_split with a caller workspace, or a smaller G.
@@ -358,6 +365,25 @@ RA_API ra_status ra_fold(const ra_state* st, const void* q, const void* kblk,
  */
 RA_API ra_status ra_merge(const ra_state* partials, int32_t G, void* out, float* lse,
                           ra_dtype out_dtype, ra_stream_t stream);
+
+/*
+ * ra_watchdog_config -- settings of the bounded waits in the tensor-core
+ * kernels (bf16 forward, fold, partial, split and backward calls).  The
+ * pages have no counterpart: it belongs to the library's failure detection.
+ *   wait_cycles  SM clock cycles one wait of a kernel may take before the
+ *                kernel gives up: it records RA_ERR_TIMEOUT (read by
+ *                ra_last_device_status), lets the copies and products it
+ *                has in flight finish, frees its tensor memory and returns.
+ *                <= 0 restores the default, 2^31 cycles (about a second).
+ *   stall_cta    a test aid: >= 0 makes the CTA with this index of every
+ *                later fold-kernel launch (forward, causal, partial, fold
+ *                and split calls) load no input, so that its waits run out
+ *                and the launch reports RA_ERR_TIMEOUT; the rows of that
+ *                CTA are then not written.  -1 (the default) turns it off.
+ * The settings are process-wide and apply to calls made after this one, on
+ * every device and thread.  Never fails.
+ */
+RA_API void ra_watchdog_config(int64_t wait_cycles, int64_t stall_cta);
 
 /*
  * ra_last_device_status -- synchronise `stream`, then read and clear the

@@ -23,7 +23,7 @@ __all__ = ["RaError", "RaState", "ra_forward", "ra_forward_causal", "ra_forward_
            "ra_forward_split_segments", "ra_forward_host", "ra_forward_host_workspace_bytes",
            "ra_backward", "ra_backward_causal", "ra_state_init",
            "ra_fold", "ra_merge",
-           "ra_last_device_status", "new_state", "library_path"]
+           "ra_last_device_status", "ra_watchdog_config", "new_state", "library_path"]
 
 
 class RaError(RuntimeError):
@@ -300,3 +300,10 @@ def ra_merge(partials, out_dtype=torch.bfloat16, out=None, lse=None, stream=None
 def ra_last_device_status(stream=None) -> int:
     """Synchronise and return (and clear) the device watchdog status code."""
     return _native.lib().ra_last_device_status(_stream(stream))
+
+
+def ra_watchdog_config(wait_cycles: int = 0, stall_cta: int = -1) -> None:
+    """Bounded-wait limit of the tensor-core kernels in SM cycles (<= 0: the
+    default of 2^31) and the test aid `stall_cta` (>= 0: that CTA of later
+    fold launches loads nothing, so its waits run out; -1: off)."""
+    _native.lib().ra_watchdog_config(int(wait_cycles), int(stall_cta))

@@ -55,6 +55,7 @@ PROTOTYPES = {
     "ra_fold": (_I32, [_SP, _P, _P, _P, _I64, _I64, _I32, _P]),
     "ra_merge": (_I32, [_SP, _I32, _P, _P, _I32, _P]),
     "ra_last_device_status": (_I32, [_P]),
+    "ra_watchdog_config": (None, [_I64, _I64]),
     "ra_status_string": (ctypes.c_char_p, [_I32]),
     "ra_version": (_I32, []),
 }

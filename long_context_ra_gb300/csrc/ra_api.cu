@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -18,7 +19,10 @@ namespace {
 // bounded waits runs out.  One copy per device.
 __device__ int g_status;
 
-constexpr int kMaxDevices = 64;
+// Watchdog settings applied to every tensor-core launch (ra_watchdog_config).
+constexpr int64_t kDefaultWaitCycles = int64_t{1} << 31;
+std::atomic<int64_t> g_wait_limit{kDefaultWaitCycles};
+std::atomic<int64_t> g_stall_cta{-1};
 
 struct DeviceInfo {
   bool ready = false;
@@ -40,8 +44,8 @@ EncodeTiledFn g_encode = nullptr;
 // watchdog word.
 ra_status current_device(DeviceInfo* out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return RA_ERR_ARCH;
-  if (dev < 0 || dev >= kMaxDevices) return RA_ERR_ARCH;
+  const ra_status os = current_ordinal(&dev);
+  if (os != RA_OK) return os;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceInfo& di = g_dev[dev];
   if (!di.ready) {
@@ -153,8 +157,11 @@ ra_status check_attention(const void* q, const void* k, const void* v, int32_t B
 
 // Launch a fold of either precision.  The bf16 path builds the TMA maps over
 // the [rows, d] views of q (slices * nq rows) and k, v (slices * nk rows).
-ra_status run_fold(const FoldArgs& a, ra_dtype dt, cudaStream_t s) {
-  if (dt == RA_F32) return launched(launch_fold_f32(a, s));
+ra_status run_fold(const FoldArgs& args, ra_dtype dt, cudaStream_t s) {
+  if (dt == RA_F32) return launched(launch_fold_f32(args, s));
+  FoldArgs a = args;
+  a.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  a.stall_cta = g_stall_cta.load(std::memory_order_relaxed);
   ra_status st = get_encoder();
   if (st != RA_OK) return st;
   CUtensorMap tq, tk, tv;
@@ -177,6 +184,14 @@ bool state_ok(const ra_state* st) {
 
 }  // namespace
 
+ra_status current_ordinal(int* dev) {
+  const cudaError_t e = cudaGetDevice(dev);
+  if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver) return RA_ERR_ARCH;
+  if (e != cudaSuccess) return RA_ERR_CUDA;
+  if (*dev < 0 || *dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+  return RA_OK;
+}
+
 int device_sm_count() {
   DeviceInfo di;
   if (current_device(&di) != RA_OK) return 1;
@@ -186,10 +201,6 @@ int device_sm_count() {
 }  // namespace ra
 
 using namespace ra;
-
-extern "C" {
-
-}  // extern "C"
 
 namespace ra {
 namespace {
@@ -427,6 +438,7 @@ ra_status backward_impl(const void* q, const void* k, const void* v, const void*
   a.tau = f.tau;
   a.scale_log2 = f.scale_log2;
   a.status = di.status;
+  a.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   if ((st = launched(launch_delta(out, dout, lse, workspace, workspace + rows, rows, d, N, P,
                                   a.layout, dtype == RA_BF16, s))) != RA_OK)
     return st;
@@ -565,6 +577,12 @@ RA_API ra_status ra_last_device_status(ra_stream_t stream) {
   if (cudaMemcpy(di.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
     return RA_ERR_CUDA;
   return word == 0 ? RA_OK : RA_ERR_TIMEOUT;
+}
+
+RA_API void ra_watchdog_config(int64_t wait_cycles, int64_t stall_cta) {
+  g_wait_limit.store(wait_cycles > 0 ? wait_cycles : kDefaultWaitCycles,
+                     std::memory_order_relaxed);
+  g_stall_cta.store(stall_cta >= 0 ? stall_cta : -1, std::memory_order_relaxed);
 }
 
 RA_API const char* ra_status_string(ra_status s) {

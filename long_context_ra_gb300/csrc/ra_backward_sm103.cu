@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
   const uint32_t o_full = dp_full + 8 * (1 + 2 * kMaxParts);
   const uint32_t drain = o_full + 8;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + L::kMisc);
-  const Abort ab{tmem_holder + 1, a.status};
+  const Abort ab{tmem_holder + 1, a.status, a.wait_limit > 0 ? a.wait_limit : kWaitLimit};
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   // unit: (slice, key block j, key tile kt); walk: the query tiles of the
@@ -666,7 +666,7 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
   const uint32_t o_full = dp_full + 8 * (1 + kMaxParts);
   const uint32_t drain = o_full + 8;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + L::kMisc);
-  const Abort ab{tmem_holder + 1, a.status};
+  const Abort ab{tmem_holder + 1, a.status, a.wait_limit > 0 ? a.wait_limit : kWaitLimit};
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   // unit: (slice, query block i, query tile qt); walk: the forward's ring

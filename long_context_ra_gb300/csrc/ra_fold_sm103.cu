@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* gbase = smem_raw + (base - raw);
   const Bars<D> bars{base + L::kBar};
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(gbase + L::kMisc);
-  const Abort ab{tmem_holder + 1, a.status};
+  const Abort ab{tmem_holder + 1, a.status, a.wait_limit > 0 ? a.wait_limit : kWaitLimit};
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -278,8 +278,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, last_parity = 0;  // per-stage bit masks, for the drain
-      bool ok = true;
-      if (n_iter > 0) {
+      // A stalled CTA (a test aid) loads nothing: its consumers' waits run
+      // out, raise the abort flag and return; nothing is in flight to drain.
+      bool ok = static_cast<int64_t>(blockIdx.x) != a.stall_cta;
+      if (ok && n_iter > 0) {
         const uint32_t qbytes = (has_t1 ? 2u : 1u) * L::kTileBytes;
         mbar_arrive_expect_tx(bars.q_full(), qbytes);
         load_tile<D>(base + L::kQ0, &tq, striped, slice * a.nq + walk.pos(i, lr0), i,
@@ -312,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         // Let every load already issued land before the CTA goes away.
-        if (n_iter > 0) wait_drain(bars.q_full(), 0);
+        if (n_iter > 0 && static_cast<int64_t>(blockIdx.x) != a.stall_cta)
+          wait_drain(bars.q_full(), 0);
         for (int s = 0; s < L::kStages; ++s)
           if (issued & (1u << s)) wait_drain(bars.kv_full(s), (last_parity >> s) & 1u);
       }

@@ -18,7 +18,7 @@
 
 namespace {
 
-constexpr int kMaxDevices = 64;
+using ra::kMaxDevices;
 // Up to this many chunks: enough that the first upload and the last download
 // are small next to the compute.
 constexpr int64_t kMaxChunks = 8;
@@ -34,7 +34,8 @@ Streams g_streams[kMaxDevices];
 // RA_ERR_ARCH), created on first use.
 ra_status device_streams(Streams* out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RA_ERR_ARCH;
+  const ra_status os = ra::current_ordinal(&dev);
+  if (os != RA_OK) return os;
   std::lock_guard<std::mutex> lock(g_mu);
   Streams& s = g_streams[dev];
   if (!s.up) {

@@ -61,6 +61,8 @@ struct FoldArgs {
   float* st_l;
   float* st_o;
   int* status;       // device watchdog word (0 = fine)
+  int64_t wait_limit;  // SM cycles a bounded wait may take (tensor path)
+  int64_t stall_cta;   // test aid: this CTA of the tensor path loads nothing (-1: none)
   PartialPtrs part;  // partial mode
 };
 
@@ -86,6 +88,7 @@ struct BackwardArgs {
   float tau;         // 1 / sqrt(d)
   float scale_log2;  // tau * log2(e)
   int* status;       // device watchdog word
+  int64_t wait_limit;  // SM cycles a bounded wait may take
 };
 
 struct MergeArgs {
@@ -125,6 +128,14 @@ constexpr int kStatusTimeout = 1;
 
 // Number of SMs of the current device (cached).
 int device_sm_count();
+
+// Devices the library keeps per-device state for (ordinals 0 .. kMaxDevices-1).
+constexpr int kMaxDevices = 64;
+
+// Ordinal of the current device: RA_ERR_ARCH when there is no usable device
+// or driver, RA_ERR_CUDA for another failure of the lookup,
+// RA_ERR_UNSUPPORTED for an ordinal of kMaxDevices or more.
+ra_status current_ordinal(int* dev);
 
 // The argument and size checks of ra_forward / ra_forward_causal, without
 // the buffers: the status those calls would return for a valid set of

@@ -17,6 +17,7 @@
 
 #include <cuda_runtime.h>
 
+#include <cstdint>
 #include <mutex>
 
 #include "ra.h"
@@ -27,7 +28,7 @@ namespace {
 // Scratch of the allocation-free split forward (see RA_SPLIT_NOALLOC_SCRATCH_BYTES).
 static __device__ __align__(256) unsigned char g_split_scratch[RA_SPLIT_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
+using ra::kMaxDevices;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
@@ -36,7 +37,8 @@ void* g_scratch_ptr[kMaxDevices] = {};
 // once per device, with that device current, and cached.
 ra_status scratch_address(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RA_ERR_ARCH;
+  const ra_status os = ra::current_ordinal(&dev);
+  if (os != RA_OK) return os;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch_ptr[dev]) {
     int major = 0, minor = 0;
@@ -58,15 +60,22 @@ extern "C" RA_API ra_status ra_forward_split_noalloc(const void* q, const void* 
                                                      void* out, float* lse, int32_t B, int32_t H,
                                                      int64_t N, int32_t d, int32_t P, int32_t G,
                                                      ra_dtype dtype, ra_stream_t stream) {
-  if (B < 0 || H < 0 || N < 0 || d < 1 || G < 1 || G > RA_MAX_PARTIALS)
-    return RA_ERR_INVALID_ARG;
+  // The arguments first, so that a bad one is reported as such whatever the
+  // size; check_forward_args also bounds the row count.
+  ra_status st = ra::check_forward_args(B, H, N, d, P, false, RA_LAYOUT_CONTIGUOUS, dtype);
+  if (st != RA_OK) return st;
+  if (G < 1 || G > RA_MAX_PARTIALS || G > P) return RA_ERR_INVALID_ARG;
   const int64_t rows = static_cast<int64_t>(B) * H * N;
   if (rows == 0) return RA_OK;
+  if (!q || !k || !v || !out || !lse) return RA_ERR_INVALID_ARG;
+  const uintptr_t al = dtype == RA_BF16 ? 16 : 4;
+  for (const void* ptr : {q, k, v, static_cast<const void*>(out)})
+    if (reinterpret_cast<uintptr_t>(ptr) % al != 0) return RA_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(lse) % 4 != 0) return RA_ERR_MISALIGNED;
   if (ra::split_workspace_bytes(rows, d, G) > RA_SPLIT_NOALLOC_SCRATCH_BYTES)
     return RA_ERR_UNSUPPORTED;  // the partial states do not fit the fixed scratch
   void* scratch = nullptr;
-  const ra_status st = scratch_address(&scratch);
-  if (st != RA_OK) return st;
+  if ((st = scratch_address(&scratch)) != RA_OK) return st;
   return ra::split_forward(q, k, v, out, lse, B, H, N, d, P, G, scratch,
                            RA_SPLIT_NOALLOC_SCRATCH_BYTES, dtype,
                            reinterpret_cast<cudaStream_t>(stream));

@@ -20,11 +20,16 @@ using namespace ptx;
 
 constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;  // keys per K/V tile
-constexpr long long kWaitLimit = 1ll << 31;  // SM cycles, about one second
+// Default limit of a bounded wait, in SM cycles (about one second).  A
+// launch may shorten it (FoldArgs / BackwardArgs wait_limit).  The drain
+// after an abort always allows the full default, so that copies and MMAs
+// still in flight land before the CTA leaves.
+constexpr long long kWaitLimit = 1ll << 31;
 
 struct Abort {
   volatile uint32_t* flag;
   int* status;
+  long long limit;  // SM cycles a wait may take before it gives up
   __device__ void raise() const {
     *flag = 1u;
     atomicCAS(status, 0, kStatusTimeout);
@@ -38,7 +43,7 @@ __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const Abort
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*ab.flag) return false;
-    if (clock64() - start > kWaitLimit) {
+    if (clock64() - start > ab.limit) {
       ab.raise();
       return false;
     }
@@ -62,7 +67,7 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const A
   while (true) {
     done = done || mbar_try_wait(bar, parity);
     if (__all_sync(0xffffffffu, done)) return true;
-    const bool timed_out = clock64() - start > kWaitLimit;
+    const bool timed_out = clock64() - start > ab.limit;
     const bool give_up = (*ab.flag != 0u) || timed_out;
     if (__any_sync(0xffffffffu, give_up)) {
       if (__any_sync(0xffffffffu, timed_out) && (threadIdx.x % 32) == 0) ab.raise();

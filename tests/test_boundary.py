@@ -139,6 +139,31 @@ def test_noalloc_split_rejects_oversize_without_device(L):
         _native.RA_ERR_ARCH
 
 
+def test_noalloc_split_checks_arguments_before_the_scratch_size(L):
+    # oversize for the scratch AND wrong otherwise: the argument error wins
+    big = dict(B=1, H=1, N=65536, d=128, P=8)
+
+    def fn(q=A, out=A, lse=A, G=8, dt=BF16, **kw):
+        a = {**big, **kw}
+        return L.ra_forward_split_noalloc(q, A, A, out, lse, a["B"], a["H"], a["N"], a["d"],
+                                          a["P"], G, dt, None)
+    assert fn() == _native.RA_ERR_UNSUPPORTED                    # valid, too large
+    assert fn(G=16) == _native.RA_ERR_INVALID_ARG                 # G > P
+    assert fn(q=None) == _native.RA_ERR_INVALID_ARG
+    assert fn(lse=None) == _native.RA_ERR_INVALID_ARG
+    assert fn(dt=9) == _native.RA_ERR_INVALID_ARG
+    assert fn(q=A + 8) == _native.RA_ERR_MISALIGNED
+    assert fn(out=A + 8) == _native.RA_ERR_MISALIGNED
+    assert fn(N=65536 - 8) == _native.RA_ERR_UNSUPPORTED         # P does not divide N
+    assert fn(N=1 << 31, P=1 << 14) == _native.RA_ERR_UNSUPPORTED  # too many rows, no overflow
+
+
+def test_watchdog_config_is_host_only(L):
+    # settings only; no device needed, nothing returned
+    L.ra_watchdog_config(1 << 20, 3)
+    L.ra_watchdog_config(0, -1)
+
+
 def test_backward_validation(L):
     def fb(ws=A, N=1024, P=4, d=64, dt=BF16):
         return L.ra_backward(A, A, A, A, A, A, A, A, A, ws, 1, 1, N, d, P, dt, None)

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import long_context_ra_gb300 as ra
-from gpu_util import TOL_LSE, TOL_OUT, assert_finite, max_err, oracle_ring, to_oracle
+from gpu_util import TOL_OUT, assert_finite, check_out_lse, check_same, oracle_ring
 from long_context_ra_gb300 import synth
 from oracle import ra_oracle
 
@@ -27,14 +27,7 @@ def rnd(shape, seed, dtype, scale=1.0):
 
 def check(O, q, k, v, P, layout, out, lse, rows=None):
     want_out, want_lse = oracle_ring(O, q, k, v, P, rows=rows, causal=True, layout=layout)
-    d = q.shape[-1]
-    o2, l2 = out.reshape(-1, d), lse.reshape(-1)
-    if rows is not None:
-        idx = torch.as_tensor(rows, device=out.device)
-        o2, l2 = o2.index_select(0, idx), l2.index_select(0, idx)
-    eo, el = max_err(o2, want_out), max_err(l2, want_lse)
-    assert eo <= TOL_OUT[q.dtype], f"{layout}: out error {eo:.3e}"
-    assert el <= TOL_LSE, f"{layout}: lse error {el:.3e}"
+    check_out_lse(out, lse, want_out, want_lse, q.dtype, f"causal {layout}", rows=rows)
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)
@@ -85,7 +78,8 @@ def test_causal_partials_merge(O, layout, dtype):
     assert any(torch.isneginf(p.m).any().item() for p in parts)  # empty partials exist
     out, lse = ra.ra_merge(parts, out_dtype=dtype)
     check(O, q, k, v, P, layout, out.reshape(B, H, N, d), lse.reshape(B, H, N))
-    assert (out.float() - out_f.reshape(-1, d).float()).abs().max().item() <= TOL_OUT[dtype]
+    check_same(out, out_f.reshape(-1, d), dtype, f"causal {layout} merge vs forward",
+               TOL_OUT[dtype])
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)

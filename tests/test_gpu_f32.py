@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import long_context_ra_gb300 as ra
-from gpu_util import TOL_LSE, TOL_OUT, check_forward, max_err, oracle_ring
+from gpu_util import TOL_OUT, check_close, check_forward, check_same, max_err, oracle_ring
 from long_context_ra_gb300 import synth
 from oracle import ra_oracle
 
@@ -91,8 +91,9 @@ def test_partial_and_merge_equal_forward(O):
     for G in (1, 2, 3, 6):
         parts = ra.ra_forward_partial(q, k, v, P=P, G=G)
         out, lse = ra.ra_merge(parts, out_dtype=torch.float32)
-        assert max_err(out, out_f.reshape(-1, d).cpu().double().numpy()) <= 1e-5
-        assert max_err(lse, lse_f.reshape(-1).cpu().double().numpy()) <= 1e-5
+        check_same(out, out_f.reshape(-1, d), torch.float32, f"G={G} merge vs forward out", 1e-5)
+        check_same(lse, lse_f.reshape(-1), torch.float32, f"G={G} merge vs forward lse", 1e-5,
+                   relative=False)
     # the partials themselves against the oracle's segment states
     parts = ra.ra_forward_partial(q, k, v, P=P, G=3)
     for gi in range(3):
@@ -100,8 +101,8 @@ def test_partial_and_merge_equal_forward(O):
         assert max_err(parts[gi].m, m) <= 1e-5
         rel_l = parts[gi].l.double().cpu().numpy() / l
         assert np.max(np.abs(rel_l - 1)) <= 1e-5
-        norm = (parts[gi].o / parts[gi].l[:, None]).double().cpu().numpy()
-        assert np.max(np.abs(norm - o / l[:, None])) <= 1e-5
+        norm = parts[gi].o / parts[gi].l[:, None]
+        check_close(norm, o / l[:, None], torch.float32, f"partial {gi} o/l", 1e-5)
 
 
 def test_fold_chain_in_ring_order_equals_forward(O):
@@ -120,8 +121,8 @@ def test_fold_chain_in_ring_order_equals_forward(O):
             vj = v[:, :, j * c:(j + 1) * c].reshape(B * H, c, d).contiguous()
             ra.ra_fold(st, qi, kj, vj, batch=B * H)
         out, lse = ra.ra_merge([st], out_dtype=torch.float32)
-        want = out_f[:, :, i * c:(i + 1) * c].reshape(-1, d).cpu().double().numpy()
-        assert max_err(out, want) <= 1e-5
+        want = out_f[:, :, i * c:(i + 1) * c].reshape(-1, d)
+        check_same(out, want, torch.float32, "fold chain vs forward", 1e-5)
         assert max_err(lse, lse_f[:, :, i * c:(i + 1) * c].reshape(-1).cpu().double().numpy()) <= 1e-5
 
 

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import long_context_ra_gb300 as ra
-from gpu_util import TOL_OUT, assert_finite, check_forward
+from gpu_util import TOL_LSE, TOL_OUT, assert_finite, check_forward, check_same
 from long_context_ra_gb300 import synth
 from oracle import ra_oracle
 
@@ -31,8 +31,8 @@ def test_split_matches_oracle(O, dtype, G):
     assert_finite(out, lse)
     check_forward(O, q, k, v, P, out, lse)
     ref_out, ref_lse = ra.ra_forward(q, k, v, P)
-    assert (out.float() - ref_out.float()).abs().max().item() <= TOL_OUT[dtype]
-    assert (lse - ref_lse).abs().max().item() <= 1e-3
+    check_same(out, ref_out, dtype, "split vs forward out", TOL_OUT[dtype])
+    check_same(lse, ref_lse, dtype, "split vs forward lse", TOL_LSE, relative=False)
 
 
 def test_split_recommendation():

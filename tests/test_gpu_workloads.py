@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import long_context_ra_gb300 as ra
-from gpu_util import assert_finite, check_forward
+from gpu_util import TOL_LSE, TOL_OUT, assert_finite, check_forward, check_same
 from long_context_ra_gb300 import synth
 from oracle import ra_oracle
 
@@ -52,8 +52,11 @@ def test_workload5_partials_and_merge(O):
     assert_finite(out, lse)
     rows = synth.sample_rows(w, 256)
     check_forward(O, q, k, v, w.P, out, lse, rows=rows)
-    # the single-pass forward agrees with partials + merge
+    # the single-pass forward agrees with partials + merge, on every row
     out_f, lse_f = ra.ra_forward(q, k, v, P=w.P)
-    assert (out_f.float() - out.float()).abs().max().item() <= 2e-2
-    assert (lse_f - lse).abs().max().item() <= 1e-3
+    for h in range(w.H):  # one head at a time keeps the host copies small
+        check_same(out[:, h], out_f[:, h], torch.bfloat16, "merge vs single-pass out",
+                   TOL_OUT[torch.bfloat16])
+        check_same(lse[:, h], lse_f[:, h], torch.bfloat16, "merge vs single-pass lse",
+                   TOL_LSE, relative=False)
     assert ra.ra_last_device_status() == 0

@@ -68,3 +68,35 @@ def test_workload_sizes():
     w = synth.WORKLOADS[4]
     assert (w.B, w.H, w.N, w.d, w.P, w.c) == (1, 8, 131072, 128, 32, 4096)
     assert w.flops == 4.0 * 8 * 131072 ** 2 * 128
+
+
+def test_workload2_forces_rescales():
+    """Workload 2's ring really rescales (alpha < 1): counted on the oracle's
+    state after each ring step, over 512 sampled rows.  A row rescales at
+    step t when the visiting block raises its running max.  With the mild
+    shift of this recipe (|q_bar| is about sqrt(d / N) = 1/8) the block
+    maxima behave like exchangeable draws, so a new block beats the t
+    earlier ones with probability about 1 / (t + 1); events occur at every
+    step, as in the pages' worked example (step B raises the max)."""
+    import numpy as np
+
+    from oracle import ra_oracle
+
+    O = ra_oracle.get()
+    w = synth.WORKLOADS[2]
+    q, k, v = synth.make_inputs(w, "cpu")
+    bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).view(torch.int16).numpy().view(np.uint16)
+    qa, ka, va = bits(q), bits(k), bits(v)
+    rows = synth.sample_rows(w, 512).numpy()
+    m_prev = None
+    events = []
+    for t in range(1, w.P + 1):
+        _, _, m, _, _ = O.ring(qa, ka, va, w.P, dtype="bf16", rows=rows, t0=0, t1=t, state=True)
+        if m_prev is not None:
+            events.append(float(np.mean(m > m_prev)))  # alpha = exp(m_prev - m) < 1
+        assert m_prev is None or np.all(m >= m_prev)  # the running max never falls
+        m_prev = m
+    assert all(e > 0 for e in events), events
+    for t, e in enumerate(events, start=1):
+        assert 0.4 / (t + 1) < e < 2.0 / (t + 1) + 0.05, (t, e)
+    assert np.mean(events) > 0.15

@@ -16,7 +16,7 @@ import ctypes
 import pytest
 import torch
 
-from gpu_util import TOL_LSE, TOL_OUT
+from gpu_util import TOL_LSE, TOL_OUT, check_same
 import long_context_ra_gb300 as ra
 from long_context_ra_gb300 import _native
 from long_context_ra_gb300.build import build
@@ -36,10 +36,10 @@ def _inputs(shape, seed):
     return [torch.randn(shape, device=DEV, generator=g).to(torch.bfloat16) for _ in range(3)]
 
 
-def _noalloc(L, q, k, v, P, G):
+def _noalloc(L, q, k, v, P, G, out=None, lse=None):
     B, H, N, d = q.shape
-    out = torch.empty_like(q)
-    lse = torch.empty(B, H, N, device=DEV, dtype=torch.float32)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(B, H, N, device=DEV, dtype=torch.float32) if lse is None else lse
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     code = L.ra_forward_split_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                       lse.data_ptr(), B, H, N, d, P, G, _native.RA_BF16, stream)
@@ -57,8 +57,25 @@ def test_noalloc_matches_caller_scratch_twice(L):
         ref_out, ref_lse = ra.ra_forward_split(q, k, v, P, G=G)
         torch.cuda.synchronize()
         assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
-        assert (out.float() - ref_out.float()).abs().max().item() <= TOL_OUT[torch.bfloat16]
-        assert (lse - ref_lse).abs().max().item() <= TOL_LSE
+        check_same(out, ref_out, torch.bfloat16, "noalloc vs split out", TOL_OUT[torch.bfloat16])
+        check_same(lse, ref_lse, torch.bfloat16, "noalloc vs split lse", TOL_LSE, relative=False)
+    assert ra.ra_last_device_status() == 0
+
+
+def test_noalloc_call_takes_no_device_memory(L):
+    """After a first call (which looks up the scratch address), a call leaves
+    the device's free memory exactly as it was: it allocated nothing."""
+    B, H, N, d, P, G = 1, 2, 4096, 128, 8, 2
+    q, k, v = _inputs((B, H, N, d), 600)
+    out = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device=DEV, dtype=torch.float32)
+    _noalloc(L, q, k, v, P, G, out, lse)
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    _noalloc(L, q, k, v, P, G, out, lse)
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before
     assert ra.ra_last_device_status() == 0
 
 
