@@ -84,9 +84,12 @@ struct Layout {
   static constexpr int kBar = kKV + kStages * kTileBytes;
   // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], drain
   static constexpr int kNumBars = 1 + 2 * kStages + 7;
-  static constexpr int kMisc = kBar + kNumBars * 8;  // TMEM base, abort flag
-  static constexpr int kSteps = kMisc + 16;          // causal step table (int4 per step)
+  // TMEM base and abort flag, then the causal step table (int4 per step);
+  // both start on a 16-byte boundary (the table is read as int4).
+  static constexpr int kMisc = (kBar + kNumBars * 8 + 15) / 16 * 16;
+  static constexpr int kSteps = kMisc + 16;
   static constexpr int kBytes = kSteps + kMaxCausalSteps * 16;
+  static_assert(kSteps % 16 == 0, "the step table is read as int4");
   static constexpr int kSmem = kBytes + 1024;  // slack for 1024-byte alignment
   static_assert(kSmem <= 232448, "shared memory budget");
 };

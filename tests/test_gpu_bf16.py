@@ -73,6 +73,30 @@ def test_large_scores(O):
     check_forward(O, q, k, v, P, out, lse)
 
 
+@pytest.mark.parametrize("jump", [200.0, -200.0])
+def test_score_jump_beyond_the_exponent_range(O, jump):
+    """A later key tile whose scores differ from the first tile's by 200
+    (about 289 in log2 units): far outside the range of a float exponent.
+    Rising, the exponentials against the old reference overflow (the
+    kernel must redo the tile with the new max); falling, they underflow to
+    nothing.  out is the mean of V over the dominant tile."""
+    B, H, N, d, P = 1, 1, 256, 64, 1
+    q = torch.zeros(B, H, N, d)
+    q[..., 0] = 8.0
+    k = torch.zeros(B, H, N, d)
+    k[..., 128:, 0] = jump  # tau q.k = 8 * jump / 8 on the second tile
+    g = torch.Generator().manual_seed(61)
+    v = torch.randn(B, H, N, d, generator=g)
+    q, k, v = (x.to(DEV, torch.bfloat16) for x in (q, k, v))
+    out, lse = ra.ra_forward(q, k, v, P=P)
+    assert_finite(out, lse)
+    check_forward(O, q, k, v, P, out, lse)
+    dom = slice(128, 256) if jump > 0 else slice(0, 128)
+    want = v[0, 0, dom].float().mean(0)
+    assert (out[0, 0].float() - want).abs().max().item() <= 2e-2
+    assert (lse[0, 0] - (max(jump, 0.0) + math.log(128))).abs().max().item() <= 1e-3
+
+
 def test_deterministic():
     shape = (1, 2, 512, 128)
     q, k, v = rnd(shape, 31), rnd(shape, 32), rnd(shape, 33)
