@@ -20,9 +20,16 @@ three operations, so the same loop runs on CPU ranks (gloo) with other
 operations in tests.
 
 Causal attention (section "Causal masking, load balance, and other
-wrinkles") is supported for the contiguous split: a block j < i is folded
-whole, block j > i is skipped (every key is later than every query of the
-rank), and the rank's own block is folded under the causal mask.
+wrinkles"; "Ring attention, explained", section "The causal-mask catch"):
+- contiguous split: a block j < i is folded whole, block j > i is skipped
+  (every key is later than every query of the rank), and the rank's own
+  block is folded under the causal mask.  Rank P - 1 does P times the work
+  of rank 0.
+- zigzag split: the sequence is cut into 2P chunks and rank i holds chunks
+  i and 2P-1-i (its block lists chunk i, then chunk 2P-1-i).  Against block
+  j < i both of its chunks see chunk j whole and chunk 2P-1-j not at all;
+  against j > i only its chunk 2P-1-i sees anything, and it sees the whole
+  block.  Every rank then does the same work at every step.
 """
 from __future__ import annotations
 
@@ -80,26 +87,49 @@ def ring_block(rank: int, step: int, world: int) -> int:
     return (rank - step) % world
 
 
-def ring_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, group=None,
-                 ops: RingOps | None = None, causal: bool = False):
-    """Attention of this rank's query block over the whole sequence.
+def _exchange(cur, nxt, send_to, recv_from, group):
+    """Post the send of the held block and the receive of the next one."""
+    p2p = [dist.P2POp(dist.isend, cur[0], send_to, group),
+           dist.P2POp(dist.isend, cur[1], send_to, group),
+           dist.P2POp(dist.irecv, nxt[0], recv_from, group),
+           dist.P2POp(dist.irecv, nxt[1], recv_from, group)]
+    return dist.batch_isend_irecv(p2p)
 
-    q, k, v: this rank's block [B, H, c, d] (block i = the rank's index in
-    `group`; the sequence is the blocks in rank order).  Returns out
-    [B, H, c, d] (q's dtype) and lse [B, H, c] (fp32) of this block.
-    Every rank must call it with blocks of the same shape."""
-    if ops is None:
-        ops = library_ops()
+
+def _neighbours(group):
     world = dist.get_world_size(group)
     rank = dist.get_rank(group)
-    B, H, c, d = q.shape
-    if k.shape != q.shape or v.shape != q.shape:
-        raise ValueError("q, k, v blocks must share one shape")
-    bh = B * H
     send_to, recv_from = ring_neighbours(rank, world)
     if group is not None:
         send_to = dist.get_global_rank(group, send_to)
         recv_from = dist.get_global_rank(group, recv_from)
+    return world, rank, send_to, recv_from
+
+
+def ring_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, group=None,
+                 ops: RingOps | None = None, causal: bool = False,
+                 layout: str = "contiguous"):
+    """Attention of this rank's query block over the whole sequence.
+
+    q, k, v: this rank's block [B, H, c, d] (block i = the rank's index in
+    `group`).  layout "contiguous": the sequence is the blocks in rank
+    order; "zigzag" (causal only): the block holds chunks i and 2P-1-i of
+    2P chunks of c/2 tokens, in that order.  Returns out [B, H, c, d] (q's
+    dtype) and lse [B, H, c] (fp32) of this block, rows in the block's
+    order.  Every rank must call it with blocks of the same shape."""
+    if ops is None:
+        ops = library_ops()
+    if layout not in ("contiguous", "zigzag"):
+        raise ValueError(f"unknown layout {layout!r}")
+    if layout == "zigzag":
+        if not causal:
+            raise ValueError("the zigzag split only matters under the causal mask")
+        return _ring_forward_zigzag(q, k, v, group, ops)
+    world, rank, send_to, recv_from = _neighbours(group)
+    B, H, c, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v blocks must share one shape")
+    bh = B * H
 
     qf = q.reshape(bh, c, d).contiguous()
     # The caller's k, v are only read: blocks arrive in two receive buffers
@@ -114,12 +144,7 @@ def ring_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, group=None,
         reqs = []
         nxt = recv[t % 2] if t + 1 < world else None
         if t + 1 < world:
-            # launched before the fold, waited on after it
-            p2p = [dist.P2POp(dist.isend, cur[0], send_to, group),
-                   dist.P2POp(dist.isend, cur[1], send_to, group),
-                   dist.P2POp(dist.irecv, nxt[0], recv_from, group),
-                   dist.P2POp(dist.irecv, nxt[1], recv_from, group)]
-            reqs = dist.batch_isend_irecv(p2p)
+            reqs = _exchange(cur, nxt, send_to, recv_from, group)  # before the fold
         if not causal or j < rank:
             ops.fold(state, qf, cur[0], cur[1], bh)
         elif j == rank:
@@ -130,3 +155,55 @@ def ring_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, group=None,
         cur = nxt
     out, lse = ops.finish(states, q.dtype)
     return out.reshape(B, H, c, d), lse.reshape(B, H, c)
+
+
+def _ring_forward_zigzag(q, k, v, group, ops: RingOps):
+    """The causal ring over the zigzag split (see the module docstring).
+
+    The block's two chunks keep separate states (rows of chunk i, "lo", and
+    of chunk 2P-1-i, "hi"), and blocks travel as [2 chunks, B*H, c/2, d] so
+    that either chunk is a contiguous operand of the fold."""
+    world, rank, send_to, recv_from = _neighbours(group)
+    B, H, c, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v blocks must share one shape")
+    if c % 2:
+        raise ValueError("the zigzag split needs an even block length")
+    bh, h = B * H, c // 2
+    halves = lambda t: t.reshape(bh, 2, h, d).transpose(0, 1).contiguous()  # [2, bh, h, d]
+    qh = halves(q)
+    cur = [halves(k), halves(v)]
+    recv = [[torch.empty_like(cur[0]), torch.empty_like(cur[1])] for _ in range(min(world - 1, 2))]
+    st = [ops.new_state(bh * h, d, q), ops.new_state(bh * h, d, q)]  # lo, hi
+    extra = [[], []]
+    as4 = lambda t: t.reshape(1, bh, h, d)
+    for t in range(world):
+        j = ring_block(rank, t, world)
+        nxt = recv[t % 2] if t + 1 < world else None
+        reqs = _exchange(cur, nxt, send_to, recv_from, group) if t + 1 < world else []
+        kc, vc = cur
+        if j == rank:
+            # own block: each chunk against itself under the mask (local
+            # order is position order), and chunk 2P-1-i sees chunk i whole
+            extra[0].append(ops.diagonal(as4(qh[0]), as4(kc[0]), as4(vc[0])))
+            extra[1].append(ops.diagonal(as4(qh[1]), as4(kc[1]), as4(vc[1])))
+            ops.fold(st[1], qh[1], kc[0], vc[0], bh)
+        elif j < rank:
+            # chunk j precedes both query chunks; chunk 2P-1-j follows both
+            ops.fold(st[0], qh[0], kc[0], vc[0], bh)
+            ops.fold(st[1], qh[1], kc[0], vc[0], bh)
+        else:
+            # only chunk 2P-1-i sees block j, and all of it
+            ops.fold(st[1], qh[1], kc[0], vc[0], bh)
+            ops.fold(st[1], qh[1], kc[1], vc[1], bh)
+        for r in reqs:
+            r.wait()
+        cur = nxt
+    outs, lses = [], []
+    for x in range(2):
+        o, l = ops.finish([st[x]] + extra[x], q.dtype)
+        outs.append(o.reshape(bh, h, d))
+        lses.append(l.reshape(bh, h))
+    out = torch.stack(outs, dim=1).reshape(B, H, c, d)
+    lse = torch.stack(lses, dim=1).reshape(B, H, c)
+    return out, lse

@@ -92,3 +92,18 @@ def test_causal_workload4_sampled(O, layout):
     rows = synth.sample_rows(w, 512, seed=11)
     check(O, q, k, v, w.P, layout, out, lse, rows=rows.numpy())
     assert ra.ra_last_device_status() == 0
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+def test_causal_at_the_largest_step_count(O, layout):
+    """P = 1024 ring blocks of one tile each: the largest step count of the
+    causal tensor path (its per-unit step table holds 1024 entries)."""
+    B, H, N, d, P = 1, 1, 1024 * 128, 128, 1024
+    q, k, v = (rnd((B, H, N, d), 500 + s, torch.bfloat16) for s in range(3))
+    out, lse = ra.ra_forward_causal(q, k, v, P, layout=layout)
+    assert_finite(out, lse)
+    g = torch.Generator().manual_seed(12)
+    rows = torch.cat([torch.tensor([0, 127, 128, N - 129, N - 128, N - 1]),
+                      torch.randint(0, N, (250,), generator=g)]).unique().numpy()
+    check(O, q, k, v, P, layout, out, lse, rows=rows)
+    assert ra.ra_last_device_status() == 0

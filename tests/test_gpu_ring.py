@@ -44,3 +44,14 @@ def test_one_rank_ring_on_the_gpu(O, group, causal, d):
     out, lse = ring_forward(q, k, v, causal=causal)
     torch.cuda.synchronize()
     check_forward(O, q, k, v, 1, out, lse, causal=causal)
+
+
+def test_one_rank_zigzag_ring_on_the_gpu(O, group):
+    """With one rank the zigzag block is chunks 0 and 1, the whole sequence
+    in order: the result is causal attention over it."""
+    g = torch.Generator(device=DEV).manual_seed(77)
+    q, k, v = (torch.randn(1, 2, 1024, 128, device=DEV, generator=g).to(torch.bfloat16)
+               for _ in range(3))
+    out, lse = ring_forward(q, k, v, causal=True, layout="zigzag")
+    torch.cuda.synchronize()
+    check_forward(O, q, k, v, 1, out, lse, causal=True)

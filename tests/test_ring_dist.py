@@ -6,8 +6,9 @@ holds.  The folds here are the fp64 oracle's (the ring's operations are
 pluggable; on GPUs they are the library's kernels), so the test checks the
 orchestration: every rank visits the blocks (i - t) mod P in order, each
 exactly once, the exchange hands each block on intact, the causal variant
-skips and masks the right blocks, and the merged result equals dense
-attention over the whole sequence ("Ring Attention: the math", sections "The
+skips and masks the right blocks (contiguous and zigzag splits; under
+zigzag every rank folds the same number of keys), and the merged result
+equals dense attention over the whole sequence ("Ring Attention: the math", sections "The
 ring schedule: passing K/V around" and "A worked numeric example")."""
 import os
 import socket
@@ -99,6 +100,24 @@ def _rank_main(rank, world, port, results):
             res[causal] = (order, want,
                            float(np.abs(out.reshape(-1, D).numpy() - w_out).max()),
                            float(np.abs(lse.reshape(-1).numpy() - w_lse).max()))
+        # zigzag: rank i holds chunks i and 2P-1-i of 2P chunks of C/2 tokens
+        h = C // 2
+        pos = list(range(rank * h, rank * h + h)) + \
+            list(range((2 * world - 1 - rank) * h, (2 * world - 1 - rank) * h + h))
+        zz = lambda t: t[:, :, pos].contiguous()
+        visits = []
+        out, lse = ring_forward(zz(q), zz(k), zz(v), ops=_oracle_ops(O, visits), causal=True,
+                                layout="zigzag")
+        bh = B * H
+        rows = [s * world * C + p for s in range(bh) for p in pos]
+        w_out, w_lse = O.dense(q.reshape(bh, world * C, D).numpy(),
+                               k.reshape(bh, world * C, D).numpy(),
+                               v.reshape(bh, world * C, D).numpy(), dtype="f64",
+                               rows=np.array(rows), causal=True)
+        # every rank folds the same number of key rows (the point of zigzag)
+        folded = sum(x.shape[1] for x in visits if not isinstance(x, str))
+        res["zigzag"] = (float(np.abs(out.reshape(-1, D).numpy() - w_out).max()),
+                         float(np.abs(lse.reshape(-1).numpy() - w_lse).max()), folded)
         # the caller's blocks are only read (blocks arrive in separate buffers)
         res["inputs_intact"] = bool(torch.equal(ki, blk(k, rank)) and torch.equal(vi, blk(v, rank)))
         results[rank] = res
@@ -115,11 +134,16 @@ def test_ring_over_gloo_equals_dense(world):
                            join=True, start_method="spawn")
         results = dict(results)
     assert sorted(results) == list(range(world))
+    folded = set()
     for rank, res in results.items():
         assert res.pop("inputs_intact"), rank
+        e_out, e_lse, n = res.pop("zigzag")
+        assert e_out <= 1e-12 and e_lse <= 1e-12, (rank, "zigzag", e_out, e_lse)
+        folded.add(n)
         for causal, (order, want, e_out, e_lse) in res.items():
             assert order == want, (rank, causal, order, want)
             assert e_out <= 1e-12 and e_lse <= 1e-12, (rank, causal, e_out, e_lse)
+    assert len(folded) == 1, folded  # the same unmasked folds on every rank
 
 
 def test_ring_schedule_matches_the_pages_table():
