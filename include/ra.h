@@ -319,6 +319,51 @@ RA_API ra_status ra_backward_causal(const void* q, const void* k, const void* v,
                                     ra_stream_t stream);
 
 /*
+ * ra_backward_rowterms -- the per-query terms of the backward for `rows`
+ * query rows: D = rowsum(dout * out) and -lse * log2(e), written to
+ * workspace[0 .. rows) and workspace[rows .. 2 rows).  The first step of the
+ * ring backward on a device ("Ring attention, explained", step 6), before
+ * its query block meets the visiting blocks with ra_backward_block.
+ *   out, dout  [rows, d] of `dtype` (out from the forward);  lse [rows] fp32.
+ *   workspace  caller-owned fp32 [2 * rows], 16-byte aligned.
+ * Errors: RA_ERR_INVALID_ARG (NULL pointer, rows < 0, d < 1, bad dtype),
+ * RA_ERR_UNSUPPORTED (rows >= 2^31), RA_ERR_MISALIGNED, RA_ERR_ARCH,
+ * RA_ERR_CUDA.
+ */
+RA_API ra_status ra_backward_rowterms(const void* out, const void* dout, const float* lse,
+                                      int64_t rows, int32_t d, ra_dtype dtype, float* workspace,
+                                      ra_stream_t stream);
+
+/*
+ * ra_backward_block -- one step of the ring backward across devices ("Ring
+ * attention, explained", step 6: the backward runs on the same ring, the
+ * key-value blocks carrying their gradient accumulators).  The query block
+ * (q, dout, its lse and row terms) meets one visiting K/V block and adds
+ *     dq_acc += tau dS K,   dk_acc += tau dS^T Q,   dv_acc += P^T dout
+ * with P = exp(tau q.k - lse) and dS = P * (dout V^T - D).  dk_acc and
+ * dv_acc belong to the visiting block and travel with it; dq_acc stays.
+ *   q, dout       [batch, c, d] of `dtype` (the query block).
+ *   k, v          [batch, c, d] of `dtype` (the visiting block).
+ *   lse           [batch, c] fp32 (the forward's, natural log).
+ *   rowterms      [2 * batch * c] fp32 from ra_backward_rowterms.
+ *   dq_acc        [batch, c, d] fp32, accumulated; dk_acc, dv_acc likewise.
+ *   causal        0: every key visible; 1: the block is the query block's
+ *                 own (key r visible to query r' iff r <= r', the diagonal
+ *                 block of a contiguous causal ring).
+ * Size rules as ra_backward with N = c and P = 1 (bf16: d in {64, 128},
+ * c % 128 == 0, 16-byte aligned tensors and accumulators).  Accumulators
+ * are read and written in place: calls that overlap on the GPU and share an
+ * accumulator race.
+ * Errors: as ra_backward; RA_ERR_INVALID_ARG for a NULL pointer or causal
+ * not 0 or 1.
+ */
+RA_API ra_status ra_backward_block(const void* q, const void* k, const void* v, const void* dout,
+                                   const float* lse, const float* rowterms, float* dq_acc,
+                                   float* dk_acc, float* dv_acc, int64_t batch, int64_t c,
+                                   int32_t d, int32_t causal, ra_dtype dtype,
+                                   ra_stream_t stream);
+
+/*
  * ra_state_init -- set a state to empty: m = -inf, l = 0, o = 0 ("Ring
  * Attention: the math", section "Accumulation math, step by step": "state = (m
  * = -inf, l = 0, o = 0)").

@@ -21,7 +21,8 @@ from ._native import RA_BF16, RA_F32, RA_MAX_PARTIALS, RaStateC
 __all__ = ["RaError", "RaState", "ra_forward", "ra_forward_causal", "ra_forward_partial",
            "ra_forward_partial_causal", "ra_forward_split", "ra_forward_split_workspace_bytes",
            "ra_forward_split_segments", "ra_forward_host", "ra_forward_host_workspace_bytes",
-           "ra_backward", "ra_backward_causal", "ra_state_init",
+           "ra_backward", "ra_backward_causal", "ra_backward_rowterms", "ra_backward_block",
+           "ra_state_init",
            "ra_fold", "ra_merge",
            "ra_last_device_status", "ra_watchdog_config", "new_state", "library_path"]
 
@@ -262,6 +263,41 @@ def ra_backward_causal(q, k, v, out, dout, lse, P: int, layout: str = "contiguou
     """Gradients for ra_forward_causal (same mask and layout)."""
     return ra_backward(q, k, v, out, dout, lse, P, workspace=workspace, stream=stream,
                        causal=layout)
+
+
+def ra_backward_rowterms(out, dout, lse, workspace=None, stream=None):
+    """Row terms (D, -lse log2 e) of a query block: out, dout [..., d] of one
+    dtype, lse of their rows; returns the fp32 workspace [2 * rows]."""
+    d = out.shape[-1]
+    rows = out.numel() // d
+    if dout.shape != out.shape or dout.dtype != out.dtype or lse.numel() != rows:
+        raise ValueError("out, dout must match and lse must have one value per row")
+    if workspace is None:
+        workspace = torch.empty(2 * rows, device=out.device, dtype=torch.float32)
+    code = _native.lib().ra_backward_rowterms(_ptr(out), _ptr(dout), _ptr(lse), rows, d,
+                                              _dtype_code(out), _ptr(workspace), _stream(stream))
+    _check(code, "ra_backward_rowterms")
+    return workspace
+
+
+def ra_backward_block(q, k, v, dout, lse, rowterms, dq_acc, dk_acc, dv_acc, causal=False,
+                      stream=None):
+    """One ring-backward step: the query block (q, dout [batch, c, d], lse
+    [batch, c], rowterms) against the visiting block (k, v), added into the
+    fp32 accumulators dq_acc (query block) and dk_acc, dv_acc (visiting
+    block).  causal=True for the query block's own block (diagonal mask)."""
+    batch, c, d = q.shape
+    for t in (k, v, dout):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError("q, k, v, dout must share shape and dtype")
+    for t in (dq_acc, dk_acc, dv_acc):
+        if t.shape != q.shape or t.dtype != torch.float32:
+            raise ValueError("accumulators are fp32 tensors of q's shape")
+    code = _native.lib().ra_backward_block(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(rowterms), _ptr(dq_acc),
+        _ptr(dk_acc), _ptr(dv_acc), batch, c, d, 1 if causal else 0, _dtype_code(q),
+        _stream(stream))
+    _check(code, "ra_backward_block")
 
 
 def ra_state_init(state: RaState, stream=None) -> RaState:

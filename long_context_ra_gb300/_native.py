@@ -51,6 +51,9 @@ PROTOTYPES = {
                            _I32, _P]),
     "ra_backward_causal": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I64, _I32,
                                   _I32, _I32, _I32, _P]),
+    "ra_backward_rowterms": (_I32, [_P, _P, _P, _I64, _I32, _I32, _P, _P]),
+    "ra_backward_block": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I32,
+                                 _P]),
     "ra_state_init": (_I32, [_SP, _P]),
     "ra_fold": (_I32, [_SP, _P, _P, _P, _I64, _I64, _I32, _P]),
     "ra_merge": (_I32, [_SP, _I32, _P, _P, _I32, _P]),

@@ -455,10 +455,93 @@ ra_status backward_impl(const void* q, const void* k, const void* v, const void*
   return launched(launch_backward_sm103(a, tq, tk, tv, tdo, s));
 }
 
+// One step of the ring backward: query block (q, dout, row terms) against
+// one visiting block (k, v), adding into fp32 accumulators.  P = 1 over a
+// block of c rows; `causal` masks later keys within the block (the diagonal
+// block of a contiguous ring).
+ra_status backward_block_impl(const void* q, const void* k, const void* v, const void* dout,
+                              const float* lse, const float* rowterms, float* dq_acc,
+                              float* dk_acc, float* dv_acc, int64_t batch, int64_t c, int32_t d,
+                              int32_t causal, ra_dtype dtype, ra_stream_t stream) {
+  if (batch < 0 || batch > INT32_MAX || causal < 0 || causal > 1) return RA_ERR_INVALID_ARG;
+  FoldArgs f;
+  ra_status st = check_attention(q, k, v, 1, static_cast<int32_t>(batch), c, d, 1, dtype, &f);
+  if (st != RA_OK) return st;
+  if (causal && (st = check_causal(c, 1, RA_LAYOUT_CONTIGUOUS, dtype, &f)) != RA_OK) return st;
+  const int64_t rows = f.slices * f.nq;
+  if (rows == 0) return RA_OK;
+  if (!dout || !lse || !rowterms || !dq_acc || !dk_acc || !dv_acc) return RA_ERR_INVALID_ARG;
+  const uintptr_t al = dtype == RA_BF16 ? 16 : 4;
+  if (!aligned(dout, al) || !aligned(lse, 4) || !aligned(rowterms, 16) || !aligned(dq_acc, al) ||
+      !aligned(dk_acc, al) || !aligned(dv_acc, al))
+    return RA_ERR_MISALIGNED;
+  DeviceInfo di;
+  if ((st = current_device(&di)) != RA_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  BackwardArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.dout = dout;
+  a.lse = lse;
+  a.delta = rowterms;
+  a.nl = rowterms + rows;
+  a.dq = dq_acc;
+  a.dk = dk_acc;
+  a.dv = dv_acc;
+  a.slices = f.slices;
+  a.N = c;
+  a.d = d;
+  a.P = 1;
+  a.causal = f.causal;
+  a.layout = kContiguous;
+  a.tau = f.tau;
+  a.scale_log2 = f.scale_log2;
+  a.status = di.status;
+  a.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  a.accumulate = 1;
+  if (dtype == RA_F32) return launched(launch_backward_f32(a, s));
+  if ((st = get_encoder()) != RA_OK) return st;
+  CUtensorMap tq, tk, tv, tdo;
+  const void* src[4] = {q, k, v, dout};
+  CUtensorMap* maps[4] = {&tq, &tk, &tv, &tdo};
+  for (int x = 0; x < 4; ++x)
+    if ((st = make_map(maps[x], src[x], rows, d)) != RA_OK) return st;
+  return launched(launch_backward_sm103(a, tq, tk, tv, tdo, s));
+}
+
 }  // namespace
 }  // namespace ra
 
 extern "C" {
+
+RA_API ra_status ra_backward_rowterms(const void* out, const void* dout, const float* lse,
+                                      int64_t rows, int32_t d, ra_dtype dtype, float* workspace,
+                                      ra_stream_t stream) {
+  if (rows < 0 || d < 1 || (dtype != RA_F32 && dtype != RA_BF16)) return RA_ERR_INVALID_ARG;
+  if (rows > kMaxRows) return RA_ERR_UNSUPPORTED;
+  if (rows == 0) return RA_OK;
+  if (!out || !dout || !lse || !workspace) return RA_ERR_INVALID_ARG;
+  const uintptr_t al = dtype == RA_BF16 ? 2 : 4;
+  if (!aligned(out, al) || !aligned(dout, al) || !aligned(lse, 4) || !aligned(workspace, 16))
+    return RA_ERR_MISALIGNED;
+  DeviceInfo di;
+  ra_status st = current_device(&di);
+  if (st != RA_OK) return st;
+  // one block of `rows` rows: block-major order is row order
+  return launched(launch_delta(out, dout, lse, workspace, workspace + rows, rows, d, rows, 1,
+                               kContiguous, dtype == RA_BF16,
+                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+RA_API ra_status ra_backward_block(const void* q, const void* k, const void* v, const void* dout,
+                                   const float* lse, const float* rowterms, float* dq_acc,
+                                   float* dk_acc, float* dv_acc, int64_t batch, int64_t c,
+                                   int32_t d, int32_t causal, ra_dtype dtype,
+                                   ra_stream_t stream) {
+  return backward_block_impl(q, k, v, dout, lse, rowterms, dq_acc, dk_acc, dv_acc, batch, c, d,
+                             causal, dtype, stream);
+}
 
 RA_API ra_status ra_backward(const void* q, const void* k, const void* v, const void* out,
                              const void* dout, const float* lse, void* dq, void* dk, void* dv,

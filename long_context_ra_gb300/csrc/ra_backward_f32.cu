@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kWarps * 32) dq_f32_kernel(const BackwardArgs 
 #pragma unroll
   for (int x = 0; x < DV; ++x) {
     const int e = lane + 32 * x;
-    if (e < d) dq[rid * d + e] = acc[x] * a.tau;
+    if (e < d) dq[rid * d + e] = (a.accumulate ? dq[rid * d + e] : 0.f) + acc[x] * a.tau;
   }
 }
 
@@ -237,8 +237,8 @@ __global__ void __launch_bounds__(kWarps * 32) dkv_f32_kernel(const BackwardArgs
   for (int x = 0; x < DV; ++x) {
     const int e = lane + 32 * x;
     if (e < d) {
-      dk[rid * d + e] = gk[x] * a.tau;
-      dv[rid * d + e] = gv[x];
+      dk[rid * d + e] = (a.accumulate ? dk[rid * d + e] : 0.f) + gk[x] * a.tau;
+      dv[rid * d + e] = (a.accumulate ? dv[rid * d + e] : 0.f) + gv[x];
     }
   }
 }

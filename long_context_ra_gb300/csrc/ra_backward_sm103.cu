@@ -313,6 +313,27 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, uint16_t* dst, fl
   }
 }
 
+// Add one TMEM row segment of 32 fp32 columns, times `scale`, into an fp32
+// accumulator row in global memory (16-byte aligned).
+__device__ __forceinline__ void add_row_f32(uint32_t taddr, float* dst, float scale) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+  float4* d4 = reinterpret_cast<float4*>(dst);
+  float4 x[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) x[e] = d4[e];
+  tmem_ld_wait();
+  reg_fence(r, 32);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    x[e].x = fmaf(__uint_as_float(r[4 * e + 0]), scale, x[e].x);
+    x[e].y = fmaf(__uint_as_float(r[4 * e + 1]), scale, x[e].y);
+    x[e].z = fmaf(__uint_as_float(r[4 * e + 2]), scale, x[e].z);
+    x[e].w = fmaf(__uint_as_float(r[4 * e + 3]), scale, x[e].w);
+    d4[e] = x[e];
+  }
+}
+
 // ---------------------------------------------------------------------------
 // dK, dV: one key tile per CTA
 // ---------------------------------------------------------------------------
@@ -592,12 +613,23 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
     if (ok && wait_warp(o_full, 0, ab)) {
       tc_fence_after();
       const int64_t r = slice * a.N + walk.pos(j, static_cast<int64_t>(kt) * kBM + row);
-      uint16_t* dv = static_cast<uint16_t*>(a.dv) + r * D;
-      uint16_t* dk = static_cast<uint16_t*>(a.dk) + r * D;
+      if (a.accumulate) {
+        // block mode: add into the fp32 accumulators that travel with the block
+        float* dv = static_cast<float*>(a.dv) + r * D;
+        float* dk = static_cast<float*>(a.dk) + r * D;
 #pragma unroll
-      for (int cc = 32 * wg; cc < D; cc += 32 * G) {
-        store_row_bf16(tdV + lane_off + cc, dv + cc, 1.f);
-        store_row_bf16(tdK + lane_off + cc, dk + cc, a.tau);
+        for (int cc = 32 * wg; cc < D; cc += 32 * G) {
+          add_row_f32(tdV + lane_off + cc, dv + cc, 1.f);
+          add_row_f32(tdK + lane_off + cc, dk + cc, a.tau);
+        }
+      } else {
+        uint16_t* dv = static_cast<uint16_t*>(a.dv) + r * D;
+        uint16_t* dk = static_cast<uint16_t*>(a.dk) + r * D;
+#pragma unroll
+        for (int cc = 32 * wg; cc < D; cc += 32 * G) {
+          store_row_bf16(tdV + lane_off + cc, dv + cc, 1.f);
+          store_row_bf16(tdK + lane_off + cc, dk + cc, a.tau);
+        }
       }
     }
   }
@@ -904,10 +936,16 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
     }
     if (ok && wait_warp(o_full, 0, ab)) {
       tc_fence_after();
-      uint16_t* dq = static_cast<uint16_t*>(a.dq) + r * D;
+      if (a.accumulate) {
+        float* dq = static_cast<float*>(a.dq) + r * D;
 #pragma unroll
-      for (int cc = 32 * wg; cc < D; cc += 32 * G)
-        store_row_bf16(tdQ + lane_off + cc, dq + cc, a.tau);
+        for (int cc = 32 * wg; cc < D; cc += 32 * G) add_row_f32(tdQ + lane_off + cc, dq + cc, a.tau);
+      } else {
+        uint16_t* dq = static_cast<uint16_t*>(a.dq) + r * D;
+#pragma unroll
+        for (int cc = 32 * wg; cc < D; cc += 32 * G)
+          store_row_bf16(tdQ + lane_off + cc, dq + cc, a.tau);
+      }
     }
   }
 

@@ -207,3 +207,93 @@ def _ring_forward_zigzag(q, k, v, group, ops: RingOps):
     out = torch.stack(outs, dim=1).reshape(B, H, c, d)
     lse = torch.stack(lses, dim=1).reshape(B, H, c)
     return out, lse
+
+
+@dataclass
+class RingBackwardOps:
+    """The operations of the ring backward.
+
+    rowterms(out, dout, lse) -> rt          per-query terms of a block
+                                            (out, dout [bh, c, d], lse [bh, c])
+    block(q, k, v, dout, lse, rt, dq, dk, dv, causal)
+                                            add one visiting block's gradients
+                                            into the fp32 accumulators
+    finish(acc, dtype) -> tensor            an accumulator in the output dtype
+    """
+
+    rowterms: Callable[[torch.Tensor, torch.Tensor, torch.Tensor], Any]
+    block: Callable[..., None]
+    finish: Callable[[torch.Tensor, torch.dtype], torch.Tensor]
+
+
+def library_backward_ops(stream=None) -> RingBackwardOps:
+    """The CUDA library's kernels (ra_backward_rowterms, ra_backward_block)."""
+    from . import ra_backward_block, ra_backward_rowterms
+
+    def _rowterms(out, dout, lse):
+        return ra_backward_rowterms(out, dout, lse, stream=stream)
+
+    def _block(q, k, v, dout, lse, rt, dq, dk, dv, causal):
+        ra_backward_block(q, k, v, dout, lse, rt, dq, dk, dv, causal=causal, stream=stream)
+
+    def _finish(acc, dtype):
+        return acc.to(dtype)
+
+    return RingBackwardOps(_rowterms, _block, _finish)
+
+
+def ring_backward(q, k, v, out, dout, lse, group=None, ops: RingBackwardOps | None = None,
+                  causal: bool = False):
+    """Gradients (dq, dk, dv) of this rank's block for L = sum(dout * out),
+    on the same ring as ring_forward (contiguous split): at step t the rank
+    meets block (i - t) mod P, adds dQ of its own queries into its
+    accumulator and the visiting block's dK, dV into the accumulators that
+    travel with that block ("Ring attention, explained", step 6).  The K/V
+    of the next block are received while the current one is processed; its
+    accumulators follow once the rank's contribution is in.  After P steps
+    every block is back on its rank with complete dK, dV.
+
+    q, k, v, out, dout: this rank's block [B, H, c, d]; lse [B, H, c] (from
+    ring_forward).  Returns dq, dk, dv [B, H, c, d] in q's dtype."""
+    if ops is None:
+        ops = library_backward_ops()
+    world, rank, send_to, recv_from = _neighbours(group)
+    B, H, c, d = q.shape
+    for t in (k, v, out, dout):
+        if t.shape != q.shape:
+            raise ValueError("q, k, v, out, dout blocks must share one shape")
+    bh = B * H
+    q3, dout3 = q.reshape(bh, c, d).contiguous(), dout.reshape(bh, c, d).contiguous()
+    lse2 = lse.reshape(bh, c).contiguous()
+    rt = ops.rowterms(out.reshape(bh, c, d).contiguous(), dout3, lse2)
+    # fp32 accumulators (fp64 when the blocks are fp64, as on CPU ranks)
+    f32 = dict(dtype=torch.float64 if q.dtype == torch.float64 else torch.float32,
+               device=q.device)
+    dq = torch.zeros(bh, c, d, **f32)
+    kv = [k.reshape(bh, c, d).contiguous(), v.reshape(bh, c, d).contiguous()]
+    kv_recv = [[torch.empty_like(kv[0]), torch.empty_like(kv[1])]
+               for _ in range(min(world - 1, 2))]
+    acc = [torch.zeros(bh, c, d, **f32), torch.zeros(bh, c, d, **f32)]  # dK, dV of the held block
+    acc_recv = [[torch.empty_like(acc[0]), torch.empty_like(acc[1])] for _ in range(2)]
+    for t in range(world):
+        j = ring_block(rank, t, world)
+        kv_next = kv_recv[t % 2] if t + 1 < world else None
+        reqs = _exchange(kv, kv_next, send_to, recv_from, group) if t + 1 < world else []
+        if not causal or j < rank:
+            ops.block(q3, kv[0], kv[1], dout3, lse2, rt, dq, acc[0], acc[1], False)
+        elif j == rank:
+            ops.block(q3, kv[0], kv[1], dout3, lse2, rt, dq, acc[0], acc[1], True)
+        # causal and j > rank: no query here sees block j; it passes through
+        if world > 1:
+            # the block's accumulators follow it to the next rank (after the
+            # contribution above); after P hops they are home
+            acc_next = acc_recv[t % 2]
+            reqs += _exchange(acc, acc_next, send_to, recv_from, group)
+        for r in reqs:
+            r.wait()
+        if world > 1:
+            acc = acc_next
+        kv = kv_next
+    shape = (B, H, c, d)
+    return (ops.finish(dq, q.dtype).reshape(shape), ops.finish(acc[0], q.dtype).reshape(shape),
+            ops.finish(acc[1], q.dtype).reshape(shape))

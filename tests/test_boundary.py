@@ -213,3 +213,24 @@ def test_largest_sizes(L):
         _native.RA_ERR_ARCH
     assert L.ra_forward_causal(A, A, A, A, A, 1, 1, 1025 * 128, 128, 1025, 0, BF16, None) == \
         _native.RA_ERR_UNSUPPORTED
+
+
+def test_backward_block_validation(L):
+    def fb(q=A, dq=A, rt=A, batch=2, c=256, d=64, causal=0, dt=BF16):
+        return L.ra_backward_block(q, A, A, A, A, rt, dq, A, A, batch, c, d, causal, dt, None)
+    assert fb(q=None) == _native.RA_ERR_INVALID_ARG
+    assert fb(rt=None) == _native.RA_ERR_INVALID_ARG
+    assert fb(causal=2) == _native.RA_ERR_INVALID_ARG
+    assert fb(batch=-1) == _native.RA_ERR_INVALID_ARG
+    assert fb(c=200) == _native.RA_ERR_UNSUPPORTED          # bf16 block of 200 rows
+    assert fb(d=96) == _native.RA_ERR_UNSUPPORTED           # bf16 head dim
+    assert fb(dq=A + 4) == _native.RA_ERR_MISALIGNED        # fp32 accumulator, 16 bytes on bf16
+    assert fb(batch=0, q=None, dq=None, rt=None) == _native.RA_OK
+    assert fb() == _native.RA_ERR_ARCH                      # valid; no device here
+    assert fb(c=24, d=40, dt=F32) == _native.RA_ERR_ARCH    # fp32: any block length
+    rt = L.ra_backward_rowterms
+    assert rt(A, A, A, 128, 64, BF16, None, None) == _native.RA_ERR_INVALID_ARG
+    assert rt(A, A, A, -1, 64, BF16, A, None) == _native.RA_ERR_INVALID_ARG
+    assert rt(A, A, A, 0, 64, BF16, None, None) == _native.RA_OK
+    assert rt(A, A, A, 128, 64, BF16, A + 4, None) == _native.RA_ERR_MISALIGNED
+    assert rt(A, A, A, 128, 64, BF16, A, None) == _native.RA_ERR_ARCH

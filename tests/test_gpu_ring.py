@@ -30,9 +30,12 @@ def group():
         port = s.getsockname()[1]
     os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
     os.environ["MASTER_PORT"] = str(port)
-    dist.init_process_group("gloo", rank=0, world_size=1)
+    mine = not dist.is_initialized()
+    if mine:
+        dist.init_process_group("gloo", rank=0, world_size=1)
     yield None
-    dist.destroy_process_group()
+    if mine:
+        dist.destroy_process_group()
 
 
 @pytest.mark.parametrize("causal", [False, True])
