@@ -243,7 +243,7 @@ def library_backward_ops(stream=None) -> RingBackwardOps:
 
 
 def ring_backward(q, k, v, out, dout, lse, group=None, ops: RingBackwardOps | None = None,
-                  causal: bool = False):
+                  causal: bool = False, layout: str = "contiguous"):
     """Gradients (dq, dk, dv) of this rank's block for L = sum(dout * out),
     on the same ring as ring_forward (contiguous split): at step t the rank
     meets block (i - t) mod P, adds dQ of its own queries into its
@@ -254,9 +254,17 @@ def ring_backward(q, k, v, out, dout, lse, group=None, ops: RingBackwardOps | No
     every block is back on its rank with complete dK, dV.
 
     q, k, v, out, dout: this rank's block [B, H, c, d]; lse [B, H, c] (from
-    ring_forward).  Returns dq, dk, dv [B, H, c, d] in q's dtype."""
+    ring_forward with the same causal and layout).  layout "zigzag" (causal
+    only): the block holds chunks i and 2P-1-i, as in ring_forward.
+    Returns dq, dk, dv [B, H, c, d] in q's dtype."""
     if ops is None:
         ops = library_backward_ops()
+    if layout not in ("contiguous", "zigzag"):
+        raise ValueError(f"unknown layout {layout!r}")
+    if layout == "zigzag":
+        if not causal:
+            raise ValueError("the zigzag split only matters under the causal mask")
+        return _ring_backward_zigzag(q, k, v, out, dout, lse, group, ops)
     world, rank, send_to, recv_from = _neighbours(group)
     B, H, c, d = q.shape
     for t in (k, v, out, dout):
@@ -297,3 +305,61 @@ def ring_backward(q, k, v, out, dout, lse, group=None, ops: RingBackwardOps | No
     shape = (B, H, c, d)
     return (ops.finish(dq, q.dtype).reshape(shape), ops.finish(acc[0], q.dtype).reshape(shape),
             ops.finish(acc[1], q.dtype).reshape(shape))
+
+
+def _ring_backward_zigzag(q, k, v, out, dout, lse, group, ops: RingBackwardOps):
+    """The causal ring backward over the zigzag split: the pieces of
+    _ring_forward_zigzag, each a block step on chunks of c/2 rows, with dQ
+    accumulated per query chunk and dK, dV per chunk of the visiting block
+    (the two chunks travel together, [2, B*H, c/2, d])."""
+    world, rank, send_to, recv_from = _neighbours(group)
+    B, H, c, d = q.shape
+    for t in (k, v, out, dout):
+        if t.shape != q.shape:
+            raise ValueError("q, k, v, out, dout blocks must share one shape")
+    if c % 2:
+        raise ValueError("the zigzag split needs an even block length")
+    bh, h = B * H, c // 2
+    halves = lambda t: t.reshape(bh, 2, h, -1).transpose(0, 1).contiguous()  # [2, bh, h, .]
+    qh, gh = halves(q), halves(dout)
+    lh = halves(lse.reshape(bh, c, 1)).reshape(2, bh, h)
+    oh = halves(out)
+    rt = [ops.rowterms(oh[x], gh[x], lh[x]) for x in range(2)]
+    f32 = dict(dtype=torch.float64 if q.dtype == torch.float64 else torch.float32,
+               device=q.device)
+    dq = torch.zeros(2, bh, h, d, **f32)
+    kv = [halves(k), halves(v)]
+    kv_recv = [[torch.empty_like(kv[0]), torch.empty_like(kv[1])]
+               for _ in range(min(world - 1, 2))]
+    acc = [torch.zeros(2, bh, h, d, **f32), torch.zeros(2, bh, h, d, **f32)]  # dK, dV
+    acc_recv = [[torch.empty_like(acc[0]), torch.empty_like(acc[1])] for _ in range(2)]
+
+    def step(x, y, causal):
+        # query chunk x of this rank against chunk y of the held block
+        ops.block(qh[x], kv[0][y], kv[1][y], gh[x], lh[x], rt[x], dq[x], acc[0][y], acc[1][y],
+                  causal)
+
+    for t in range(world):
+        j = ring_block(rank, t, world)
+        kv_next = kv_recv[t % 2] if t + 1 < world else None
+        reqs = _exchange(kv, kv_next, send_to, recv_from, group) if t + 1 < world else []
+        if j == rank:
+            step(0, 0, True)
+            step(1, 0, False)
+            step(1, 1, True)
+        elif j < rank:
+            step(0, 0, False)
+            step(1, 0, False)
+        else:
+            step(1, 0, False)
+            step(1, 1, False)
+        if world > 1:
+            acc_next = acc_recv[t % 2]
+            reqs += _exchange(acc, acc_next, send_to, recv_from, group)
+        for r in reqs:
+            r.wait()
+        if world > 1:
+            acc = acc_next
+        kv = kv_next
+    whole = lambda a: ops.finish(a, q.dtype).transpose(0, 1).reshape(B, H, c, d)
+    return whole(dq), whole(acc[0]), whole(acc[1])

@@ -107,12 +107,13 @@ def group():
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("causal", [False, True])
-def test_one_rank_ring_backward_on_the_gpu(O, group, causal):
+@pytest.mark.parametrize("causal,layout", [(False, "contiguous"), (True, "contiguous"),
+                                           (True, "zigzag")])
+def test_one_rank_ring_backward_on_the_gpu(O, group, causal, layout):
     B, H, N, d = 1, 2, 1024, 128
     q, k, v, dout = (rnd((B, H, N, d), 850 + s, torch.bfloat16) for s in range(4))
-    out, lse = ring_forward(q, k, v, causal=causal)
-    dq, dk, dv = ring_backward(q, k, v, out, dout, lse, causal=causal)
+    out, lse = ring_forward(q, k, v, causal=causal, layout=layout)
+    dq, dk, dv = ring_backward(q, k, v, out, dout, lse, causal=causal, layout=layout)
     torch.cuda.synchronize()
     wq, wk, wv = oracle_grads(O, q, k, v, out, dout, lse, 1, causal)
     for name, got, want in (("dq", dq, wq), ("dk", dk, wk), ("dv", dv, wv)):

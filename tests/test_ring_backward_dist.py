@@ -5,8 +5,8 @@ queries against the block it holds.  The per-block gradient here is the
 plain formula in fp64 numpy (on GPUs it is the library's kernel), so the
 test checks the orchestration: each block meets every query block once,
 its accumulators come home complete, the causal variant skips and masks
-the right blocks, and dq, dk, dv equal the oracle's ring backward over the
-whole sequence."""
+the right blocks (contiguous and zigzag splits), and dq, dk, dv equal the
+oracle's ring backward over the whole sequence."""
 import os
 import socket
 
@@ -37,7 +37,8 @@ def _numpy_ops(calls):
         qn, kn, vn, gn = (x.numpy() for x in (q, k, v, dout))
         s = np.einsum("bqe,bke->bqk", qn, kn) * tau
         if causal:
-            s = np.where(np.tril(np.ones((C, C), bool)), s, -np.inf)
+            n = qn.shape[1]
+            s = np.where(np.tril(np.ones((n, n), bool)), s, -np.inf)
         p = np.exp(s - lse.numpy()[:, :, None])
         dp = np.einsum("bqe,bke->bqk", gn, vn)
         ds = p * (dp - rt[:, :, None])
@@ -87,6 +88,21 @@ def _rank_main(rank, world, port, results):
                          if torch.equal(kk.reshape(B, H, C, D), k[:, :, j * C:(j + 1) * C]))
                     for kk, _ in calls]
             res[causal] = (errs, seen, [c for _, c in calls])
+        # zigzag: rank i holds chunks i and 2P-1-i of 2P chunks of C/2 tokens
+        h = C // 2
+        pos = list(range(rank * h, rank * h + h)) + \
+            list(range((2 * world - 1 - rank) * h, (2 * world - 1 - rank) * h + h))
+        out, lse = O.dense(arr(q), arr(k), arr(v), causal=True)
+        out = torch.from_numpy(out).reshape(B, H, N, D)
+        lse = torch.from_numpy(lse).reshape(B, H, N)
+        zz = lambda t: t[:, :, pos].contiguous()
+        calls = []
+        dq, dk, dv = ring_backward(zz(q), zz(k), zz(v), zz(out), zz(dout), zz(lse),
+                                   ops=_numpy_ops(calls), causal=True, layout="zigzag")
+        wq, wk, wv = O.backward(arr(q), arr(k), arr(v), out.reshape(bh, N, D).numpy(),
+                                arr(dout), lse.reshape(bh, N).numpy(), world, causal=True)
+        res["zigzag"] = [float(np.abs(got.reshape(bh, C, D).numpy() - want[:, pos]).max())
+                         for got, want in ((dq, wq), (dk, wk), (dv, wv))]
         results[rank] = res
     finally:
         dist.destroy_process_group()
@@ -102,6 +118,8 @@ def test_ring_backward_over_gloo_equals_the_oracle(world):
         results = dict(results)
     assert sorted(results) == list(range(world))
     for rank, res in results.items():
+        zz = res.pop("zigzag")
+        assert max(zz) <= 1e-12, (rank, "zigzag", zz)
         for causal, (errs, seen, masked) in res.items():
             assert max(errs) <= 1e-12, (rank, causal, errs)
             want = [(rank - t) % world for t in range(world)]
