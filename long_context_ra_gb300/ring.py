@@ -15,9 +15,9 @@ On GPUs the exchange is torch.distributed point-to-point (NCCL) into a
 second, local receive buffer, so the fold kernel only ever reads this
 device's memory; the fold, the causal diagonal block and the final
 normalisation are the library's kernels (ra_fold, ra_forward_partial_causal,
-ra_merge).  The orchestration itself is device-agnostic: `ops` supplies the
-three operations, so the same loop runs on CPU ranks (gloo) with other
-operations in tests.
+ra_merge; the backward's ra_backward_rowterms and ra_backward_block).  The
+orchestration itself is device-agnostic: `ops` supplies the arithmetic, so
+the same loops run on CPU ranks (gloo) with other operations in tests.
 
 Causal attention (section "Causal masking, load balance, and other
 wrinkles"; "Ring attention, explained", section "The causal-mask catch"):
@@ -42,7 +42,7 @@ import torch.distributed as dist
 
 @dataclass
 class RingOps:
-    """The three operations the ring needs.
+    """The operations the forward ring needs.
 
     new_state(rows, d, like)            an empty state (m = -inf, l = 0, o = 0)
     fold(state, q, k, v, batch)         fold a visiting block: q [batch, rq, d],
