@@ -162,19 +162,12 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 // p = exp2(s * sl2 + neg) for the 128 scores of this row, two per FMA; p is
 // rounded to bf16 pairs and written over the first 64 columns of S (tS),
 // where the P V product reads it.  Returns the row sum of p (four
-// independent pair sums).  kSecondHalfInFlight: the loads of scores 64..127
-// were issued but not waited for; they land while the first half is
-// computed, and are waited for before the second.
-template <bool kSecondHalfInFlight>
-__device__ __forceinline__ float exp_store(uint32_t (&s)[kBN], uint64_t scale2, uint64_t neg2,
-                                           uint32_t tS) {
+// independent pair sums).
+__device__ __forceinline__ float exp_store(const uint32_t (&s)[kBN], uint64_t scale2,
+                                           uint64_t neg2, uint32_t tS) {
   uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
-    if (kSecondHalfInFlight && half == 1) {
-      tmem_ld_wait();
-      reg_fence(s + 64, 64);
-    }
     uint32_t pk[32];
 #pragma unroll
     for (int jj = 0; jj < 32; ++jj) {
@@ -481,23 +474,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         uint32_t s[kBN];
-        // Fast path (the forward, once the reference is set; see below): its
-        // second half of scores is still loading while the first is used.
-        const bool fast = !kCausal && a.mode == kForward &&
-                          __all_sync(0xffffffffu, m_ref != -INFINITY);
-        tmem_ld32(tS, s);
-        tmem_ld32(tS + 32, s + 32);
-        if (fast) {
-          tmem_ld_wait();
-          reg_fence(s, 64);
-          tmem_ld32(tS + 64, s + 64);
-          tmem_ld32(tS + 96, s + 96);
-        } else {
-          tmem_ld32(tS + 64, s + 64);
-          tmem_ld32(tS + 96, s + 96);
-          tmem_ld_wait();
-          reg_fence(s, kBN);
-        }
+#pragma unroll
+        for (int c = 0; c < kBN; c += 32) tmem_ld32(tS + c, s + c);
+        tmem_ld_wait();
+        reg_fence(s, kBN);
         if (kCausal) {
           // keys after the query's own position take no part (score -inf)
           const int4 ent = steps[ts];
@@ -524,8 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // exact.  The partial and fold modes always take the exact path,
         // since they report the true running max.
         bool redo = true;
-        if (fast) {
-          const float lt = exp_store<true>(s, scale2, pack_f32x2(-m_ref, -m_ref), tS);
+        if (a.mode == kForward && __all_sync(0xffffffffu, m_ref != -INFINITY)) {
+          const float lt = exp_store(s, scale2, pack_f32x2(-m_ref, -m_ref), tS);
           if (!__any_sync(0xffffffffu, lt > kFastSumBound)) {
             l += lt;
             redo = false;
@@ -572,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // a row that has seen no visible key yet keeps m_ref = -inf; its
           // masked scores must still give p = 0 rather than NaN
           const float neg = (kCausal && m_ref == -INFINITY) ? 0.f : -m_ref;
-          l += exp_store<false>(s, scale2, pack_f32x2(neg, neg), tS);
+          l += exp_store(s, scale2, pack_f32x2(neg, neg), tS);
         }
         tmem_st_wait();
         tc_fence_before();
