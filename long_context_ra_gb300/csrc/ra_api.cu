@@ -11,6 +11,7 @@
 
 #include "ra.h"
 #include "ra_internal.h"
+#include "ra_trace.h"
 
 namespace ra {
 namespace {
@@ -337,6 +338,7 @@ extern "C" {
 RA_API ra_status ra_forward(const void* q, const void* k, const void* v, void* out, float* lse,
                             int32_t B, int32_t H, int64_t N, int32_t d, int32_t P, ra_dtype dtype,
                             ra_stream_t stream) {
+  RA_TRACE("ra_forward");
   return forward_impl(q, k, v, out, lse, B, H, N, d, P, false, RA_LAYOUT_CONTIGUOUS, dtype,
                       stream);
 }
@@ -345,6 +347,7 @@ RA_API ra_status ra_forward_causal(const void* q, const void* k, const void* v, 
                                    float* lse, int32_t B, int32_t H, int64_t N, int32_t d,
                                    int32_t P, ra_layout layout, ra_dtype dtype,
                                    ra_stream_t stream) {
+  RA_TRACE("ra_forward_causal");
   return forward_impl(q, k, v, out, lse, B, H, N, d, P, true, layout, dtype, stream);
 }
 
@@ -352,6 +355,7 @@ RA_API ra_status ra_forward_partial(const void* q, const void* k, const void* v,
                                     int32_t H, int64_t N, int32_t d, int32_t P, int32_t G,
                                     const ra_state* partials, ra_dtype dtype,
                                     ra_stream_t stream) {
+  RA_TRACE("ra_forward_partial");
   return partial_impl(q, k, v, B, H, N, d, P, G, partials, false, RA_LAYOUT_CONTIGUOUS, dtype,
                       stream);
 }
@@ -360,6 +364,7 @@ RA_API ra_status ra_forward_partial_causal(const void* q, const void* k, const v
                                            int32_t B, int32_t H, int64_t N, int32_t d, int32_t P,
                                            int32_t G, const ra_state* partials, ra_layout layout,
                                            ra_dtype dtype, ra_stream_t stream) {
+  RA_TRACE("ra_forward_partial_causal");
   return partial_impl(q, k, v, B, H, N, d, P, G, partials, true, layout, dtype, stream);
 }
 
@@ -391,6 +396,7 @@ RA_API ra_status ra_forward_split(const void* q, const void* k, const void* v, v
                                   float* lse, int32_t B, int32_t H, int64_t N, int32_t d,
                                   int32_t P, int32_t G, void* workspace, int64_t workspace_bytes,
                                   ra_dtype dtype, ra_stream_t stream) {
+  RA_TRACE("ra_forward_split");
   return split_forward(q, k, v, out, lse, B, H, N, d, P, G, workspace, workspace_bytes, dtype,
                        reinterpret_cast<cudaStream_t>(stream));
 }
@@ -518,6 +524,7 @@ extern "C" {
 RA_API ra_status ra_backward_rowterms(const void* out, const void* dout, const float* lse,
                                       int64_t rows, int32_t d, ra_dtype dtype, float* workspace,
                                       ra_stream_t stream) {
+  RA_TRACE("ra_backward_rowterms");
   if (rows < 0 || d < 1 || (dtype != RA_F32 && dtype != RA_BF16)) return RA_ERR_INVALID_ARG;
   if (rows > kMaxRows) return RA_ERR_UNSUPPORTED;
   if (rows == 0) return RA_OK;
@@ -539,6 +546,7 @@ RA_API ra_status ra_backward_block(const void* q, const void* k, const void* v, 
                                    float* dk_acc, float* dv_acc, int64_t batch, int64_t c,
                                    int32_t d, int32_t causal, ra_dtype dtype,
                                    ra_stream_t stream) {
+  RA_TRACE("ra_backward_block");
   return backward_block_impl(q, k, v, dout, lse, rowterms, dq_acc, dk_acc, dv_acc, batch, c, d,
                              causal, dtype, stream);
 }
@@ -547,6 +555,7 @@ RA_API ra_status ra_backward(const void* q, const void* k, const void* v, const 
                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
                              float* workspace, int32_t B, int32_t H, int64_t N, int32_t d,
                              int32_t P, ra_dtype dtype, ra_stream_t stream) {
+  RA_TRACE("ra_backward");
   return backward_impl(q, k, v, out, dout, lse, dq, dk, dv, workspace, B, H, N, d, P, false,
                        RA_LAYOUT_CONTIGUOUS, dtype, stream);
 }
@@ -556,11 +565,13 @@ RA_API ra_status ra_backward_causal(const void* q, const void* k, const void* v,
                                     void* dv, float* workspace, int32_t B, int32_t H, int64_t N,
                                     int32_t d, int32_t P, ra_layout layout, ra_dtype dtype,
                                     ra_stream_t stream) {
+  RA_TRACE("ra_backward_causal");
   return backward_impl(q, k, v, out, dout, lse, dq, dk, dv, workspace, B, H, N, d, P, true,
                        layout, dtype, stream);
 }
 
 RA_API ra_status ra_state_init(const ra_state* st, ra_stream_t stream) {
+  RA_TRACE("ra_state_init");
   if (!state_ok(st)) return RA_ERR_INVALID_ARG;
   if (!aligned(st->m, 4) || !aligned(st->l, 4) || !aligned(st->o, 4)) return RA_ERR_MISALIGNED;
   if (st->rows == 0) return RA_OK;
@@ -573,6 +584,7 @@ RA_API ra_status ra_state_init(const ra_state* st, ra_stream_t stream) {
 
 RA_API ra_status ra_fold(const ra_state* st, const void* q, const void* kblk, const void* vblk,
                          int64_t batch, int64_t kv_rows, ra_dtype dtype, ra_stream_t stream) {
+  RA_TRACE("ra_fold");
   if (!state_ok(st) || !q || !kblk || !vblk) return RA_ERR_INVALID_ARG;
   if (batch < 1 || kv_rows < 0) return RA_ERR_INVALID_ARG;
   if (dtype != RA_F32 && dtype != RA_BF16) return RA_ERR_INVALID_ARG;
@@ -617,6 +629,7 @@ RA_API ra_status ra_fold(const ra_state* st, const void* q, const void* kblk, co
 
 RA_API ra_status ra_merge(const ra_state* partials, int32_t G, void* out, float* lse,
                           ra_dtype out_dtype, ra_stream_t stream) {
+  RA_TRACE("ra_merge");
   if (!partials || G < 1 || G > RA_MAX_PARTIALS || !out || !lse) return RA_ERR_INVALID_ARG;
   if (out_dtype != RA_F32 && out_dtype != RA_BF16) return RA_ERR_INVALID_ARG;
   MergeArgs a{};
@@ -648,6 +661,7 @@ RA_API ra_status ra_merge(const ra_state* partials, int32_t G, void* out, float*
 }
 
 RA_API ra_status ra_last_device_status(ra_stream_t stream) {
+  RA_TRACE("ra_last_device_status");
   DeviceInfo di;
   ra_status s = current_device(&di);
   if (s != RA_OK) return s;

@@ -15,6 +15,7 @@
 
 #include "ra.h"
 #include "ra_internal.h"
+#include "ra_trace.h"
 
 namespace {
 
@@ -92,6 +93,7 @@ RA_API ra_status ra_forward_host(const void* q, const void* k, const void* v, vo
                                  float* lse, int32_t B, int32_t H, int64_t N, int32_t d,
                                  int32_t P, int32_t causal, ra_layout layout, ra_dtype dtype,
                                  void* workspace, int64_t workspace_bytes, ra_stream_t stream) {
+  RA_TRACE("ra_forward_host");
   if (causal != 0 && causal != 1) return RA_ERR_INVALID_ARG;
   ra_status st = ra::check_forward_args(B, H, N, d, P, causal != 0, layout, dtype);
   if (st != RA_OK) return st;

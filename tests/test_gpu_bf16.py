@@ -186,3 +186,35 @@ def test_misaligned_pointer_rejected():
     with pytest.raises(ra.RaError) as e:
         ra.ra_forward(q, q, q, P=1)
     assert e.value.code == 3
+
+
+def test_state_checkpoint_and_resume(O):
+    """The (m, l, o) state is the whole of a half-done ring: fold the first
+    half of every query block's ring, copy the state to the host, restore it
+    into fresh device buffers, fold the rest, and the result equals the
+    one-call forward (and the oracle)."""
+    B, H, N, d, P = 1, 2, 1024, 128, 4
+    c = N // P
+    q, k, v = rnd((B, H, N, d), 61), rnd((B, H, N, d), 62), rnd((B, H, N, d), 63)
+    out_f, lse_f = ra.ra_forward(q, k, v, P=P)
+    order = O.ring_order(P)
+    blk = lambda t, j: t[:, :, j * c:(j + 1) * c].reshape(B * H, c, d).contiguous()
+    outs, lses = [], []
+    for i in range(P):
+        st = ra.ra_state_init(ra.new_state(B * H * c, d))
+        for t in range(P // 2):
+            ra.ra_fold(st, blk(q, i), blk(k, int(order[i, t])), blk(v, int(order[i, t])),
+                       batch=B * H)
+        saved = [x.cpu() for x in (st.m, st.l, st.o)]  # the checkpoint
+        del st
+        st = ra.RaState(*(x.to(DEV) for x in saved))   # resumed elsewhere
+        for t in range(P // 2, P):
+            ra.ra_fold(st, blk(q, i), blk(k, int(order[i, t])), blk(v, int(order[i, t])),
+                       batch=B * H)
+        o, l = ra.ra_merge([st], out_dtype=torch.bfloat16)
+        outs.append(o.reshape(B * H, c, d))
+        lses.append(l.reshape(B * H, c))
+    out = torch.cat(outs, dim=1).reshape(B, H, N, d)
+    lse = torch.cat(lses, dim=1).reshape(B, H, N)
+    check_forward(O, q, k, v, P, out, lse)
+    check_same(out, out_f, torch.bfloat16, "resumed vs one call", TOL_OUT[torch.bfloat16])
