@@ -60,3 +60,45 @@ def test_workload5_partials_and_merge(O):
         check_same(lse[:, h], lse_f[:, h], torch.bfloat16, "merge vs single-pass lse",
                    TOL_LSE, relative=False)
     assert ra.ra_last_device_status() == 0
+
+
+def test_workload4_size_closed_forms():
+    """Properties with a closed form, checked on every row at the size of
+    workload 4 (N = 131072, d = 128, P = 32; two heads).  Identical keys:
+    every weight is 1/N, so out = mean of V and lse = tau q.k + ln N ("Ring
+    Attention: the math", the online-softmax identity with all scores
+    equal).  One
+    dominant key (a score 39.6 above all others, which keep e^-39.6 of the
+    weight): out = that key's value row for every query block, whichever
+    step of its ring brings the key's block, and the kernel must raise its
+    reference max when that block arrives."""
+    import math
+
+    w = synth.WORKLOADS[4]
+    B, H, N, d, P = 1, 2, w.N, w.d, w.P
+    g = torch.Generator(device=DEV).manual_seed(404)
+    q = torch.randn(B, H, N, d, device=DEV, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, H, N, d, device=DEV, generator=g).to(torch.bfloat16)
+    k1 = torch.randn(B, H, 1, d, device=DEV, generator=g).to(torch.bfloat16)
+    k = k1.expand(B, H, N, d).contiguous()
+    out, lse = ra.ra_forward(q, k, v, P=P)
+    want_out = v.double().mean(dim=2, keepdim=True).expand(B, H, N, d)
+    want_lse = (q.double() * k1.double()).sum(-1) / math.sqrt(d) + math.log(N)
+    check_same(out, want_out, torch.bfloat16, "identical keys: out = mean(V)",
+               TOL_OUT[torch.bfloat16])
+    check_same(lse, want_lse, torch.bfloat16, "identical keys: lse", TOL_LSE, relative=False)
+    # one dominant key in the last block: q all equal so the score gap is exact
+    qd = torch.zeros(B, H, N, d, device=DEV, dtype=torch.bfloat16)
+    qd[..., 0] = 1.0
+    kd = torch.zeros(B, H, N, d, device=DEV, dtype=torch.bfloat16)
+    j0 = N - 77
+    kd[:, :, j0, 0] = 448.0  # exact in bf16: tau q.k = 448 / sqrt(128) ~ 39.6 for key j0
+    s0 = 448.0 / math.sqrt(d)
+    out, lse = ra.ra_forward(qd, kd, v, P=P)
+    want_out = v[:, :, j0:j0 + 1].double().expand(B, H, N, d)
+    check_same(out, want_out, torch.bfloat16, "dominant key: out = v[j0]",
+               TOL_OUT[torch.bfloat16])
+    want_lse = torch.full((B, H, N), s0 + math.log1p((N - 1) * math.exp(-s0)),
+                          device=DEV, dtype=torch.float64)
+    check_same(lse, want_lse, torch.bfloat16, "dominant key: lse", TOL_LSE, relative=False)
+    assert ra.ra_last_device_status() == 0
