@@ -218,3 +218,27 @@ def test_state_checkpoint_and_resume(O):
     lse = torch.cat(lses, dim=1).reshape(B, H, N)
     check_forward(O, q, k, v, P, out, lse)
     check_same(out, out_f, torch.bfloat16, "resumed vs one call", TOL_OUT[torch.bfloat16])
+
+
+def test_streams_and_concurrent_calls():
+    """Calls are asynchronous on the caller's stream and share no state:
+    the same call on a side stream gives the same bits, and two calls
+    running at once on two streams each give their own result."""
+    shape = (1, 4, 2048, 128)
+    q, k, v = rnd(shape, 71), rnd(shape, 72), rnd(shape, 73)
+    q2, k2, v2 = rnd(shape, 74), rnd(shape, 75), rnd(shape, 76)
+    ref1 = ra.ra_forward(q, k, v, P=4)
+    ref2 = ra.ra_forward(q2, k2, v2, P=4)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s1):
+        got1 = ra.ra_forward(q, k, v, P=4)
+    with torch.cuda.stream(s2):
+        got2 = ra.ra_forward(q2, k2, v2, P=4)
+    s1.synchronize()
+    s2.synchronize()
+    for got, ref in ((got1, ref1), (got2, ref2)):
+        assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
+    assert ra.ra_last_device_status() == 0
