@@ -361,11 +361,12 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
                const __grid_constant__ CUtensorMap tdo) {
   using L = DkvLayout<D>;
   using T = Tiles<D>;
-  // Where the next tile's S^T goes.  Early (between dV and dK; pass B then
-  // keeps p in registers, since S^T overwrites them in tS) measured 3.6 %
-  // faster with two warpgroups and 2.2 % slower with four, so the causal
-  // kernels issue it early and the plain ones after dK.
-  constexpr bool kEarlyS = kCausal;
+  // Where the next tile's S^T goes: it overwrites the p in tS, so it comes
+  // after the dV products (pass B keeps p in registers).  With two
+  // warpgroups (causal) it goes straight before dK; with four (plain) it
+  // goes between dK's two parts, which measured 0.5-3 % faster there than
+  // either straight before dK or after it.
+  constexpr bool kSBetweenDk = !kCausal;
   constexpr int kLoadWarp = Roles<G>::kLoadWarp;
   constexpr int kMmaWarp = Roles<G>::kMmaWarp;
   constexpr int kParts = Roles<G>::kParts;
@@ -477,10 +478,10 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       // Per tile, in pipe order: dP^T; dV over the parts of pass A as they
-      // land; dK over the parts of pass B; the next tile's S^T either before
-      // dK (kEarlyS) or after it.  Pass A runs while dP^T is on the tensor
-      // cores and pass B while dV is (and, with kEarlyS, the next pass A
-      // while dK is).
+      // land; dK over the parts of pass B, with the next tile's S^T before
+      // dK or between its parts (kSBetweenDk).  Pass A runs while dP^T is
+      // on the tensor cores, pass B while dV is and the next pass A while
+      // dK is.
       const uint64_t dK = desc_sw128(base + L::kK, 16, 1024);
       const uint64_t dV = desc_sw128(base + L::kV, 16, 1024);
       bool ok = wait1(kv_full(), 0, ab);
@@ -507,16 +508,18 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
           tc_fence_after();
           mma_tn_part<D, G>(tdV, tS, dDOs, h, h == 0 ? acc : 1u);  // dV += P^T dO, part h
         }
-        // the next tile's S^T, early: it overwrites the p in tS, which the dV
-        // products before it have read and pass B holds in registers
-        if (kEarlyS && ok && it + 1 < n_iter) {
-          const int s1 = (it + 1) % kStages;
-          if (!wait1(st_full(s1), static_cast<uint32_t>(((it + 1) / kStages) & 1), ab)) {
+        // the next tile's S^T (K Q^T of the next stage), issued once the dV
+        // products have read the p in tS: before dK, or after dK's part 0
+        const int s1 = (it + 1) % kStages;
+        const uint32_t s1_par = static_cast<uint32_t>(((it + 1) / kStages) & 1);
+        const uint64_t dQ1 = desc_sw128(base + L::kStage0 + s1 * L::kStageBytes, 16, 1024);
+        if (!kSBetweenDk && ok && it + 1 < n_iter) {
+          if (!wait1(st_full(s1), s1_par, ab)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          mma_nt<D>(tS, dK, desc_sw128(base + L::kStage0 + s1 * L::kStageBytes, 16, 1024));
+          mma_nt<D>(tS, dK, dQ1);
           mma_commit(s_full);
         }
         for (int h = 0; h < kParts && ok; ++h) {
@@ -526,20 +529,18 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
           }
           tc_fence_after();
           mma_tn_part<D, G>(tdK, tP, dQs, h, h == 0 ? acc : 1u);  // dK += dS^T Q, part h
+          if (kSBetweenDk && h == 0 && it + 1 < n_iter) {
+            if (!wait1(st_full(s1), s1_par, ab)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            mma_nt<D>(tS, dK, dQ1);
+            mma_commit(s_full);
+          }
         }
         if (!ok) break;
         mma_commit(st_empty(s));
-        // the next tile's S^T, late: after pass B has read the p in tS
-        if (!kEarlyS && it + 1 < n_iter) {
-          const int s1 = (it + 1) % kStages;
-          if (!wait1(st_full(s1), static_cast<uint32_t>(((it + 1) / kStages) & 1), ab)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          mma_nt<D>(tS, dK, desc_sw128(base + L::kStage0 + s1 * L::kStageBytes, 16, 1024));
-          mma_commit(s_full);
-        }
       }
       if (ok) {
         mma_commit(o_full);
@@ -578,9 +579,8 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
         lo = m < 0 ? 0 : (m > kBN ? kBN : static_cast<int>(m));
       }
       // pass A: p, feeding dV (warpgroup wg takes k-steps 4h + wg + G m of part h);
-      // with the early next S^T, this thread's p stay in registers for pass B
-      // (S^T overwrites them in tS as soon as the dV products have read it);
-      // otherwise pass B reads them back from tS
+      // this thread's p stay in registers for pass B, since the next S^T
+      // overwrites them in tS as soon as the dV products have read it
       uint32_t pkeep[kParts][Roles<G>::kStepsPerGroup][8];
 #pragma unroll
       for (int h = 0; h < kParts; ++h) {
@@ -602,9 +602,8 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
       for (int h = 0; h < kParts; ++h) {
 #pragma unroll
         for (int m = 0; m < Roles<G>::kStepsPerGroup; ++m)
-          pass_ds<true, !kEarlyS>(16 * (Roles<G>::kStepsPerPart * h + wg + G * m),
-                                                  tS + lane_off, tP + lane_off, rows + kBM, 0.f,
-                                                  pkeep[h][m]);
+          pass_ds<true, false>(16 * (Roles<G>::kStepsPerPart * h + wg + G * m), tS + lane_off,
+                               tP + lane_off, rows + kBM, 0.f, pkeep[h][m]);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(pb(h));
