@@ -132,10 +132,28 @@ def causal_flops(w) -> float:
     return 4.0 * w.B * w.H * w.d * w.N * (w.N + 1) / 2.0
 
 
+L2_BYTES = 129 * 2**20  # GB300 L2
+FLUSH_BYTES = 512 * 2**20  # written between timed steps when the inputs fit in L2
+
+
+def input_bytes(w) -> int:
+    esize = 2 if "bf16" in w.name else 4
+    return 3 * w.rows * w.d * esize
+
+
+def flushes_l2(w) -> bool:
+    """True when q, k and v together fit in twice the L2: the timed steps are
+    then separated by an L2 flush instead of relying on the input size."""
+    return input_bytes(w) < 2 * L2_BYTES
+
+
 def l2_note(w) -> str:
     """How the timed steps avoid an L2-resident working set (both arms)."""
-    esize = 2 if "bf16" in w.name else 4
-    return f"inputs larger than L2 (q+k+v = {3 * w.rows * w.d * esize / 2**20:.0f} MiB)"
+    mib = input_bytes(w) / 2**20
+    if flushes_l2(w):
+        return (f"L2 flushed before every timed step ({FLUSH_BYTES >> 20} MiB written, "
+                f"outside the timed events; q+k+v = {mib:.0f} MiB)")
+    return f"inputs larger than L2 (q+k+v = {mib:.0f} MiB)"
 
 
 def host_pipeline_stages(host_in, host_out, dev_in, results, w, stream) -> dict:
@@ -337,14 +355,27 @@ def run_ours(args, w) -> None:
     e1 = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    if flushes_l2(w):
+        # small inputs: each step timed alone, after a write larger than L2
+        flush = torch.empty(FLUSH_BYTES, device=dev, dtype=torch.uint8)
+        marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+        for a, b in marks:
+            flush.fill_(1)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in marks) / args.steps
+    else:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
     barrier()
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1) / args.steps
     if ra.ra_last_device_status() != 0:
         raise RuntimeError("kernel watchdog fired in the timed region")
     ms_max = max_over_ranks(ms, dev, world)
@@ -400,7 +431,7 @@ def run_ours(args, w) -> None:
     traffic = None if (args.causal or args.backward) else profiled_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": UNIT,
                 "frac": achieved / peaks["bf16"], "traffic": traffic,
-                "kernel": "fold_sm103_kernel<128>",
+                "kernel": f"fold_sm103_kernel<{w.d}>",
                 "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
                 if peaks["source"] == "measured" else "fallback 1.9 PFLOP/s bf16 burst"}
 
