@@ -431,7 +431,12 @@ def run_ours(args, w) -> None:
     traffic = None if (args.causal or args.backward) else profiled_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": UNIT,
                 "frac": achieved / peaks["bf16"], "traffic": traffic,
-                "kernel": f"fold_sm103_kernel<{w.d}>",
+                "kernel": (f"dkv_kernel<{w.d}> + dq_kernel<{w.d}> (the whole backward step)"
+                           if args.backward else
+                           f"fold_sm103_kernel<{w.d}> partials + merge (the whole step)"
+                           if args.split is not None else
+                           f"fold_sm103_kernel<{w.d}, causal>" if args.causal else
+                           f"fold_sm103_kernel<{w.d}>"),
                 "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
                 if peaks["source"] == "measured" else "fallback 1.9 PFLOP/s bf16 burst"}
 
