@@ -64,6 +64,30 @@ def test_growing_and_shrinking_max(O):
     check_forward(O, q, k, v, P, out, lse)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_max_rises_in_the_second_half_of_tiles(O, d):
+    """Keys 64-127 of every 128-key tile lifted along the mean query, more
+    for every later tile: in the forward's fast path the first half of each
+    tile passes its check and goes to the tensor cores, and the second half
+    then moves the reference max, so O and l are rescaled after that first
+    half's product (and the second half redone).  Also the causal kernel."""
+    B, H, N, P = 1, 2, 1024, 4
+    q = rnd((B, H, N, d), 71).float()
+    k = rnd((B, H, N, d), 72).float()
+    v = rnd((B, H, N, d), 73)
+    u = q.mean(dim=2, keepdim=True)
+    u = u / u.norm(dim=-1, keepdim=True)
+    for j in range(N // 128):
+        k[:, :, j * 128 + 64:(j + 1) * 128] += (3.0 * j) * u
+    q = (q * 3).to(torch.bfloat16)
+    k = k.to(torch.bfloat16)
+    out, lse = ra.ra_forward(q, k, v, P=P)
+    check_forward(O, q, k, v, P, out, lse)
+    out, lse = ra.ra_forward_causal(q, k, v, P, layout="contiguous")
+    check_forward(O, q, k, v, P, out, lse, causal=True, layout="contiguous")
+    assert ra.ra_last_device_status() == 0
+
+
 def test_large_scores(O):
     """Scores of magnitude ~100: no overflow in exp or in l."""
     B, H, N, d, P = 1, 1, 512, 64, 2
