@@ -421,10 +421,12 @@ RA_API ra_status ra_merge(const ra_state* partials, int32_t G, void* out, float*
  *                has in flight finish, frees its tensor memory and returns.
  *                <= 0 restores the default, 2^31 cycles (about a second).
  *   stall_cta    a test aid: >= 0 makes the CTA with this index of every
- *                later fold-kernel launch (forward, causal, partial, fold
- *                and split calls) load no input, so that its waits run out
- *                and the launch reports RA_ERR_TIMEOUT; the rows of that
- *                CTA are then not written.  -1 (the default) turns it off.
+ *                later tensor-core launch (the fold kernel of the forward,
+ *                causal, partial, fold and split calls; the dK/dV and dQ
+ *                kernels of the backward calls) load no input, so that its
+ *                waits run out and the call reports RA_ERR_TIMEOUT; the rows
+ *                of that CTA are then not written.  -1 (the default) turns
+ *                it off.
  * The settings are process-wide and apply to calls made after this one, on
  * every device and thread.  Never fails.
  */

@@ -341,5 +341,6 @@ def ra_last_device_status(stream=None) -> int:
 def ra_watchdog_config(wait_cycles: int = 0, stall_cta: int = -1) -> None:
     """Bounded-wait limit of the tensor-core kernels in SM cycles (<= 0: the
     default of 2^31) and the test aid `stall_cta` (>= 0: that CTA of later
-    fold launches loads nothing, so its waits run out; -1: off)."""
+    fold, dK/dV and dQ launches loads nothing, so its waits run out; -1:
+    off)."""
     _native.lib().ra_watchdog_config(int(wait_cycles), int(stall_cta))

@@ -445,6 +445,7 @@ ra_status backward_impl(const void* q, const void* k, const void* v, const void*
   a.scale_log2 = f.scale_log2;
   a.status = di.status;
   a.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  a.stall_cta = g_stall_cta.load(std::memory_order_relaxed);
   if ((st = launched(launch_delta(out, dout, lse, workspace, workspace + rows, rows, d, N, P,
                                   a.layout, dtype == RA_BF16, s))) != RA_OK)
     return st;
@@ -505,6 +506,7 @@ ra_status backward_block_impl(const void* q, const void* k, const void* v, const
   a.scale_log2 = f.scale_log2;
   a.status = di.status;
   a.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  a.stall_cta = g_stall_cta.load(std::memory_order_relaxed);
   a.accumulate = 1;
   if (dtype == RA_F32) return launched(launch_backward_f32(a, s));
   if ((st = get_encoder()) != RA_OK) return st;

@@ -438,14 +438,19 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
 
   if (warp == kLoadWarp) {
     if (lane == 0) {
+      // A stalled CTA (a test aid) loads nothing: its consumers' waits run
+      // out, raise the abort flag and return; nothing is in flight to drain.
+      const bool stalled = static_cast<int64_t>(blockIdx.x) == a.stall_cta;
       const int64_t klr = static_cast<int64_t>(kt) * kBM;  // first local key row
-      mbar_arrive_expect_tx(kv_full(), 2 * T::kTileBytes);
-      load_tile<D>(base + L::kK, &tk, striped, slice * a.N + walk.pos(j, klr), j,
-                   slice * c + klr, kv_full());
-      load_tile<D>(base + L::kV, &tv, striped, slice * a.N + walk.pos(j, klr), j,
-                   slice * c + klr, kv_full());
+      if (!stalled) {
+        mbar_arrive_expect_tx(kv_full(), 2 * T::kTileBytes);
+        load_tile<D>(base + L::kK, &tk, striped, slice * a.N + walk.pos(j, klr), j,
+                     slice * c + klr, kv_full());
+        load_tile<D>(base + L::kV, &tv, striped, slice * a.N + walk.pos(j, klr), j,
+                     slice * c + klr, kv_full());
+      }
       uint32_t issued = 0, last_parity = 0;
-      bool ok = true;
+      bool ok = !stalled;
       KWalk w = walk;
       w.start();
       for (int it = 0; it < n_iter && ok; ++it, w.next()) {
@@ -470,7 +475,7 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
         last_parity = (last_parity & ~(1u << s)) | (ph << s);
       }
       if (!ok) {
-        wait_drain(kv_full(), 0);
+        if (!stalled) wait_drain(kv_full(), 0);
         for (int s = 0; s < kStages; ++s)
           if (issued & (1u << s)) wait_drain(st_full(s), (last_parity >> s) & 1u);
       }
@@ -761,14 +766,18 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
 
   if (warp == kLoadWarp) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, 2 * T::kTileBytes);
-      load_tile<D>(base + L::kQ, &tq, striped, slice * a.N + walk.pos(i, qlr0), i,
-                   slice * c + qlr0, q_full);
-      load_tile<D>(base + L::kDO, &tdo, striped, slice * a.N + walk.pos(i, qlr0), i,
-                   slice * c + qlr0, q_full);
+      // A stalled CTA (a test aid) loads nothing (see the dK/dV kernel).
+      const bool stalled = static_cast<int64_t>(blockIdx.x) == a.stall_cta;
+      if (!stalled) {
+        mbar_arrive_expect_tx(q_full, 2 * T::kTileBytes);
+        load_tile<D>(base + L::kQ, &tq, striped, slice * a.N + walk.pos(i, qlr0), i,
+                     slice * c + qlr0, q_full);
+        load_tile<D>(base + L::kDO, &tdo, striped, slice * a.N + walk.pos(i, qlr0), i,
+                     slice * c + qlr0, q_full);
+      }
       // per ring, the stages with a load in flight and their last parity
       uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
-      bool ok = true;
+      bool ok = !stalled;
       Walk w = walk;
       w.start();
       for (int it = 0; it < n_iter && ok; ++it, w.next()) {
@@ -797,7 +806,7 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
         v_par = (v_par & ~(1u << vs)) | (vph << vs);
       }
       if (!ok) {
-        wait_drain(q_full, 0);
+        if (!stalled) wait_drain(q_full, 0);
         for (int s = 0; s < L::kKStages; ++s)
           if (k_issued & (1u << s)) wait_drain(k_full(s), (k_par >> s) & 1u);
         for (int s = 0; s < L::kVStages; ++s)

@@ -89,6 +89,7 @@ struct BackwardArgs {
   float scale_log2;  // tau * log2(e)
   int* status;       // device watchdog word
   int64_t wait_limit;  // SM cycles a bounded wait may take
+  int64_t stall_cta;   // test aid: this CTA of each tensor-core kernel loads nothing (-1: none)
   int32_t accumulate;  // 1: dq, dk, dv are fp32 accumulators; add instead of store
 };
 

@@ -105,3 +105,60 @@ def test_stalled_fold_call_times_out(O):
     assert np.max(np.abs(st.m.double().cpu().numpy() - m)) <= 1e-4
     check_close(st.o / st.l[:, None], o / l[:, None], torch.bfloat16, "fold after timeout",
                 2e-2)
+
+
+def _backward_want(O, q, k, v, out, dout, lse, P):
+    from gpu_util import to_oracle
+    B, H, N, d = q.shape
+    qa, tag = to_oracle(q)
+    ka, _ = to_oracle(k)
+    va, _ = to_oracle(v)
+    oa = out.double().reshape(B * H, N, d).cpu().numpy()
+    ga = dout.double().reshape(B * H, N, d).cpu().numpy()
+    la = lse.double().reshape(B * H, N).cpu().numpy()
+    return O.backward(qa, ka, va, oa, ga, la, P, dtype=tag)
+
+
+def test_short_limit_alone_raises_nothing_in_the_backward(O):
+    B, H, N, d, P = 1, 2, 1024, 128, 4
+    q, k, v, dout = (rnd((B, H, N, d), 730 + s) for s in range(4))
+    out, lse = ra.ra_forward(q, k, v, P)
+    ra.ra_watchdog_config(SHORT, -1)
+    grads = ra.ra_backward(q, k, v, out, dout, lse, P)
+    assert ra.ra_last_device_status() == _native.RA_OK
+    for name, got, want in zip(("dq", "dk", "dv"), grads,
+                               _backward_want(O, q, k, v, out, dout, lse, P)):
+        check_close(got.reshape(-1, d), want.reshape(-1, d), torch.bfloat16,
+                    f"backward {name} under a short limit", 2e-2)
+
+
+def test_stalled_backward_cta_times_out_and_the_context_recovers(O):
+    """CTA 3 of the dK/dV kernel and of the dQ kernel loads nothing.  With
+    2 heads, P = 4 and c = 256 both kernels have 16 CTAs of one 128-row tile;
+    CTA 3 is head 0, block 1, tile 1 (rows 384 .. 511 of head 0) in both, so
+    every other row of dq, dk and dv is still right."""
+    B, H, N, d, P = 1, 2, 1024, 128, 4
+    q, k, v, dout = (rnd((B, H, N, d), 740 + s) for s in range(4))
+    out, lse = ra.ra_forward(q, k, v, P)
+    assert ra.ra_last_device_status() == _native.RA_OK
+    ra.ra_watchdog_config(SHORT, 3)
+    t0 = time.perf_counter()
+    grads = ra.ra_backward(q, k, v, out, dout, lse, P)
+    status = ra.ra_last_device_status()
+    elapsed = time.perf_counter() - t0
+    ra.ra_watchdog_config(0, -1)
+    assert status == _native.RA_ERR_TIMEOUT
+    assert ra.ra_last_device_status() == _native.RA_OK
+    assert elapsed < 5.0
+    want = _backward_want(O, q, k, v, out, dout, lse, P)
+    rows = [r for r in range(B * H * N) if not 384 <= r < 512]
+    idx = torch.tensor(rows, device=DEV)
+    for name, got, w in zip(("dq", "dk", "dv"), grads, want):
+        check_close(got.reshape(-1, d).index_select(0, idx), w.reshape(-1, d)[rows],
+                    torch.bfloat16, f"backward {name}, rows of the other CTAs", 2e-2)
+    # the context is intact: the same call with the default settings is right
+    grads = ra.ra_backward(q, k, v, out, dout, lse, P)
+    assert ra.ra_last_device_status() == _native.RA_OK
+    for name, got, w in zip(("dq", "dk", "dv"), grads, want):
+        check_close(got.reshape(-1, d), w.reshape(-1, d), torch.bfloat16,
+                    f"backward {name} after a timeout", 2e-2)
