@@ -10,6 +10,15 @@ and writes out and lse.  Prints ONE JSON line (rank 0).
 
 Several GPUs (torchrun) run independent replicas of the same workload (the
 virtual ring lives on one GPU; there is no exchange between ranks).
+
+  python bench.py --ring R   # the compute of an R-rank ring, played on one GPU
+
+--ring times what the ranks of a multi-device ring (long_context_ra_gb300.ring)
+compute, without the exchange: every rank's state initialisation, its R
+ra_fold steps over the blocks (i - t) mod R, and its final ra_merge, for all
+R ranks one after another on this GPU.  Each of those launches is the one a
+rank makes on its own device, so the figure is the per-device efficiency of
+the ring's compute.
 """
 from __future__ import annotations
 
@@ -321,6 +330,30 @@ def run_ours(args, w) -> None:
         def step():
             return ra.ra_backward(q, k, v, out0, dout, lse0, w.P, workspace=ws,
                                   causal=args.causal)
+    elif args.ring is not None:
+        R = args.ring
+        c, bh = w.N // R, w.B * w.H
+        if R < 1 or w.N % R or c % 128:
+            raise SystemExit(f"--ring {R}: the block N / R must be a multiple of 128")
+
+        def blocks(t):
+            return [t[:, :, i * c:(i + 1) * c].reshape(bh, c, w.d).contiguous() for i in range(R)]
+
+        qs, ks, vs = blocks(q), blocks(k), blocks(v)  # what each rank holds
+        states = [ra.new_state(bh * c, w.d, dev) for _ in range(R)]
+        r_out = [torch.empty(bh * c, w.d, device=dev, dtype=q.dtype) for _ in range(R)]
+        r_lse = [torch.empty(bh * c, device=dev, dtype=torch.float32) for _ in range(R)]
+
+        def step():
+            for st in states:
+                ra.ra_state_init(st)
+            for t in range(R):
+                for i in range(R):
+                    j = (i - t) % R
+                    ra.ra_fold(states[i], qs[i], ks[j], vs[j], batch=bh)
+            for i in range(R):
+                ra.ra_merge([states[i]], out=r_out[i], lse=r_lse[i])
+            return r_out + r_lse
     elif args.split is not None:
         G = args.split or ra.ra_forward_split_segments(w.B, w.H, w.N, w.d, w.P, w.dtype)
         ws = torch.empty(ra.ra_forward_split_workspace_bytes(w.B, w.H, w.N, w.d, G), device=dev,
@@ -385,10 +418,12 @@ def run_ours(args, w) -> None:
     # to the device, the call, its results back to pinned host memory, every
     # step
     dev_in = [q, k, v] + ([out0, dout, lse0] if args.backward else [])
+    if args.ring is not None:
+        dev_in = qs + ks + vs  # each rank's blocks
     host_in = [x.cpu().pin_memory() for x in dev_in]
     results = step()
     host_out = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results]
-    if not args.backward and args.split is None:
+    if not args.backward and args.split is None and args.ring is None:
         # the host-buffer entry point: chunked upload / compute / download
         e2e_path = "ra_forward_host"
         ws_host = torch.empty(ra.ra_forward_host_workspace_bytes(w.B, w.H, w.N, w.d, q.dtype),
@@ -428,13 +463,16 @@ def run_ours(args, w) -> None:
 
     peaks = load_peaks()
     achieved = flops / (ms * 1e-3) / 1e12  # one fold launch per step
-    traffic = None if (args.causal or args.backward) else profiled_traffic(w.name)
+    traffic = None if (args.causal or args.backward or args.ring is not None) \
+        else profiled_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": UNIT,
                 "frac": achieved / peaks["bf16"], "traffic": traffic,
                 "kernel": (f"dkv_kernel<{w.d}> + dq_kernel<{w.d}> (the whole backward step)"
                            if args.backward else
                            f"fold_sm103_kernel<{w.d}> partials + merge (the whole step)"
                            if args.split is not None else
+                           f"fold_sm103_kernel<{w.d}> in fold mode + merge (all ranks' steps)"
+                           if args.ring is not None else
                            f"fold_sm103_kernel<{w.d}, causal>" if args.causal else
                            f"fold_sm103_kernel<{w.d}>"),
                 "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
@@ -442,7 +480,7 @@ def run_ours(args, w) -> None:
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.causal \
-            and not args.backward:
+            and not args.backward and args.ring is None:
         cpu, _, _ = cpu_oracle_baseline(w, q, k, v, args.cpu_seconds)
 
     if rank == 0:
@@ -454,13 +492,19 @@ def run_ours(args, w) -> None:
                        **({"causal": args.causal} if args.causal else {}),
                        **({"split_segments": G} if args.split is not None else {}),
                        **({"pass": "backward"} if args.backward else {}),
+                       **({"ring_ranks": args.ring, "block": w.N // args.ring,
+                           "pass": "ring compute: every rank's state init, R ra_fold steps "
+                                   "and ra_merge, played on one GPU, no exchange"}
+                          if args.ring is not None else {}),
                        "l2": l2_note(w)},
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e_max, "path": e2e_path,
                     "steps": n_e2e, "of_device_value": e2e_value / value,
                     **({"stages_ms": stages} if stages else {})},
-            "gpu_launches": args.steps * (3 if args.backward else 2 if args.split is not None else 1),
+            "gpu_launches": args.steps * (3 if args.backward else 2 if args.split is not None
+                                          else args.ring * (args.ring + 2)
+                                          if args.ring is not None else 1),
             "clocks": clocks,
             "pct_of_peak": 100.0 * achieved / peaks["bf16"],
             "exps_per_s": (flops / (4.0 * w.d)) / (ms * 1e-3),
@@ -484,6 +528,8 @@ def main() -> None:
                     help="time ra_forward_split with G segments (0 = recommended)")
     ap.add_argument("--backward", action="store_true",
                     help="time ra_backward (5 products per head counted: 10 B H N^2 d)")
+    ap.add_argument("--ring", type=int, default=None,
+                    help="time the compute of an R-rank multi-device ring on this GPU")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0,
