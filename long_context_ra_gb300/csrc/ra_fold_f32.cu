@@ -58,9 +58,34 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// tau q.k for one key row: four independent FMA chains, 16-byte loads when
+// every row starts on a 16-byte boundary (vec), a scalar tail otherwise.
+__device__ __forceinline__ float dot_row(const float* __restrict__ qrow,
+                                         const float* __restrict__ kr, int d, bool vec) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  int e = 0;
+  if (vec) {
+    const float4* k4 = reinterpret_cast<const float4*>(kr);
+    const float4* q4 = reinterpret_cast<const float4*>(qrow);
+    const int n4 = d / 4;
+#pragma unroll 4
+    for (int x = 0; x < n4; ++x) {
+      const float4 kk = k4[x];
+      const float4 qq = q4[x];
+      a0 = fmaf(qq.x, kk.x, a0);
+      a1 = fmaf(qq.y, kk.y, a1);
+      a2 = fmaf(qq.z, kk.z, a2);
+      a3 = fmaf(qq.w, kk.w, a3);
+    }
+    e = 4 * n4;
+  }
+  for (; e < d; ++e) a0 = fmaf(qrow[e], kr[e], a0);
+  return (a0 + a1) + (a2 + a3);
+}
+
 template <int DV>  // o values per lane: d <= 32 * DV
 __global__ void __launch_bounds__(kWarps * 32) fold_f32_kernel(const FoldArgs a) {
-  __shared__ float qs[kWarps][32 * DV];
+  __shared__ __align__(16) float qs[kWarps][32 * DV];
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int d = a.d;
@@ -75,6 +100,9 @@ __global__ void __launch_bounds__(kWarps * 32) fold_f32_kernel(const FoldArgs a)
   const int t0 = static_cast<int>(static_cast<int64_t>(g) * a.P / a.G);
   const int t1 = static_cast<int>(static_cast<int64_t>(g + 1) * a.P / a.G);
 
+  // rows of k start on 16-byte boundaries when d is a multiple of 4 and k
+  // itself is 16-byte aligned
+  const bool vec = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(a.k) % 16 == 0);
   const float* q = static_cast<const float*>(a.q) + rid * d;
   for (int e = lane; e < d; e += 32) qs[warp][e] = q[e];
   __syncwarp();
@@ -104,22 +132,21 @@ __global__ void __launch_bounds__(kWarps * 32) fold_f32_kernel(const FoldArgs a)
       const int64_t kpos = key < ck ? pos_of(a.layout, j, key, a.P, ck) : 0;
       const bool valid = key < ck && (!a.causal || kpos <= n);
       float s = -INFINITY;
-      if (valid) {
-        const float* kr = kbase + kpos * d;
-        float acc = 0.f;
-        for (int e = 0; e < d; ++e) acc = fmaf(qs[warp][e], kr[e], acc);
-        s = acc * a.tau;
-      }
+      if (valid) s = dot_row(qs[warp], kbase + kpos * d, d, vec) * a.tau;
       const float m_new = fmaxf(m, warp_max(s));
       const float alpha = m_new == -INFINITY ? 1.f : expf(m - m_new);
       const float p = valid ? expf(s - m_new) : 0.f;
       l = alpha * l + warp_sum(p);
 #pragma unroll
       for (int v = 0; v < DV; ++v) o[v] *= alpha;
-      const int nvalid = ck - c0 < 32 ? static_cast<int>(ck - c0) : 32;
-      for (int jj = 0; jj < nvalid; ++jj) {
+      // o += p V over the chunk's keys.  The loop has a fixed trip count
+      // (masked keys and keys past the block's end have p = 0; the latter
+      // read the slice's first row), so the V loads of several keys are in
+      // flight at once.  As on the tensor-core path, a masked key's v is
+      // multiplied by 0 rather than skipped.
+#pragma unroll 8
+      for (int jj = 0; jj < 32; ++jj) {
         const float pj = __shfl_sync(0xffffffffu, p, jj);
-        if (pj == 0.f) continue;  // masked (or underflowed) key adds nothing
         const float* vr = vbase + __shfl_sync(0xffffffffu, kpos, jj) * d;
 #pragma unroll
         for (int v = 0; v < DV; ++v) {
