@@ -103,11 +103,54 @@ __global__ void __launch_bounds__(256) delta_kernel(const void* out, const void*
   }
 }
 
+// Two dot products of length d at once, s = x.y and dp = u.w: 16-byte loads
+// and two FMA chains each when every row starts on a 16-byte boundary (vec),
+// a scalar tail otherwise.
+__device__ __forceinline__ void dot2(const float* __restrict__ x, const float* __restrict__ y,
+                                     const float* __restrict__ u, const float* __restrict__ w,
+                                     int d, bool vec, float& s, float& dp) {
+  float s0 = 0.f, s1 = 0.f, p0 = 0.f, p1 = 0.f;
+  int e = 0;
+  if (vec) {
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    const float4* y4 = reinterpret_cast<const float4*>(y);
+    const float4* u4 = reinterpret_cast<const float4*>(u);
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    const int n4 = d / 4;
+#pragma unroll 2
+    for (int i = 0; i < n4; ++i) {
+      const float4 a = x4[i], b = y4[i], c = u4[i], f = w4[i];
+      s0 = fmaf(a.x, b.x, s0);
+      s1 = fmaf(a.y, b.y, s1);
+      s0 = fmaf(a.z, b.z, s0);
+      s1 = fmaf(a.w, b.w, s1);
+      p0 = fmaf(c.x, f.x, p0);
+      p1 = fmaf(c.y, f.y, p1);
+      p0 = fmaf(c.z, f.z, p0);
+      p1 = fmaf(c.w, f.w, p1);
+    }
+    e = 4 * n4;
+  }
+  for (; e < d; ++e) {
+    s0 = fmaf(x[e], y[e], s0);
+    p0 = fmaf(u[e], w[e], p0);
+  }
+  s = s0 + s1;
+  dp = p0 + p1;
+}
+
+// rows of every operand start on 16-byte boundaries
+__device__ __forceinline__ bool rows_vec(const BackwardArgs& a) {
+  const uintptr_t m = reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k) |
+                      reinterpret_cast<uintptr_t>(a.v) | reinterpret_cast<uintptr_t>(a.dout);
+  return a.d % 4 == 0 && m % 16 == 0;
+}
+
 // Gradient of one query row (warp) over all key blocks in ring order.
 template <int DV>
 __global__ void __launch_bounds__(kWarps * 32) dq_f32_kernel(const BackwardArgs a) {
-  __shared__ float qs[kWarps][32 * DV];
-  __shared__ float gs[kWarps][32 * DV];
+  __shared__ __align__(16) float qs[kWarps][32 * DV];
+  __shared__ __align__(16) float gs[kWarps][32 * DV];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int d = a.d;
   const int64_t rid = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
@@ -125,6 +168,7 @@ __global__ void __launch_bounds__(kWarps * 32) dq_f32_kernel(const BackwardArgs 
   }
   __syncwarp();
   const float lse = a.lse[rid], D = a.delta[bmajor(a.layout, slice, a.N, n, a.P, c)];
+  const bool vec = rows_vec(a);
   float acc[DV];
 #pragma unroll
   for (int x = 0; x < DV; ++x) acc[x] = 0.f;
@@ -138,21 +182,17 @@ __global__ void __launch_bounds__(kWarps * 32) dq_f32_kernel(const BackwardArgs 
       const int64_t kp = key < c ? bpos(a.layout, j, key, a.P, c) : 0;
       float ds = 0.f;
       if (key < c && (!a.causal || kp <= n)) {
-        const float* kr = k + (sb + kp) * d;
-        const float* vr = v + (sb + kp) * d;
-        float s = 0.f, dp = 0.f;
-        for (int e = 0; e < d; ++e) {
-          s = fmaf(qs[warp][e], kr[e], s);
-          dp = fmaf(gs[warp][e], vr[e], dp);
-        }
+        float s, dp;
+        dot2(qs[warp], k + (sb + kp) * d, gs[warp], v + (sb + kp) * d, d, vec, s, dp);
         const float p = expf(s * a.tau - lse);
         ds = p * (dp - D);
       }
-      const int nk = c - c0 < 32 ? static_cast<int>(c - c0) : 32;
-      for (int jj = 0; jj < nk; ++jj) {
+      // fixed trip count (ds = 0 for masked keys and keys past the block's
+      // end, which read the slice's first row): several loads in flight
+#pragma unroll 8
+      for (int jj = 0; jj < 32; ++jj) {
         const float dsj = __shfl_sync(0xffffffffu, ds, jj);
         const int64_t kpj = __shfl_sync(0xffffffffu, kp, jj);
-        if (dsj == 0.f) continue;
         const float* kr = k + (sb + kpj) * d;
 #pragma unroll
         for (int x = 0; x < DV; ++x) {
@@ -173,8 +213,8 @@ __global__ void __launch_bounds__(kWarps * 32) dq_f32_kernel(const BackwardArgs 
 // Gradients of one key row (warp) over the query blocks its block visits.
 template <int DV>
 __global__ void __launch_bounds__(kWarps * 32) dkv_f32_kernel(const BackwardArgs a) {
-  __shared__ float ks[kWarps][32 * DV];
-  __shared__ float vs[kWarps][32 * DV];
+  __shared__ __align__(16) float ks[kWarps][32 * DV];
+  __shared__ __align__(16) float vs[kWarps][32 * DV];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int d = a.d;
   const int64_t rid = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
@@ -191,6 +231,7 @@ __global__ void __launch_bounds__(kWarps * 32) dkv_f32_kernel(const BackwardArgs
     vs[warp][e] = v[rid * d + e];
   }
   __syncwarp();
+  const bool vec = rows_vec(a);
   float gk[DV], gv[DV];
 #pragma unroll
   for (int x = 0; x < DV; ++x) gk[x] = gv[x] = 0.f;
@@ -202,22 +243,18 @@ __global__ void __launch_bounds__(kWarps * 32) dkv_f32_kernel(const BackwardArgs
       const int64_t qp = row < c ? bpos(a.layout, i, row, a.P, c) : 0;
       float p = 0.f, ds = 0.f;
       if (row < c && (!a.causal || qp >= n)) {
-        const float* qr = q + (sb + qp) * d;
-        const float* gr = g + (sb + qp) * d;
-        float s = 0.f, dp = 0.f;
-        for (int e = 0; e < d; ++e) {
-          s = fmaf(qr[e], ks[warp][e], s);
-          dp = fmaf(gr[e], vs[warp][e], dp);
-        }
+        float s, dp;
+        dot2(q + (sb + qp) * d, ks[warp], g + (sb + qp) * d, vs[warp], d, vec, s, dp);
         p = expf(s * a.tau - a.lse[sb + qp]);
         ds = p * (dp - a.delta[sb + static_cast<int64_t>(i) * c + row]);
       }
-      const int nq = c - c0 < 32 ? static_cast<int>(c - c0) : 32;
-      for (int jj = 0; jj < nq; ++jj) {
+      // fixed trip count (p = ds = 0 for masked rows and rows past the
+      // block's end, which read the slice's first row): loads in flight
+#pragma unroll 8
+      for (int jj = 0; jj < 32; ++jj) {
         const float pj = __shfl_sync(0xffffffffu, p, jj);
         const float dsj = __shfl_sync(0xffffffffu, ds, jj);
         const int64_t qpj = __shfl_sync(0xffffffffu, qp, jj);
-        if (pj == 0.f && dsj == 0.f) continue;
         const float* qr = q + (sb + qpj) * d;
         const float* gr = g + (sb + qpj) * d;
 #pragma unroll
