@@ -1,20 +1,29 @@
 // fp32 fold kernel (FFMA only, no TF32): the exact-precision path for any
 // head dimension 1 <= d <= 256 and any block size.
 //
-// One warp owns one query row ("Ring Attention: the math", section "Sharding
-// the sequence": queries stay home) and walks the key blocks in ring order
-// j = (i - t) mod P (section "The ring schedule: passing K/V around").  Each
-// block is folded 32 keys at a time -- one key per lane -- with the update of
-// section "The online-softmax identity that makes streaming legal":
+// One CTA (4 warps) owns 64 query rows of one query block i ("Ring
+// Attention: the math", section "Sharding the sequence": queries stay home)
+// and walks the key blocks in ring order j = (i - t) mod P (section "The ring
+// schedule: passing K/V around").  Each block is folded 32 keys at a time
+// with the update of section "The online-softmax identity that makes
+// streaming legal":
 //   s = tau q.k;  m' = max(m, max s);  alpha = exp(m - m');
 //   l' = alpha l + sum exp(s - m');  o' = alpha o + sum exp(s - m') v.
-// Folding a block in chunks is exact by the same identity.  The lanes split
-// o: lane e holds o[e], o[e + 32], ...
+// Folding a block in chunks is exact by the same identity.
+//
+// The query tile and each 32-key K/V tile are staged in shared memory and
+// shared by the 64 rows.  Warp w owns rows 16w .. 16w + 15; lane (rg, kg) =
+// (lane / 8, lane % 8) computes the 4 x 4 block of scores of rows
+// 16w + 4rg + 0..3 against keys 4kg + 0..3, and holds o of the same 4 rows
+// in the columns 4kg + 32m + 0..3.  A row's max and sum are reduced over the
+// 8 lanes of its group.  Q and K are stored transposed ([d][rows]) so that a
+// lane reads 4 rows or 4 keys of one column as one 16-byte load.
 //
 // Causal ("Ring attention, explained", "The causal-mask catch"): a query at
 // position n sees key positions <= n.  Under every layout the positions of a
 // block increase along its local order, so the visible keys of a block are a
-// prefix and the walk over it stops at the first chunk that starts after n.
+// prefix, and the walk over a block stops at the first tile that starts after
+// the CTA's last query.
 
 #include <cmath>
 
@@ -23,7 +32,14 @@
 namespace ra {
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kThreads = 128;  // 4 warps
+constexpr int kBM = 64;        // query rows per CTA
+constexpr int kBN = 32;        // keys per K/V tile
+constexpr int kQS = kBM + 4;   // row stride of the transposed Q and P tiles (floats)
+constexpr int kKS = kBN + 4;   // row stride of the transposed K tile (floats)
+// below this many CTAs the tiled kernel leaves most SMs idle, and the
+// row-per-warp kernel (64 x more CTAs) is faster
+constexpr int64_t kSmallGrid = 32;
 
 // Position of local row r of block j under `layout` (P blocks of c rows).
 __device__ __forceinline__ int64_t pos_of(int layout, int64_t j, int64_t r, int64_t P,
@@ -35,6 +51,267 @@ __device__ __forceinline__ int64_t pos_of(int layout, int64_t j, int64_t r, int6
   if (layout == kStriped) return j + P * r;
   return j * c + r;
 }
+
+// Shared-memory footprint (floats) for head dimensions up to DT.
+template <int DT>
+struct Smem {
+  static constexpr int kQ = 0;                    // Q^T  [DT][kQS]
+  static constexpr int kK = kQ + DT * kQS;        // K^T  [DT][kKS]
+  static constexpr int kV = kK + DT * kKS;        // V    [kBN][DT + 4]
+  static constexpr int kP = kV + kBN * (DT + 4);  // P^T  [kBN][kQS]
+  static constexpr int kFloats = kP + kBN * kQS;
+  static constexpr int kBytes = kFloats * 4;
+};
+
+// max / sum over the 8 lanes of a row group (lanes 8g .. 8g + 7)
+__device__ __forceinline__ float group_max(float x) {
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+  return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
+}
+__device__ __forceinline__ float group_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  return x + __shfl_xor_sync(0xffffffffu, x, 4);
+}
+
+template <int DT>  // d <= DT; DT in {64, 128, 256}
+__global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
+  using S = Smem<DT>;
+  constexpr int kCols = DT / 32;  // float4 column groups of o a lane holds
+  extern __shared__ __align__(16) float sm[];
+  float* qT = sm + S::kQ;
+  float* kT = sm + S::kK;
+  float* vs = sm + S::kV;
+  float* pT = sm + S::kP;
+
+  const int tid = threadIdx.x;
+  const int warp = tid / 32, lane = tid % 32;
+  const int rg = lane / 8, kg = lane % 8;
+  const int d = a.d;
+  const int64_t cq = a.nq / a.P;
+  const int64_t ck = a.nk / a.P;
+  const int64_t tiles_q = (cq + kBM - 1) / kBM;
+  int64_t u = blockIdx.x;
+  const int64_t qt = u % tiles_q;
+  u /= tiles_q;
+  const int i = static_cast<int>(u % a.P);
+  const int64_t slice = u / a.P;
+  const int g = blockIdx.y;  // segment
+  const int t0 = static_cast<int>(static_cast<int64_t>(g) * a.P / a.G);
+  const int t1 = static_cast<int>(static_cast<int64_t>(g + 1) * a.P / a.G);
+  const int64_t r0 = qt * kBM;  // first local query row of the CTA
+
+  const float* q = static_cast<const float*>(a.q) + slice * a.nq * d;
+  const float* kb = static_cast<const float*>(a.k) + slice * a.nk * d;
+  const float* vb = static_cast<const float*>(a.v) + slice * a.nk * d;
+
+  // Q^T tile: column e of row x at qT[e * kQS + x]; rows past the block and
+  // columns past d are zero
+  for (int x = tid; x < kBM * DT; x += kThreads) {
+    const int row = x / DT, e = x % DT;
+    const int64_t r = r0 + row;
+    float val = 0.f;
+    if (r < cq && e < d) val = q[pos_of(a.layout, i, r, a.P, cq) * d + e];
+    qT[e * kQS + row] = val;
+  }
+
+  // this lane's 4 rows: local rows, positions, state
+  const int lrow0 = 16 * warp + 4 * rg;  // first of the 4 rows within the CTA
+  int64_t qpos[4];
+  bool rvalid[4];
+  float m[4], l[4];
+  float o[4][kCols][4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const int64_t r = r0 + lrow0 + x;
+    rvalid[x] = r < cq;
+    qpos[x] = rvalid[x] ? pos_of(a.layout, i, r, a.P, cq) : 0;
+    m[x] = -INFINITY;
+    l[x] = 0.f;
+#pragma unroll
+    for (int c = 0; c < kCols; ++c)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) o[x][c][y] = 0.f;
+  }
+  if (a.mode == kFold) {
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      if (!rvalid[x]) continue;
+      const int64_t row = slice * a.nq + qpos[x];
+      m[x] = a.st_m[row];
+      l[x] = a.st_l[row];
+#pragma unroll
+      for (int c = 0; c < kCols; ++c)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          const int e = 4 * kg + 32 * c + y;
+          if (e < d) o[x][c][y] = a.st_o[row * d + e];
+        }
+    }
+  }
+  // the CTA's last query position (positions grow along a block's rows)
+  const int64_t rlast = (r0 + kBM < cq ? r0 + kBM : cq) - 1;
+  const int64_t qlast = pos_of(a.layout, i, rlast, a.P, cq);
+
+  for (int t = t0; t < t1; ++t) {
+    int j = (i - t) % a.P;
+    if (j < 0) j += a.P;
+    for (int64_t c0 = 0; c0 < ck; c0 += kBN) {
+      if (a.causal && pos_of(a.layout, j, c0, a.P, ck) > qlast) break;  // rest masked
+      __syncthreads();  // the previous tile's K, V and P are no longer read
+      // K^T and V tiles; keys past the block and columns past d are zero
+      for (int x = tid; x < kBN * DT; x += kThreads) {
+        const int key = x / DT, e = x % DT;
+        const int64_t kk = c0 + key;
+        float kv = 0.f, vv = 0.f;
+        if (kk < ck && e < d) {
+          const int64_t row = pos_of(a.layout, j, kk, a.P, ck);
+          kv = kb[row * d + e];
+          vv = vb[row * d + e];
+        }
+        kT[e * kKS + key] = kv;
+        vs[key * (DT + 4) + e] = vv;
+      }
+      __syncthreads();
+
+      // scores of the lane's 4 rows x 4 keys
+      float s[4][4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) s[x][y] = 0.f;
+#pragma unroll 4
+      for (int e = 0; e < d; ++e) {
+        const float4 qa = *reinterpret_cast<const float4*>(qT + e * kQS + lrow0);
+        const float4 ka = *reinterpret_cast<const float4*>(kT + e * kKS + 4 * kg);
+        const float qv[4] = {qa.x, qa.y, qa.z, qa.w};
+        const float kv[4] = {ka.x, ka.y, ka.z, ka.w};
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+#pragma unroll
+          for (int y = 0; y < 4; ++y) s[x][y] = fmaf(qv[x], kv[y], s[x][y]);
+      }
+      // masks: keys past the block, and (causal) keys after the query
+      bool kvalid[4];
+      int64_t kpos[4];
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const int64_t kk = c0 + 4 * kg + y;
+        kvalid[y] = kk < ck;
+        kpos[y] = kvalid[y] ? pos_of(a.layout, j, kk, a.P, ck) : 0;
+      }
+      float p[4][4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          const bool vis = kvalid[y] && (!a.causal || kpos[y] <= qpos[x]);
+          s[x][y] = vis ? s[x][y] * a.tau : -INFINITY;
+          mx = fmaxf(mx, s[x][y]);
+        }
+        const float m_new = fmaxf(m[x], group_max(mx));
+        const float alpha = m_new == -INFINITY ? 1.f : expf(m[x] - m_new);
+        float sum = 0.f;
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          p[x][y] = s[x][y] == -INFINITY ? 0.f : expf(s[x][y] - m_new);
+          sum += p[x][y];
+        }
+        l[x] = alpha * l[x] + group_sum(sum);
+        m[x] = m_new;
+#pragma unroll
+        for (int c = 0; c < kCols; ++c)
+#pragma unroll
+          for (int y = 0; y < 4; ++y) o[x][c][y] *= alpha;
+      }
+      // P^T of the warp's rows, then o += p V over the tile's keys
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+        *reinterpret_cast<float4*>(pT + (4 * kg + y) * kQS + lrow0) =
+            make_float4(p[0][y], p[1][y], p[2][y], p[3][y]);
+      __syncwarp();
+#pragma unroll 4
+      for (int key = 0; key < kBN; ++key) {
+        const float4 pp = *reinterpret_cast<const float4*>(pT + key * kQS + lrow0);
+        const float pv[4] = {pp.x, pp.y, pp.z, pp.w};
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) {
+          const float4 vv = *reinterpret_cast<const float4*>(vs + key * (DT + 4) + 4 * kg + 32 * c);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            o[x][c][0] = fmaf(pv[x], vv.x, o[x][c][0]);
+            o[x][c][1] = fmaf(pv[x], vv.y, o[x][c][1]);
+            o[x][c][2] = fmaf(pv[x], vv.z, o[x][c][2]);
+            o[x][c][3] = fmaf(pv[x], vv.w, o[x][c][3]);
+          }
+        }
+      }
+    }
+  }
+
+  // write the rows: out = o / l and lse, or the state (m, l, o)
+  float* mo = a.mode == kPartial ? a.part.m[g] : a.st_m;
+  float* lo = a.mode == kPartial ? a.part.l[g] : a.st_l;
+  float* oo = a.mode == kPartial ? a.part.o[g] : a.st_o;
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    if (!rvalid[x]) continue;
+    const int64_t row = slice * a.nq + qpos[x];
+    if (a.mode == kForward) {
+      float* out = static_cast<float*>(a.out) + row * d;
+      const float inv = 1.f / l[x];
+#pragma unroll
+      for (int c = 0; c < kCols; ++c)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          const int e = 4 * kg + 32 * c + y;
+          if (e < d) out[e] = o[x][c][y] * inv;
+        }
+      if (kg == 0) a.lse[row] = m[x] + logf(l[x]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < kCols; ++c)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          const int e = 4 * kg + 32 * c + y;
+          if (e < d) oo[row * d + e] = o[x][c][y];
+        }
+      if (kg == 0) {
+        mo[row] = m[x];
+        lo[row] = l[x];
+      }
+    }
+  }
+}
+
+template <int DT>
+cudaError_t launch_dt(const FoldArgs& a, cudaStream_t s) {
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(fold_f32_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Smem<DT>::kBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const int64_t cq = a.nq / a.P;
+  const int64_t tiles_q = (cq + kBM - 1) / kBM;
+  const dim3 grid(static_cast<unsigned>(a.slices * a.P * tiles_q), static_cast<unsigned>(a.G));
+  fold_f32_kernel<DT><<<grid, kThreads, Smem<DT>::kBytes, s>>>(a);
+  return cudaGetLastError();
+}
+
+// ---- small problems: one warp per query row ----
+// When the tiled kernel would launch only a few CTAs (a few hundred query
+// rows), one warp per row spreads the rows over more SMs.  Each warp walks
+// the blocks in ring order 32 keys at a time, one key per lane, and the lanes
+// split o (lane e holds o[e], o[e + 32], ...).
+
+constexpr int kWarps = 4;
 
 // Block holding position n.
 __device__ __forceinline__ int64_t block_of(int layout, int64_t n, int64_t P, int64_t c) {
@@ -84,7 +361,7 @@ __device__ __forceinline__ float dot_row(const float* __restrict__ qrow,
 }
 
 template <int DV>  // o values per lane: d <= 32 * DV
-__global__ void __launch_bounds__(kWarps * 32) fold_f32_kernel(const FoldArgs a) {
+__global__ void __launch_bounds__(kWarps * 32) fold_f32_rows_kernel(const FoldArgs a) {
   __shared__ __align__(16) float qs[kWarps][32 * DV];
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -187,17 +464,25 @@ template <int DV>
 cudaError_t launch_dv(const FoldArgs& a, cudaStream_t s) {
   const int64_t rows = a.slices * a.nq;
   const dim3 grid(static_cast<unsigned>((rows + kWarps - 1) / kWarps), static_cast<unsigned>(a.G));
-  fold_f32_kernel<DV><<<grid, kWarps * 32, 0, s>>>(a);
+  fold_f32_rows_kernel<DV><<<grid, kWarps * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fold_f32(const FoldArgs& a, cudaStream_t s) {
-  if (a.d <= 32) return launch_dv<1>(a, s);
-  if (a.d <= 64) return launch_dv<2>(a, s);
-  if (a.d <= 128) return launch_dv<4>(a, s);
-  if (a.d <= 256) return launch_dv<8>(a, s);
+  if (a.slices * a.nq == 0) return cudaSuccess;
+  const int64_t tiled_ctas = a.slices * a.P * ((a.nq / a.P + kBM - 1) / kBM) * a.G;
+  if (tiled_ctas < kSmallGrid) {
+    if (a.d <= 32) return launch_dv<1>(a, s);
+    if (a.d <= 64) return launch_dv<2>(a, s);
+    if (a.d <= 128) return launch_dv<4>(a, s);
+    if (a.d <= 256) return launch_dv<8>(a, s);
+    return cudaErrorInvalidValue;
+  }
+  if (a.d <= 64) return launch_dt<64>(a, s);
+  if (a.d <= 128) return launch_dt<128>(a, s);
+  if (a.d <= 256) return launch_dt<256>(a, s);
   return cudaErrorInvalidValue;
 }
 

@@ -83,6 +83,59 @@ def test_ragged_shapes(O, shape, P):
     check_forward(O, q, k, v, P, out, lse)
 
 
+# Shapes large enough for the tiled fp32 kernel (at least 32 CTAs of 64
+# query rows): ragged query tiles and K/V tiles, d in every width class.
+TILED = [((2, 4, 1000, 100), 4), ((1, 8, 512, 256), 2), ((1, 16, 300, 33), 3),
+         ((2, 8, 256, 64), 1), ((1, 12, 600, 128), 5)]
+
+
+@pytest.mark.parametrize("shape,P", TILED)
+def test_tiled_shapes(O, shape, P):
+    g = torch.Generator(device=DEV).manual_seed(sum(shape) * 17 + P)
+    q, k, v = (torch.randn(shape, device=DEV, generator=g) * 1.5 for _ in range(3))
+    out, lse = ra.ra_forward(q, k, v, P=P)
+    check_forward(O, q, k, v, P, out, lse)
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
+def test_tiled_causal(O, layout):
+    B, H, N, d, P = 1, 8, 1024, 72, 4
+    g = torch.Generator(device=DEV).manual_seed(71)
+    q, k, v = (torch.randn(B, H, N, d, device=DEV, generator=g) * 1.5 for _ in range(3))
+    out, lse = ra.ra_forward_causal(q, k, v, P, layout=layout)
+    check_forward(O, q, k, v, P, out, lse, causal=True, layout=layout)
+
+
+def test_tiled_partials_and_fold_chain(O):
+    """Partial states (G = 3) and a chain of ra_fold calls through the tiled
+    kernel (ra_fold of 8 x 256 rows: 32 CTAs), against the oracle's segment
+    states and the forward."""
+    B, H, N, d, P = 1, 8, 1536, 40, 6
+    c = N // P
+    g = torch.Generator(device=DEV).manual_seed(72)
+    q, k, v = (torch.randn(B, H, N, d, device=DEV, generator=g) for _ in range(3))
+    out_f, lse_f = ra.ra_forward(q, k, v, P=P)
+    check_forward(O, q, k, v, P, out_f, lse_f)
+    parts = ra.ra_forward_partial(q, k, v, P=P, G=3)
+    for gi in range(3):
+        _, _, m, l, o = oracle_ring(O, q, k, v, P, t0=2 * gi, t1=2 * gi + 2, state=True)
+        assert max_err(parts[gi].m, m) <= 1e-5
+        assert np.max(np.abs(parts[gi].l.double().cpu().numpy() / l - 1)) <= 1e-5
+        check_close(parts[gi].o / parts[gi].l[:, None], o / l[:, None], torch.float32,
+                    f"tiled partial {gi} o/l", 1e-5)
+    order = O.ring_order(P)
+    i = 2
+    st = ra.ra_state_init(ra.new_state(B * H * c, d))
+    qi = q[:, :, i * c:(i + 1) * c].reshape(B * H, c, d).contiguous()
+    for t in range(P):
+        j = int(order[i, t])
+        ra.ra_fold(st, qi, k[:, :, j * c:(j + 1) * c].reshape(B * H, c, d).contiguous(),
+                   v[:, :, j * c:(j + 1) * c].reshape(B * H, c, d).contiguous(), batch=B * H)
+    out, lse = ra.ra_merge([st], out_dtype=torch.float32)
+    check_same(out, out_f[:, :, i * c:(i + 1) * c].reshape(-1, d), torch.float32,
+               "tiled fold chain vs forward", 1e-5)
+
+
 def test_partial_and_merge_equal_forward(O):
     B, H, N, d, P = 1, 2, 96, 48, 6
     g = torch.Generator(device=DEV).manual_seed(5)
