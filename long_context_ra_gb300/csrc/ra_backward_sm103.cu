@@ -817,41 +817,37 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
     if (lane == 0) {
       const uint64_t dQ = desc_sw128(base + L::kQ, 16, 1024);
       const uint64_t dDO = desc_sw128(base + L::kDO, 16, 1024);
-      auto kdesc = [&](int it, uint32_t lbo) {
-        return desc_sw128(base + L::kK0 + (it % L::kKStages) * T::kTileBytes, lbo, 1024);
-      };
-      auto wait_k = [&](int it) {
-        return wait1(k_full(it % L::kKStages),
-                     static_cast<uint32_t>((it / L::kKStages) & 1), ab);
-      };
-      // S(it) = Q K(it)^T into buffer it % 2, then signal it
-      auto issue_s = [&](int it) {
-        tc_fence_after();
-        mma_nt<D>(tS(it), dQ, kdesc(it, 16));
-        mma_commit(s_full(it & 1));
-      };
-      // dP(it) = dO V(it)^T, then signal it and free V(it)
-      auto issue_dp = [&](int it) {
-        const int vs = it % L::kVStages;
-        if (!wait1(v_full(vs), static_cast<uint32_t>((it / L::kVStages) & 1), ab)) return false;
-        tc_fence_after();
-        mma_nt<D>(tP, dDO, desc_sw128(base + L::kV0 + vs * T::kTileBytes, 16, 1024));
-        mma_commit(dp_full);
-        mma_commit(v_empty(vs));
-        return true;
-      };
+      const uint32_t k0 = base + L::kK0;  // K stage 0; stage s at + s * kTileBytes
+      // Per key tile it: S(it) = Q K(it)^T into S buffer it % 2 (s_full),
+      // dP(it) = dO V(it)^T (dp_full; frees V(it)), then dQ += dS K over the
+      // parts of pass B.
       bool ok = wait1(q_full, 0, ab);
       if (ok && n_iter > 0) {
-        ok = wait_k(0);
-        if (ok) issue_s(0);
-        if (ok) ok = issue_dp(0);
+        ok = wait1(k_full(0), 0, ab);
+        if (ok) {
+          tc_fence_after();
+          mma_nt<D>(tS(0), dQ, desc_sw128(k0, 16, 1024));
+          mma_commit(s_full(0));
+          ok = wait1(v_full(0), 0, ab);
+        }
+        if (ok) {
+          tc_fence_after();
+          mma_nt<D>(tP, dDO, desc_sw128(base + L::kV0, 16, 1024));
+          mma_commit(dp_full);
+          mma_commit(v_empty(0));
+        }
         if (ok && n_iter > 1) {
-          ok = wait_k(1);
-          if (ok) issue_s(1);
+          ok = wait1(k_full(1 % L::kKStages), static_cast<uint32_t>((1 / L::kKStages) & 1), ab);
+          if (ok) {
+            tc_fence_after();
+            mma_nt<D>(tS(1), dQ, desc_sw128(k0 + (1 % L::kKStages) * T::kTileBytes, 16, 1024));
+            mma_commit(s_full(1));
+          }
         }
       }
       for (int it = 0; it < n_iter && ok; ++it) {
-        const uint64_t dKs = kdesc(it, T::kBoxBytes);
+        const uint64_t dKs =
+            desc_sw128(k0 + (it % L::kKStages) * T::kTileBytes, T::kBoxBytes, 1024);
         for (int h = 0; h < kParts && ok; ++h) {
           if (!wait1(pb(h), static_cast<uint32_t>(it & 1), ab)) {
             ok = false;
@@ -865,16 +861,26 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
         // dP(it+1) overwrites dS(it) (read by the dQ products above, earlier
         // in the pipe) and dP(it) (read by pass B, complete); S(it+2) goes to
         // the buffer of S(it), whose p pass B has read too.
-        if (it + 1 < n_iter && !issue_dp(it + 1)) {
-          ok = false;
-          break;
-        }
-        if (it + 2 < n_iter) {
-          if (!wait_k(it + 2)) {
+        if (it + 1 < n_iter) {
+          const int vs = (it + 1) % L::kVStages;
+          if (!wait1(v_full(vs), static_cast<uint32_t>(((it + 1) / L::kVStages) & 1), ab)) {
             ok = false;
             break;
           }
-          issue_s(it + 2);
+          tc_fence_after();
+          mma_nt<D>(tP, dDO, desc_sw128(base + L::kV0 + vs * T::kTileBytes, 16, 1024));
+          mma_commit(dp_full);
+          mma_commit(v_empty(vs));
+        }
+        if (it + 2 < n_iter) {
+          const int ks = (it + 2) % L::kKStages;
+          if (!wait1(k_full(ks), static_cast<uint32_t>(((it + 2) / L::kKStages) & 1), ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_nt<D>(tS(it + 2), dQ, desc_sw128(k0 + ks * T::kTileBytes, 16, 1024));
+          mma_commit(s_full((it + 2) & 1));
         }
       }
       if (ok) {
