@@ -8,11 +8,14 @@
 // the key-value blocks carrying their gradient accumulators).
 //
 // The fp32 path has two kernels, neither with atomics:
-//   dq: one warp per query row walks the key blocks in ring order
-//       (i - t) mod P, as the forward does;
-//   dkv: one warp per key row walks the query blocks its block visits on the
-//       ring, (j + t) mod P, and accumulates dK and dV for its row.
-// Lanes split the head dimension (lane e holds elements e, e + 32, ...).
+//   dq: query rows walk the key blocks in ring order (i - t) mod P, as the
+//       forward does;
+//   dkv: key rows walk the query blocks their block visits on the ring,
+//       (j + t) mod P, and accumulate dK and dV.
+// For d <= 128 and grids of 128 CTAs or more both are tiled (64 stationary
+// rows per CTA, 32-row tiles of the other side staged in shared memory);
+// otherwise one warp owns one row and the lanes split the head dimension
+// (lane e holds elements e, e + 32, ...).
 // Causal ("Ring attention, explained", "The causal-mask catch"): a query at
 // position n sees keys at positions <= n; `layout` says which positions form
 // each block (contiguous, zigzag or striped), as in the forward.
@@ -291,6 +294,344 @@ cudaError_t launch_bwd_dv(const BackwardArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+
+// ---- tiled kernels (d <= 128, grids of 128 CTAs or more) ----
+// As the tiled forward: a CTA of 4 warps keeps 64 rows stationary and
+// streams 32-row tiles of the other side through shared memory; lane (rg,
+// kg) = (lane / 8, lane % 8) of warp w computes the 4 x 4 blocks of rows
+// 16w + 4rg + 0..3 against streamed rows 4kg + 0..3 and accumulates its
+// rows' gradients in columns 4kg + 32m + 0..3.  Tiles used as a product's
+// reduction operand are stored transposed ([d][rows]) for 16-byte reads.
+constexpr int kTT = 128;        // threads
+constexpr int kTM = 64;         // stationary rows per CTA
+constexpr int kTN = 32;         // streamed rows per tile
+constexpr int kSS = kTM + 4;    // row stride of transposed stationary tiles, P^T, dS^T
+constexpr int kNS = kTN + 4;    // row stride of transposed streamed tiles
+// Each tiled CTA takes a whole SM (up to 158 KB of shared memory): below
+// about one CTA per SM the row kernels, with 16 x more CTAs, are faster.
+constexpr int64_t kTiledMinCtas = 128;
+
+template <int DT>
+struct DqSmem {  // floats
+  static constexpr int kQ = 0;                    // Q^T   [DT][kSS]
+  static constexpr int kG = kQ + DT * kSS;        // dO^T  [DT][kSS]
+  static constexpr int kK = kG + DT * kSS;        // K^T   [DT][kNS]
+  static constexpr int kV = kK + DT * kNS;        // V^T   [DT][kNS]
+  static constexpr int kKr = kV + DT * kNS;       // K     [kTN][DT + 4]
+  static constexpr int kDS = kKr + kTN * (DT + 4);  // dS^T [kTN][kSS]
+  static constexpr int kBytes = (kDS + kTN * kSS) * 4;
+};
+
+template <int DT>
+struct DkvSmem {  // floats
+  static constexpr int kK = 0;                    // K^T   [DT][kSS]
+  static constexpr int kV = kK + DT * kSS;        // V^T   [DT][kSS]
+  static constexpr int kQ = kV + DT * kSS;        // Q^T   [DT][kNS]
+  static constexpr int kG = kQ + DT * kNS;        // dO^T  [DT][kNS]
+  static constexpr int kQr = kG + DT * kNS;       // Q     [kTN][DT + 4]
+  static constexpr int kGr = kQr + kTN * (DT + 4);  // dO  [kTN][DT + 4]
+  static constexpr int kP = kGr + kTN * (DT + 4);   // P^T  [kTN][kSS]
+  static constexpr int kDS = kP + kTN * kSS;        // dS^T [kTN][kSS]
+  static constexpr int kBytes = (kDS + kTN * kSS) * 4;
+};
+
+// s[x][y] += a[e][r0 + x] * b[e][c0 + y] and t[x][y] += c[e][r0 + x] * f[e][c0 + y]
+// over e < d: the two 4 x 4 score blocks of a lane from transposed tiles.
+__device__ __forceinline__ void two_blocks(const float* a, const float* b, const float* c,
+                                           const float* f, int d, int sa, int sb, int r0,
+                                           int c0, float (&s)[4][4], float (&t)[4][4]) {
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y) s[x][y] = t[x][y] = 0.f;
+#pragma unroll 2
+  for (int e = 0; e < d; ++e) {
+    const float4 a4 = *reinterpret_cast<const float4*>(a + e * sa + r0);
+    const float4 b4 = *reinterpret_cast<const float4*>(b + e * sb + c0);
+    const float4 c4 = *reinterpret_cast<const float4*>(c + e * sa + r0);
+    const float4 f4 = *reinterpret_cast<const float4*>(f + e * sb + c0);
+    const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+    const float cv[4] = {c4.x, c4.y, c4.z, c4.w}, fv[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        s[x][y] = fmaf(av[x], bv[y], s[x][y]);
+        t[x][y] = fmaf(cv[x], fv[y], t[x][y]);
+      }
+  }
+}
+
+// acc[x][m][y] += sum over the tile's rows k of wT[k][r0 + x] * src[k][4 kg + 32 m + y]
+template <int DT>
+__device__ __forceinline__ void accumulate_rows(const float* wT, const float* src, int r0, int kg,
+                                                float (&acc)[4][DT / 32][4]) {
+#pragma unroll 4
+  for (int k = 0; k < kTN; ++k) {
+    const float4 w4 = *reinterpret_cast<const float4*>(wT + k * kSS + r0);
+    const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+    for (int m = 0; m < DT / 32; ++m) {
+      const float4 v4 = *reinterpret_cast<const float4*>(src + k * (DT + 4) + 4 * kg + 32 * m);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        acc[x][m][0] = fmaf(wv[x], v4.x, acc[x][m][0]);
+        acc[x][m][1] = fmaf(wv[x], v4.y, acc[x][m][1]);
+        acc[x][m][2] = fmaf(wv[x], v4.z, acc[x][m][2]);
+        acc[x][m][3] = fmaf(wv[x], v4.w, acc[x][m][3]);
+      }
+    }
+  }
+}
+
+// Stationary tile of 64 rows (block b, local rows r0 ..), transposed: the
+// column e of row x at dst[e * kSS + x]; rows past the block and columns
+// past d are zero.
+template <int DT>
+__device__ __forceinline__ void load_stationary(float* dst, const float* src, int layout, int b,
+                                                int64_t r0, int64_t P, int64_t c, int d,
+                                                int tid) {
+  for (int x = tid; x < kTM * DT; x += kTT) {
+    const int row = x / DT, e = x % DT;
+    const int64_t r = r0 + row;
+    float val = 0.f;
+    if (r < c && e < d) val = src[bpos(layout, b, r, P, c) * d + e];
+    dst[e * kSS + row] = val;
+  }
+}
+
+// Streamed tile of 32 rows (block b, local rows r0 ..): transposed into dT
+// (column e of row x at dT[e * kNS + x]) and, if dR, row-major into dR.
+template <int DT>
+__device__ __forceinline__ void load_streamed(float* dT, float* dR, const float* src, int layout,
+                                              int b, int64_t r0, int64_t P, int64_t c, int d,
+                                              int tid) {
+  for (int x = tid; x < kTN * DT; x += kTT) {
+    const int row = x / DT, e = x % DT;
+    const int64_t r = r0 + row;
+    float val = 0.f;
+    if (r < c && e < d) val = src[bpos(layout, b, r, P, c) * d + e];
+    dT[e * kNS + row] = val;
+    if (dR) dR[row * (DT + 4) + e] = val;
+  }
+}
+
+// dQ for 64 query rows of block i: the key blocks in ring order (i - t) mod P.
+template <int DT>
+__global__ void __launch_bounds__(kTT) dq_f32_tiled(const BackwardArgs a) {
+  using S = DqSmem<DT>;
+  extern __shared__ __align__(16) float sm[];
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int rg = lane / 8, kg = lane % 8;
+  const int d = a.d;
+  const int64_t c = a.N / a.P;
+  const int64_t tiles = (c + kTM - 1) / kTM;
+  int64_t u = blockIdx.x;
+  const int64_t qt = u % tiles;
+  u /= tiles;
+  const int i = static_cast<int>(u % a.P);
+  const int64_t slice = u / a.P;
+  const int64_t sb = slice * a.N;
+  const float* q = static_cast<const float*>(a.q) + sb * d;
+  const float* k = static_cast<const float*>(a.k) + sb * d;
+  const float* v = static_cast<const float*>(a.v) + sb * d;
+  const float* g = static_cast<const float*>(a.dout) + sb * d;
+  const int64_t r0 = qt * kTM;
+  load_stationary<DT>(sm + S::kQ, q, a.layout, i, r0, a.P, c, d, tid);
+  load_stationary<DT>(sm + S::kG, g, a.layout, i, r0, a.P, c, d, tid);
+
+  const int lrow0 = 16 * warp + 4 * rg;
+  int64_t qpos[4];
+  bool rvalid[4];
+  float lse[4], D[4];
+  float acc[4][DT / 32][4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const int64_t r = r0 + lrow0 + x;
+    rvalid[x] = r < c;
+    qpos[x] = rvalid[x] ? bpos(a.layout, i, r, a.P, c) : 0;
+    lse[x] = rvalid[x] ? a.lse[sb + qpos[x]] : 0.f;
+    D[x] = rvalid[x] ? a.delta[sb + static_cast<int64_t>(i) * c + r] : 0.f;
+#pragma unroll
+    for (int m = 0; m < DT / 32; ++m)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) acc[x][m][y] = 0.f;
+  }
+  const int64_t rlast = (r0 + kTM < c ? r0 + kTM : c) - 1;
+  const int64_t qlast = bpos(a.layout, i, rlast, a.P, c);
+
+  for (int t = 0; t < a.P; ++t) {
+    int j = (i - t) % a.P;
+    if (j < 0) j += a.P;
+    for (int64_t c0 = 0; c0 < c; c0 += kTN) {
+      if (a.causal && bpos(a.layout, j, c0, a.P, c) > qlast) break;  // rest of block masked
+      __syncthreads();
+      load_streamed<DT>(sm + S::kK, sm + S::kKr, k, a.layout, j, c0, a.P, c, d, tid);
+      load_streamed<DT>(sm + S::kV, nullptr, v, a.layout, j, c0, a.P, c, d, tid);
+      __syncthreads();
+      float s[4][4], dp[4][4];
+      two_blocks(sm + S::kQ, sm + S::kK, sm + S::kG, sm + S::kV, d, kSS, kNS, lrow0, 4 * kg, s,
+                 dp);
+      float ds[4][4];
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const int64_t kk = c0 + 4 * kg + y;
+        const bool kvalid = kk < c;
+        const int64_t kpos = kvalid ? bpos(a.layout, j, kk, a.P, c) : 0;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const bool vis = kvalid && rvalid[x] && (!a.causal || kpos <= qpos[x]);
+          const float p = vis ? expf(s[x][y] * a.tau - lse[x]) : 0.f;
+          ds[x][y] = p * (dp[x][y] - D[x]);
+        }
+      }
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+        *reinterpret_cast<float4*>(sm + S::kDS + (4 * kg + y) * kSS + lrow0) =
+            make_float4(ds[0][y], ds[1][y], ds[2][y], ds[3][y]);
+      __syncwarp();
+      accumulate_rows<DT>(sm + S::kDS, sm + S::kKr, lrow0, kg, acc);
+    }
+  }
+  float* dq = static_cast<float*>(a.dq);
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    if (!rvalid[x]) continue;
+    const int64_t row = (sb + qpos[x]) * d;
+#pragma unroll
+    for (int m = 0; m < DT / 32; ++m)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const int e = 4 * kg + 32 * m + y;
+        if (e < d) dq[row + e] = (a.accumulate ? dq[row + e] : 0.f) + acc[x][m][y] * a.tau;
+      }
+  }
+}
+
+// dK, dV for 64 key rows of block j: the query blocks (j + t) mod P.
+template <int DT>
+__global__ void __launch_bounds__(kTT) dkv_f32_tiled(const BackwardArgs a) {
+  using S = DkvSmem<DT>;
+  extern __shared__ __align__(16) float sm[];
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int rg = lane / 8, kg = lane % 8;
+  const int d = a.d;
+  const int64_t c = a.N / a.P;
+  const int64_t tiles = (c + kTM - 1) / kTM;
+  int64_t u = blockIdx.x;
+  const int64_t kt = u % tiles;
+  u /= tiles;
+  const int j = static_cast<int>(u % a.P);
+  const int64_t slice = u / a.P;
+  const int64_t sb = slice * a.N;
+  const float* q = static_cast<const float*>(a.q) + sb * d;
+  const float* k = static_cast<const float*>(a.k) + sb * d;
+  const float* v = static_cast<const float*>(a.v) + sb * d;
+  const float* g = static_cast<const float*>(a.dout) + sb * d;
+  const int64_t r0 = kt * kTM;
+  load_stationary<DT>(sm + S::kK, k, a.layout, j, r0, a.P, c, d, tid);
+  load_stationary<DT>(sm + S::kV, v, a.layout, j, r0, a.P, c, d, tid);
+
+  const int lrow0 = 16 * warp + 4 * rg;
+  int64_t kpos[4];
+  bool rvalid[4];
+  float gk[4][DT / 32][4], gv[4][DT / 32][4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const int64_t r = r0 + lrow0 + x;
+    rvalid[x] = r < c;
+    kpos[x] = rvalid[x] ? bpos(a.layout, j, r, a.P, c) : 0;
+#pragma unroll
+    for (int m = 0; m < DT / 32; ++m)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) gk[x][m][y] = gv[x][m][y] = 0.f;
+  }
+  const int64_t kfirst = bpos(a.layout, j, r0, a.P, c);  // the CTA's first key position
+
+  for (int t = 0; t < a.P; ++t) {
+    const int i = (j + t) % a.P;  // the query block this key block meets at step t
+    for (int64_t c0 = 0; c0 < c; c0 += kTN) {
+      // causal: a query tile whose last query precedes every key here sees none
+      if (a.causal) {
+        const int64_t qe = (c0 + kTN < c ? c0 + kTN : c) - 1;
+        if (bpos(a.layout, i, qe, a.P, c) < kfirst) continue;
+      }
+      __syncthreads();
+      load_streamed<DT>(sm + S::kQ, sm + S::kQr, q, a.layout, i, c0, a.P, c, d, tid);
+      load_streamed<DT>(sm + S::kG, sm + S::kGr, g, a.layout, i, c0, a.P, c, d, tid);
+      __syncthreads();
+      float s[4][4], dp[4][4];
+      two_blocks(sm + S::kK, sm + S::kQ, sm + S::kV, sm + S::kG, d, kSS, kNS, lrow0, 4 * kg, s,
+                 dp);
+      float p[4][4], ds[4][4];
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const int64_t qq = c0 + 4 * kg + y;
+        const bool qvalid = qq < c;
+        const int64_t qpos = qvalid ? bpos(a.layout, i, qq, a.P, c) : 0;
+        const float lse = qvalid ? a.lse[sb + qpos] : 0.f;
+        const float D = qvalid ? a.delta[sb + static_cast<int64_t>(i) * c + qq] : 0.f;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const bool vis = qvalid && rvalid[x] && (!a.causal || qpos >= kpos[x]);
+          p[x][y] = vis ? expf(s[x][y] * a.tau - lse) : 0.f;
+          ds[x][y] = p[x][y] * (dp[x][y] - D);
+        }
+      }
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        *reinterpret_cast<float4*>(sm + S::kP + (4 * kg + y) * kSS + lrow0) =
+            make_float4(p[0][y], p[1][y], p[2][y], p[3][y]);
+        *reinterpret_cast<float4*>(sm + S::kDS + (4 * kg + y) * kSS + lrow0) =
+            make_float4(ds[0][y], ds[1][y], ds[2][y], ds[3][y]);
+      }
+      __syncwarp();
+      accumulate_rows<DT>(sm + S::kP, sm + S::kGr, lrow0, kg, gv);
+      accumulate_rows<DT>(sm + S::kDS, sm + S::kQr, lrow0, kg, gk);
+    }
+  }
+  float* dk = static_cast<float*>(a.dk);
+  float* dv = static_cast<float*>(a.dv);
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    if (!rvalid[x]) continue;
+    const int64_t row = (sb + kpos[x]) * d;
+#pragma unroll
+    for (int m = 0; m < DT / 32; ++m)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const int e = 4 * kg + 32 * m + y;
+        if (e < d) {
+          dk[row + e] = (a.accumulate ? dk[row + e] : 0.f) + gk[x][m][y] * a.tau;
+          dv[row + e] = (a.accumulate ? dv[row + e] : 0.f) + gv[x][m][y];
+        }
+      }
+  }
+}
+
+template <int DT>
+cudaError_t launch_tiled(const BackwardArgs& a, cudaStream_t s) {
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(dq_f32_tiled<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DqSmem<DT>::kBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(dkv_f32_tiled<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               DkvSmem<DT>::kBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const int64_t c = a.N / a.P;
+  const unsigned grid = static_cast<unsigned>(a.slices * a.P * ((c + kTM - 1) / kTM));
+  dq_f32_tiled<DT><<<grid, kTT, DqSmem<DT>::kBytes, s>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dkv_f32_tiled<DT><<<grid, kTT, DkvSmem<DT>::kBytes, s>>>(a);
+  return cudaGetLastError();
+}
 }  // namespace
 
 cudaError_t launch_delta(const void* out, const void* dout, const float* lse, float* delta,
@@ -307,6 +648,11 @@ cudaError_t launch_delta(const void* out, const void* dout, const float* lse, fl
 }
 
 cudaError_t launch_backward_f32(const BackwardArgs& a, cudaStream_t s) {
+  const int64_t tiled_ctas = a.slices * a.P * ((a.N / a.P + kTM - 1) / kTM);
+  if (a.d <= 128 && tiled_ctas >= kTiledMinCtas) {
+    if (a.d <= 64) return launch_tiled<64>(a, s);
+    return launch_tiled<128>(a, s);
+  }
   if (a.d <= 32) return launch_bwd_dv<1>(a, s);
   if (a.d <= 64) return launch_bwd_dv<2>(a, s);
   if (a.d <= 128) return launch_bwd_dv<4>(a, s);

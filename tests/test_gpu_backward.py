@@ -66,6 +66,24 @@ def test_f32_backward(O, shape, P):
     full_check(O, q, k, v, P, torch.float32)
 
 
+# fp32 shapes large enough for the tiled kernels (d <= 128, 128 CTAs or more
+# of 64 rows): ragged 64-row and 32-row tiles, d in both width classes
+F32_TILED = [((1, 8, 1000, 100), 4), ((4, 8, 384, 40), 3), ((1, 32, 256, 128), 2),
+             ((1, 16, 1024, 64), 1)]
+
+
+@pytest.mark.parametrize("shape,P", F32_TILED)
+def test_f32_backward_tiled(O, shape, P):
+    q, k, v = (rnd(shape, 60 + s, torch.float32, 1.3) for s in range(3))
+    full_check(O, q, k, v, P, torch.float32)
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
+def test_f32_backward_tiled_causal(O, layout):
+    q, k, v = (rnd((1, 8, 1024, 72), 64 + s, torch.float32, 1.3) for s in range(3))
+    full_check(O, q, k, v, 4, torch.float32, causal=layout)
+
+
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("B,H,N,P", [(1, 1, 256, 1), (1, 2, 512, 2), (2, 1, 768, 3),
                                      (1, 2, 1024, 8)])

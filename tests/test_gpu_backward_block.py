@@ -76,6 +76,38 @@ def test_ring_of_blocks_on_one_gpu(O, dtype, d, c, causal):
         check_close(got, want, dtype, f"ring of blocks {name}", tol)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_of_fp32_blocks_tiled(O, causal):
+    """The fp32 block steps with enough rows for the tiled kernels (64 heads
+    of 128-row blocks: 128 CTAs a step), accumulating across the ring."""
+    B, H, P, c, d = 1, 64, 4, 128, 72
+    N, bh = P * c, B * H
+    q, k, v, dout = (rnd((B, H, N, d), 840 + s, torch.float32) for s in range(4))
+    out, lse = (ra.ra_forward_causal(q, k, v, P) if causal else ra.ra_forward(q, k, v, P))
+    blk = lambda t, j: t.reshape(bh, N, -1)[:, j * c:(j + 1) * c].contiguous()
+    lse3 = lse.reshape(bh, N, 1)
+    rts = [ra.ra_backward_rowterms(blk(out, i), blk(dout, i), blk(lse3, i).reshape(bh, c))
+           for i in range(P)]
+    dq = [torch.zeros(bh, c, d, device=DEV) for _ in range(P)]
+    dk = [torch.zeros(bh, c, d, device=DEV) for _ in range(P)]
+    dv = [torch.zeros(bh, c, d, device=DEV) for _ in range(P)]
+    for i in range(P):
+        for t in range(P):
+            j = (i - t) % P
+            if causal and j > i:
+                continue
+            ra.ra_backward_block(blk(q, i), blk(k, j), blk(v, j), blk(dout, i),
+                                 blk(lse3, i).reshape(bh, c), rts[i], dq[i], dk[j], dv[j],
+                                 causal=causal and j == i)
+    torch.cuda.synchronize()
+    assert ra.ra_last_device_status() == 0
+    wq, wk, wv = oracle_grads(O, q, k, v, out, dout, lse, P, causal)
+    cat = lambda xs: torch.cat(xs, dim=1)
+    for name, got, want in (("dq", cat(dq), wq), ("dk", cat(dk), wk), ("dv", cat(dv), wv)):
+        check_close(got, want, torch.float32, f"tiled fp32 ring of blocks {name}",
+                    1e-5 * max(1.0, float(np.abs(want).max())))
+
+
 def test_block_accumulates_into_existing_values():
     """Accumulators are added to, not overwritten."""
     bh, c, d = 2, 128, 64
