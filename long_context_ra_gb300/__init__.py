@@ -51,17 +51,25 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}: use bfloat16 or float32")
 
 
-def _stream(stream) -> ctypes.c_void_p:
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
-def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
+def _stream(stream) -> int:
+    """The CUDA stream handle (an int, which ctypes passes as a pointer): the
+    given stream, or the current one of the current device."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _ptr(t: torch.Tensor) -> int:
     if not t.is_cuda:
         raise ValueError("tensors must be on a CUDA device")
     if not t.is_contiguous():
         raise ValueError("tensors must be contiguous")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 @dataclass
@@ -84,7 +92,7 @@ class RaState:
         for t in (self.m, self.l, self.o):
             if t.dtype != torch.float32:
                 raise TypeError("state tensors must be float32")
-        return RaStateC(_ptr(self.m).value, _ptr(self.l).value, _ptr(self.o).value, self.rows,
+        return RaStateC(_ptr(self.m), _ptr(self.l), _ptr(self.o), self.rows,
                         self.d)
 
 
