@@ -228,7 +228,7 @@ def cpu_oracle_baseline(w, q, k, v, target_s: float):
     n = int(min(len(pool), max(16, len(probe) * target_s / max(t_probe, 1e-6))))
     rows = pool[np.linspace(0, len(pool) - 1, n).astype(np.int64)]
     t0 = time.perf_counter()
-    O.ring(qa, ka, va, w.P, dtype="bf16", rows=rows)
+    want = O.ring(qa, ka, va, w.P, dtype="bf16", rows=rows)
     dt = time.perf_counter() - t0
     # the same oracle on one core, on a sample sized for about 3 s
     O1 = ra_oracle.Oracle(threads=1)
@@ -242,7 +242,28 @@ def cpu_oracle_baseline(w, q, k, v, target_s: float):
                       f"value = rows x 4*N*d flops / time",
             "value_1core": n1 * per_row / dt1 / 1e12,
             "sample_1core": f"{n1} of those rows on one core, {dt1:.1f} s",
-            "projected_full_s": dt * w.rows / n}, n, dt
+            "projected_full_s": dt * w.rows / n}, rows, want
+
+
+def sampled_parity(out, lse, rows, w_out, w_lse, w) -> dict:
+    """The timed run's out and lse on the rows the CPU baseline computed,
+    against those oracle values (the parity bars of the tests)."""
+    import numpy as np
+    import torch
+
+    idx = torch.as_tensor(rows, device=out.device)
+    got_out = out.reshape(-1, w.d).index_select(0, idx).double().cpu().numpy()
+    got_lse = lse.reshape(-1).index_select(0, idx).double().cpu().numpy()
+    e_out = float(np.abs(got_out - w_out).max())
+    e_lse = float(np.abs(got_lse - w_lse).max())
+    ref = float(np.abs(w_out).max())
+    rms = float(np.sqrt(np.mean((got_out - w_out) ** 2)) / np.sqrt(np.mean(w_out ** 2)))
+    bars = {"max_abs_out": 2e-2, "max_abs_lse": 1e-3, "rel_max_out": 2.0 ** -6,
+            "rel_rms_out": 2.0 ** -7}
+    got = {"max_abs_out": e_out, "max_abs_lse": e_lse, "rel_max_out": e_out / ref,
+           "rel_rms_out": rms}
+    return {"rows": int(len(rows)), "against": "the fp64 oracle on the rows of cpu_baseline",
+            **got, "bars": bars, "pass": all(got[x] <= bars[x] for x in bars)}
 
 
 def run_reference(args, w) -> None:
@@ -478,10 +499,11 @@ def run_ours(args, w) -> None:
                 "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
                 if peaks["source"] == "measured" else "fallback 1.9 PFLOP/s bf16 burst"}
 
-    cpu = None
+    cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.causal \
             and not args.backward and args.ring is None:
-        cpu, _, _ = cpu_oracle_baseline(w, q, k, v, args.cpu_seconds)
+        cpu, rows, (w_out, w_lse) = cpu_oracle_baseline(w, q, k, v, args.cpu_seconds)
+        parity = sampled_parity(out, lse, rows, w_out, w_lse, w)
 
     if rank == 0:
         line = {
@@ -498,6 +520,7 @@ def run_ours(args, w) -> None:
                           if args.ring is not None else {}),
                        "l2": l2_note(w)},
             "roofline": roofline, "cpu_baseline": cpu,
+            **({"parity": parity} if parity else {}),
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e_max, "path": e2e_path,
                     "steps": n_e2e, "of_device_value": e2e_value / value,
