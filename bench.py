@@ -266,6 +266,35 @@ def sampled_parity(out, lse, rows, w_out, w_lse, w) -> dict:
             **got, "bars": bars, "pass": all(got[x] <= bars[x] for x in bars)}
 
 
+def backward_parity(q, k, v, out, dout, lse, grads, w, causal: bool) -> dict:
+    """dq of 64 seeded query rows and dk, dv of 64 seeded key rows of the
+    timed backward, against the fp64 oracle's per-row backward."""
+    import numpy as np
+    import torch
+
+    from long_context_ra_gb300 import synth
+    from oracle import ra_oracle
+
+    O = ra_oracle.get()
+    rows = synth.sample_rows(w, 64, seed=5).numpy()
+    bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).cpu().view(torch.int16).numpy().view(np.uint16)
+    want = O.backward_rows(bits(q), bits(k), bits(v), bits(out), bits(dout),
+                           lse.double().cpu().numpy(), rows, rows, dtype="bf16", causal=causal)
+    idx = torch.as_tensor(rows, device=q.device)
+    res = {}
+    ok = True
+    for name, got, wt in zip(("dq", "dk", "dv"), grads, want):
+        g = got.reshape(-1, w.d).index_select(0, idx).double().cpu().numpy()
+        e = float(np.abs(g - wt).max())
+        ref = float(np.abs(wt).max())
+        rms = float(np.sqrt(np.mean((g - wt) ** 2)) / np.sqrt(np.mean(wt ** 2)))
+        res[name] = {"max_abs": e, "rel_max": e / ref, "rel_rms": rms}
+        ok = ok and e <= 2e-2 * max(1.0, ref) and e / ref <= 2.0 ** -6 and rms <= 2.0 ** -7
+    return {"rows": int(len(rows)), "against": "the fp64 oracle's per-row backward",
+            **res, "bars": {"max_abs": "2e-2 max(1, max|ref|)", "rel_max": 2.0 ** -6,
+                            "rel_rms": 2.0 ** -7}, "pass": ok}
+
+
 def run_reference(args, w) -> None:
     """The CPU oracle as the reference arm, on this arm's workload and metric."""
     rank = int(os.environ.get("RANK", "0"))
@@ -504,6 +533,9 @@ def run_ours(args, w) -> None:
             and not args.backward and args.ring is None:
         cpu, rows, (w_out, w_lse) = cpu_oracle_baseline(w, q, k, v, args.cpu_seconds)
         parity = sampled_parity(out, lse, rows, w_out, w_lse, w)
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline and args.backward \
+            and args.causal in (None, "contiguous"):
+        parity = backward_parity(q, k, v, out0, dout, lse0, results, w, args.causal is not None)
 
     if rank == 0:
         line = {
