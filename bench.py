@@ -266,6 +266,25 @@ def sampled_parity(out, lse, rows, w_out, w_lse, w) -> dict:
             **got, "bars": bars, "pass": all(got[x] <= bars[x] for x in bars)}
 
 
+def causal_parity(q, k, v, out, lse, w, layout: str) -> dict:
+    """The timed causal forward's out and lse on 256 seeded rows against the
+    fp64 oracle's causal ring with the same layout."""
+    import numpy as np
+    import torch
+
+    from long_context_ra_gb300 import synth
+    from oracle import ra_oracle
+
+    O = ra_oracle.get()
+    rows = synth.sample_rows(w, 256, seed=11).numpy()
+    bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).cpu().view(torch.int16).numpy().view(np.uint16)
+    w_out, w_lse = O.ring(bits(q), bits(k), bits(v), w.P, dtype="bf16", rows=rows, causal=True,
+                          layout=layout)
+    par = sampled_parity(out, lse, rows, w_out, w_lse, w)
+    par["against"] = f"the fp64 oracle's causal ring ({layout}) on seeded rows"
+    return par
+
+
 def backward_parity(q, k, v, out, dout, lse, grads, w, causal: bool) -> dict:
     """dq of 64 seeded query rows and dk, dv of 64 seeded key rows of the
     timed backward, against the fp64 oracle's per-row backward."""
@@ -533,6 +552,9 @@ def run_ours(args, w) -> None:
             and not args.backward and args.ring is None:
         cpu, rows, (w_out, w_lse) = cpu_oracle_baseline(w, q, k, v, args.cpu_seconds)
         parity = sampled_parity(out, lse, rows, w_out, w_lse, w)
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline and args.causal \
+            and not args.backward:
+        parity = causal_parity(q, k, v, out, lse, w, args.causal)
     elif rank == 0 and world == 1 and not args.no_cpu_baseline and args.backward \
             and args.causal in (None, "contiguous"):
         parity = backward_parity(q, k, v, out0, dout, lse0, results, w, args.causal is not None)
