@@ -63,6 +63,33 @@ struct Smem {
   static constexpr int kBytes = kFloats * 4;
 };
 
+// The K/V tiles a CTA visits, in order: ring steps t = t0 .. t1 - 1 (block
+// j = (i - t) mod P), each block's 32-key tiles in local order, under the
+// causal mask only those starting at or before the CTA's last query.
+struct TileCursor {
+  int t, t1, i, j, P, layout;
+  bool causal;
+  int64_t c0, ck, qlast;
+  __device__ void set_block() {
+    j = (i - t) % P;
+    if (j < 0) j += P;
+  }
+  __device__ bool valid() const { return t < t1; }
+  // from (t, c0) forward to the first visible tile, or past the last step
+  __device__ void settle() {
+    while (t < t1) {
+      if (c0 < ck && !(causal && pos_of(layout, j, c0, P, ck) > qlast)) return;
+      ++t;
+      c0 = 0;
+      if (t < t1) set_block();
+    }
+  }
+  __device__ void advance() {
+    c0 += kBN;
+    settle();
+  }
+};
+
 // max / sum over the 8 lanes of a row group (lanes 8g .. 8g + 7)
 __device__ __forceinline__ float group_max(float x) {
   x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
@@ -154,13 +181,45 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
   const int64_t rlast = (r0 + kBM < cq ? r0 + kBM : cq) - 1;
   const int64_t qlast = pos_of(a.layout, i, rlast, a.P, cq);
 
-  for (int t = t0; t < t1; ++t) {
-    int j = (i - t) % a.P;
-    if (j < 0) j += a.P;
-    for (int64_t c0 = 0; c0 < ck; c0 += kBN) {
-      if (a.causal && pos_of(a.layout, j, c0, a.P, ck) > qlast) break;  // rest masked
-      __syncthreads();  // the previous tile's K, V and P are no longer read
-      // K^T and V tiles; keys past the block and columns past d are zero
+  // K^T and V tiles; keys past the block and columns past d are zero.  In
+  // the 128-wide class the next tile's values are fetched into registers
+  // while the current tile is computed (kPre of K and of V a thread); at
+  // DT = 64 the registers would cost a resident CTA per SM (measured slower),
+  // and at DT = 256 there are none to spare.
+  constexpr bool kPrefetch = DT == 128;
+  constexpr int kPre = kPrefetch ? kBN * DT / kThreads : 1;
+  float kr[kPre], vr[kPre];
+  TileCursor cur{t0, t1, i, 0, a.P, a.layout, a.causal != 0, 0, ck, qlast};
+  if (cur.valid()) cur.set_block();
+  cur.settle();
+  auto fetch = [&](const TileCursor& tc) {
+#pragma unroll
+    for (int it = 0; it < kPre; ++it) {
+      const int x = tid + it * kThreads;
+      const int key = x / DT, e = x % DT;
+      const int64_t kk = tc.c0 + key;
+      kr[it] = vr[it] = 0.f;
+      if (kk < ck && e < d) {
+        const int64_t row = pos_of(a.layout, tc.j, kk, a.P, ck);
+        kr[it] = kb[row * d + e];
+        vr[it] = vb[row * d + e];
+      }
+    }
+  };
+  if (kPrefetch && cur.valid()) fetch(cur);
+  while (cur.valid()) {
+    const int j = cur.j;
+    const int64_t c0 = cur.c0;
+    __syncthreads();  // the previous tile's K, V and P are no longer read
+    if (kPrefetch) {
+#pragma unroll
+      for (int it = 0; it < kPre; ++it) {
+        const int x = tid + it * kThreads;
+        const int key = x / DT, e = x % DT;
+        kT[e * kKS + key] = kr[it];
+        vs[key * (DT + 4) + e] = vr[it];
+      }
+    } else {
       for (int x = tid; x < kBN * DT; x += kThreads) {
         const int key = x / DT, e = x % DT;
         const int64_t kk = c0 + key;
@@ -173,7 +232,11 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
         kT[e * kKS + key] = kv;
         vs[key * (DT + 4) + e] = vv;
       }
-      __syncthreads();
+    }
+    __syncthreads();
+    cur.advance();
+    if (kPrefetch && cur.valid()) fetch(cur);  // in flight during this tile's math
+    {
 
       // scores of the lane's 4 rows x 4 keys
       float s[4][4];
