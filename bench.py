@@ -266,6 +266,27 @@ def sampled_parity(out, lse, rows, w_out, w_lse, w) -> dict:
             **got, "bars": bars, "pass": all(got[x] <= bars[x] for x in bars)}
 
 
+def ring_parity(ra, q, k, v, r_out, r_lse, w, R: int) -> dict:
+    """Every rank's out and lse of the played ring against the fused forward
+    of the same inputs (two routes of the library to the same rows)."""
+    import torch
+
+    out, lse = ra.ra_forward(q, k, v, w.P)
+    c, bh = w.N // R, w.B * w.H
+    e_out = e_lse = ref = 0.0
+    for i in range(R):
+        want = out[:, :, i * c:(i + 1) * c].reshape(bh * c, w.d).float()
+        e_out = max(e_out, (r_out[i].float() - want).abs().max().item())
+        ref = max(ref, want.abs().max().item())
+        wl = lse[:, :, i * c:(i + 1) * c].reshape(-1)
+        e_lse = max(e_lse, (r_lse[i] - wl).abs().max().item())
+    torch.cuda.synchronize()
+    bars = {"max_abs_out": 2e-2, "max_abs_lse": 1e-3, "rel_max_out": 2.0 ** -6}
+    got = {"max_abs_out": e_out, "max_abs_lse": e_lse, "rel_max_out": e_out / ref}
+    return {"rows": bh * w.N, "against": "ra_forward on the same inputs (every row)", **got,
+            "bars": bars, "pass": all(got[x] <= bars[x] for x in bars)}
+
+
 def causal_parity(q, k, v, out, lse, w, layout: str) -> dict:
     """The timed causal forward's out and lse on 256 seeded rows against the
     fp64 oracle's causal ring with the same layout."""
@@ -552,6 +573,8 @@ def run_ours(args, w) -> None:
             and not args.backward and args.ring is None:
         cpu, rows, (w_out, w_lse) = cpu_oracle_baseline(w, q, k, v, args.cpu_seconds)
         parity = sampled_parity(out, lse, rows, w_out, w_lse, w)
+    elif rank == 0 and world == 1 and args.ring is not None:
+        parity = ring_parity(ra, q, k, v, r_out, r_lse, w, args.ring)
     elif rank == 0 and world == 1 and not args.no_cpu_baseline and args.causal \
             and not args.backward:
         parity = causal_parity(q, k, v, out, lse, w, args.causal)
