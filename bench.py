@@ -287,9 +287,11 @@ def ring_parity(ra, q, k, v, r_out, r_lse, w, R: int) -> dict:
             "bars": bars, "pass": all(got[x] <= bars[x] for x in bars)}
 
 
-def causal_parity(q, k, v, out, lse, w, layout: str) -> dict:
-    """The timed causal forward's out and lse on 256 seeded rows against the
-    fp64 oracle's causal ring with the same layout."""
+def cpu_oracle_baseline_causal(w, q, k, v, layout: str, target_s: float):
+    """The CPU baseline of a causal forward: the fp64 oracle's causal ring
+    (same layout) timed on seeded query rows on all host cores, about
+    `target_s` seconds; a row at position n costs 4 d (n + 1) flops.
+    Returns (baseline, rows, the oracle's (out, lse) of those rows)."""
     import numpy as np
     import torch
 
@@ -297,18 +299,29 @@ def causal_parity(q, k, v, out, lse, w, layout: str) -> dict:
     from oracle import ra_oracle
 
     O = ra_oracle.get()
-    rows = synth.sample_rows(w, 256, seed=11).numpy()
     bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).cpu().view(torch.int16).numpy().view(np.uint16)
-    w_out, w_lse = O.ring(bits(q), bits(k), bits(v), w.P, dtype="bf16", rows=rows, causal=True,
-                          layout=layout)
-    par = sampled_parity(out, lse, rows, w_out, w_lse, w)
-    par["against"] = f"the fp64 oracle's causal ring ({layout}) on seeded rows"
-    return par
+    qa, ka, va = bits(q), bits(k), bits(v)
+    probe = synth.sample_rows(w, 16, seed=11).numpy()
+    t0 = time.perf_counter()
+    O.ring(qa, ka, va, w.P, dtype="bf16", rows=probe, causal=True, layout=layout)
+    t_probe = time.perf_counter() - t0
+    n = int(min(4096, max(64, len(probe) * target_s / max(t_probe, 1e-6))))
+    rows = synth.sample_rows(w, n, seed=11).numpy()
+    t0 = time.perf_counter()
+    want = O.ring(qa, ka, va, w.P, dtype="bf16", rows=rows, causal=True, layout=layout)
+    dt = time.perf_counter() - t0
+    flops = float(np.sum(4.0 * w.d * (rows % w.N + 1)))
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": O.threads, "kind": "oracle",
+            "sample": f"{len(rows)} seeded query rows of {w.name} under the causal mask "
+                      f"({layout}; fp64 ring), {dt:.1f} s; value = the rows' visible "
+                      f"4*d*(n+1) flops / time"}, rows, want
 
 
-def backward_parity(q, k, v, out, dout, lse, grads, w, causal: bool) -> dict:
-    """dq of 64 seeded query rows and dk, dv of 64 seeded key rows of the
-    timed backward, against the fp64 oracle's per-row backward."""
+def cpu_oracle_baseline_backward(w, q, k, v, out, dout, lse, causal: bool):
+    """The CPU baseline of a backward: the fp64 oracle's per-row backward
+    timed on all host cores for dq of 64 seeded query rows and dk, dv of 64
+    seeded key rows (a dq row costs 6 N d flops, a dk, dv row 8 N d).
+    Returns (baseline, rows, the oracle's (dq, dk, dv) of those rows)."""
     import numpy as np
     import torch
 
@@ -318,9 +331,30 @@ def backward_parity(q, k, v, out, dout, lse, grads, w, causal: bool) -> dict:
     O = ra_oracle.get()
     rows = synth.sample_rows(w, 64, seed=5).numpy()
     bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).cpu().view(torch.int16).numpy().view(np.uint16)
-    want = O.backward_rows(bits(q), bits(k), bits(v), bits(out), bits(dout),
-                           lse.double().cpu().numpy(), rows, rows, dtype="bf16", causal=causal)
-    idx = torch.as_tensor(rows, device=q.device)
+    args = (bits(q), bits(k), bits(v), bits(out), bits(dout), lse.double().cpu().numpy())
+    t0 = time.perf_counter()
+    want = O.backward_rows(*args, rows, rows, dtype="bf16", causal=causal)
+    dt = time.perf_counter() - t0
+    pos = (rows % w.N).astype(np.float64)
+    if causal:  # a query at position n meets n + 1 keys, a key N - n queries
+        flops = float(np.sum(6.0 * w.d * (pos + 1) + 8.0 * w.d * (w.N - pos)))
+    else:
+        flops = len(rows) * 14.0 * w.N * w.d
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": O.threads, "kind": "oracle",
+            "sample": f"dq of {len(rows)} seeded query rows and dk, dv of {len(rows)} seeded "
+                      f"key rows of {w.name} (fp64 per-row backward"
+                      f"{', causal' if causal else ''}), {dt:.2f} s; value = 6 d flops per "
+                      f"visible key of a dq row + 8 d per visible query of a dk, dv row, "
+                      f"/ time"}, rows, want
+
+
+def backward_parity(grads, rows, want, w) -> dict:
+    """dq, dk, dv of the timed backward on the rows of its CPU baseline,
+    against those oracle values (the tests' bars)."""
+    import numpy as np
+    import torch
+
+    idx = torch.as_tensor(rows, device=grads[0].device)
     res = {}
     ok = True
     for name, got, wt in zip(("dq", "dk", "dv"), grads, want):
@@ -330,9 +364,10 @@ def backward_parity(q, k, v, out, dout, lse, grads, w, causal: bool) -> dict:
         rms = float(np.sqrt(np.mean((g - wt) ** 2)) / np.sqrt(np.mean(wt ** 2)))
         res[name] = {"max_abs": e, "rel_max": e / ref, "rel_rms": rms}
         ok = ok and e <= 2e-2 * max(1.0, ref) and e / ref <= 2.0 ** -6 and rms <= 2.0 ** -7
-    return {"rows": int(len(rows)), "against": "the fp64 oracle's per-row backward",
-            **res, "bars": {"max_abs": "2e-2 max(1, max|ref|)", "rel_max": 2.0 ** -6,
-                            "rel_rms": 2.0 ** -7}, "pass": ok}
+    return {"rows": int(len(rows)), "against": "the fp64 oracle's per-row backward (the rows "
+            "of cpu_baseline)", **res,
+            "bars": {"max_abs": "2e-2 max(1, max|ref|)", "rel_max": 2.0 ** -6,
+                     "rel_rms": 2.0 ** -7}, "pass": ok}
 
 
 def run_reference(args, w) -> None:
@@ -577,10 +612,16 @@ def run_ours(args, w) -> None:
         parity = ring_parity(ra, q, k, v, r_out, r_lse, w, args.ring)
     elif rank == 0 and world == 1 and not args.no_cpu_baseline and args.causal \
             and not args.backward:
-        parity = causal_parity(q, k, v, out, lse, w, args.causal)
+        cpu, rows, (w_out, w_lse) = cpu_oracle_baseline_causal(w, q, k, v, args.causal,
+                                                                args.cpu_seconds)
+        parity = sampled_parity(out, lse, rows, w_out, w_lse, w)
+        parity["against"] = f"the fp64 oracle's causal ring ({args.causal}) on the rows of " \
+                            "cpu_baseline"
     elif rank == 0 and world == 1 and not args.no_cpu_baseline and args.backward \
             and args.causal in (None, "contiguous"):
-        parity = backward_parity(q, k, v, out0, dout, lse0, results, w, args.causal is not None)
+        cpu, rows, want = cpu_oracle_baseline_backward(w, q, k, v, out0, dout, lse0,
+                                                       args.causal is not None)
+        parity = backward_parity(results, rows, want, w)
 
     if rank == 0:
         line = {
