@@ -207,6 +207,18 @@ def job_throughput(flops_per_replica: float, world: int, ms_max: float) -> float
     return world * flops_per_replica / (ms_max * 1e-3) / 1e12
 
 
+def oracle_view(t, w):
+    """(array, dtype tag) of a [B, H, N, d] tensor for the oracle: bf16 as its
+    bit patterns, fp32 as is (the oracle widens both exactly)."""
+    import numpy as np
+    import torch
+
+    t = t.reshape(w.B * w.H, w.N, w.d).cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16), "bf16"
+    return t.float().numpy(), "f32"
+
+
 def cpu_oracle_baseline(w, q, k, v, target_s: float):
     """Time the fp64 oracle (as it stands) on a bounded, seeded sample of the
     workload's query rows on all host cores; scale to TFLOP/s."""
@@ -216,26 +228,25 @@ def cpu_oracle_baseline(w, q, k, v, target_s: float):
     from oracle import ra_oracle
 
     O = ra_oracle.get()
-    bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).cpu().view(torch.int16).numpy().view(np.uint16)
-    qa, ka, va = bits(q), bits(k), bits(v)
+    (qa, tag), (ka, _), (va, _) = oracle_view(q, w), oracle_view(k, w), oracle_view(v, w)
     g = np.random.default_rng(99)
     pool = np.sort(g.choice(w.rows, size=min(w.rows, 65536), replace=False))
     per_row = 4.0 * w.N * w.d
     probe = pool[:: max(1, len(pool) // 16)][:16]
     t0 = time.perf_counter()
-    O.ring(qa, ka, va, w.P, dtype="bf16", rows=probe)
+    O.ring(qa, ka, va, w.P, dtype=tag, rows=probe)
     t_probe = time.perf_counter() - t0
     n = int(min(len(pool), max(16, len(probe) * target_s / max(t_probe, 1e-6))))
     rows = pool[np.linspace(0, len(pool) - 1, n).astype(np.int64)]
     t0 = time.perf_counter()
-    want = O.ring(qa, ka, va, w.P, dtype="bf16", rows=rows)
+    want = O.ring(qa, ka, va, w.P, dtype=tag, rows=rows)
     dt = time.perf_counter() - t0
     # the same oracle on one core, on a sample sized for about 3 s
     O1 = ra_oracle.Oracle(threads=1)
     n1 = int(min(n, max(4, 3.0 * n / (max(dt, 1e-6) * O.threads))))
     rows1 = rows[np.linspace(0, len(rows) - 1, n1).astype(np.int64)]
     t0 = time.perf_counter()
-    O1.ring(qa, ka, va, w.P, dtype="bf16", rows=rows1)
+    O1.ring(qa, ka, va, w.P, dtype=tag, rows=rows1)
     dt1 = time.perf_counter() - t0
     return {"value": n * per_row / dt / 1e12, "unit": UNIT, "cores": O.threads, "kind": "oracle",
             "sample": f"{n} seeded query rows of {w.name} (ring recurrence, fp64), {dt:.1f} s; "
@@ -258,8 +269,12 @@ def sampled_parity(out, lse, rows, w_out, w_lse, w) -> dict:
     e_lse = float(np.abs(got_lse - w_lse).max())
     ref = float(np.abs(w_out).max())
     rms = float(np.sqrt(np.mean((got_out - w_out) ** 2)) / np.sqrt(np.mean(w_out ** 2)))
-    bars = {"max_abs_out": 2e-2, "max_abs_lse": 1e-3, "rel_max_out": 2.0 ** -6,
-            "rel_rms_out": 2.0 ** -7}
+    if w.dtype == torch.float32:  # the FFMA path's bars
+        bars = {"max_abs_out": 1e-5, "max_abs_lse": 1e-5, "rel_max_out": 2.0 ** -13,
+                "rel_rms_out": 2.0 ** -14}
+    else:
+        bars = {"max_abs_out": 2e-2, "max_abs_lse": 1e-3, "rel_max_out": 2.0 ** -6,
+                "rel_rms_out": 2.0 ** -7}
     got = {"max_abs_out": e_out, "max_abs_lse": e_lse, "rel_max_out": e_out / ref,
            "rel_rms_out": rms}
     return {"rows": int(len(rows)), "against": "the fp64 oracle on the rows of cpu_baseline",
@@ -299,16 +314,15 @@ def cpu_oracle_baseline_causal(w, q, k, v, layout: str, target_s: float):
     from oracle import ra_oracle
 
     O = ra_oracle.get()
-    bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).cpu().view(torch.int16).numpy().view(np.uint16)
-    qa, ka, va = bits(q), bits(k), bits(v)
+    (qa, tag), (ka, _), (va, _) = oracle_view(q, w), oracle_view(k, w), oracle_view(v, w)
     probe = synth.sample_rows(w, 16, seed=11).numpy()
     t0 = time.perf_counter()
-    O.ring(qa, ka, va, w.P, dtype="bf16", rows=probe, causal=True, layout=layout)
+    O.ring(qa, ka, va, w.P, dtype=tag, rows=probe, causal=True, layout=layout)
     t_probe = time.perf_counter() - t0
     n = int(min(4096, max(64, len(probe) * target_s / max(t_probe, 1e-6))))
     rows = synth.sample_rows(w, n, seed=11).numpy()
     t0 = time.perf_counter()
-    want = O.ring(qa, ka, va, w.P, dtype="bf16", rows=rows, causal=True, layout=layout)
+    want = O.ring(qa, ka, va, w.P, dtype=tag, rows=rows, causal=True, layout=layout)
     dt = time.perf_counter() - t0
     flops = float(np.sum(4.0 * w.d * (rows % w.N + 1)))
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": O.threads, "kind": "oracle",
@@ -330,10 +344,10 @@ def cpu_oracle_baseline_backward(w, q, k, v, out, dout, lse, causal: bool):
 
     O = ra_oracle.get()
     rows = synth.sample_rows(w, 64, seed=5).numpy()
-    bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).cpu().view(torch.int16).numpy().view(np.uint16)
-    args = (bits(q), bits(k), bits(v), bits(out), bits(dout), lse.double().cpu().numpy())
+    views = [oracle_view(t, w) for t in (q, k, v, out, dout)]
+    args = tuple(a for a, _ in views) + (lse.double().cpu().numpy(),)
     t0 = time.perf_counter()
-    want = O.backward_rows(*args, rows, rows, dtype="bf16", causal=causal)
+    want = O.backward_rows(*args, rows, rows, dtype=views[0][1], causal=causal)
     dt = time.perf_counter() - t0
     pos = (rows % w.N).astype(np.float64)
     if causal:  # a query at position n meets n + 1 keys, a key N - n queries
@@ -383,21 +397,20 @@ def run_reference(args, w) -> None:
 
     O = ra_oracle.get()
     q, k, v = synth.make_inputs(w, "cpu")
-    bits = lambda t: t.reshape(w.B * w.H, w.N, w.d).view(torch.int16).numpy().view(np.uint16)
-    qa, ka, va = bits(q), bits(k), bits(v)
+    (qa, tag), (ka, _), (va, _) = oracle_view(q, w), oracle_view(k, w), oracle_view(v, w)
     per_row = 4.0 * w.N * w.d
     g = np.random.default_rng(7)
     probe = np.sort(g.choice(w.rows, size=8, replace=False))
     t0 = time.perf_counter()
-    O.ring(qa, ka, va, w.P, dtype="bf16", rows=probe)
+    O.ring(qa, ka, va, w.P, dtype=tag, rows=probe)
     t_probe = (time.perf_counter() - t0) / len(probe)
     budget = args.ref_seconds / max(1, args.steps + args.warmup)  # whole run ~2 minutes
-    n = int(max(4, min(4096, budget / max(t_probe, 1e-6))))
+    n = int(min(w.rows, max(4, min(4096, budget / max(t_probe, 1e-6)))))
     times = []
     for s in range(args.warmup + args.steps):
         rows = np.sort(g.choice(w.rows, size=n, replace=False))
         t0 = time.perf_counter()
-        O.ring(qa, ka, va, w.P, dtype="bf16", rows=rows)
+        O.ring(qa, ka, va, w.P, dtype=tag, rows=rows)
         if s >= args.warmup:
             times.append(time.perf_counter() - t0)
     t_step = sum(times) / len(times)
@@ -602,6 +615,17 @@ def run_ours(args, w) -> None:
                            f"fold_sm103_kernel<{w.d}>"),
                 "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
                 if peaks["source"] == "measured" else "fallback 1.9 PFLOP/s bf16 burst"}
+    if w.dtype == torch.float32:
+        # the FFMA path: bound by fp32 FMA issue, not the tensor cores.  Peak =
+        # SMs x 128 FP32 lanes x 2 flops x the maximum SM clock seen.
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = clocks.get("sm_max_mhz") or 2070.0
+        alu_peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+        roofline.update({"bound": "alu", "peak": alu_peak, "frac": achieved / alu_peak,
+                         "traffic": None,
+                         "kernel": "fold_f32 (tiled, or one warp per row on small grids)",
+                         "peak_source": f"derived: {sms} SMs x 128 FP32 lanes x 2 flops x "
+                                        f"{mhz:.0f} MHz"})
 
     cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.causal \
@@ -627,7 +651,8 @@ def run_ours(args, w) -> None:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if w.dtype == torch.float32 else "bf16", "data": "synthetic",
             "config": {**w.describe(), "parallelism": "replicas",
                        **({"causal": args.causal} if args.causal else {}),
                        **({"split_segments": G} if args.split is not None else {}),
