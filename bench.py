@@ -172,7 +172,8 @@ def host_pipeline_stages(host_in, host_out, dev_in, results, w, stream) -> dict:
     import torch
 
     slices = w.B * w.H
-    chunks = min(slices, 8)  # ra_forward_host's chunk count
+    # ra_forward_host's chunk count: at most 8, at least 16 MiB of q, k, v each
+    chunks = max(1, min(slices, 8, input_bytes(w) // (16 << 20)))
     first = slices // chunks  # slices in the first chunk
     last = slices - (chunks - 1) * slices // chunks
     e0 = torch.cuda.Event(enable_timing=True)

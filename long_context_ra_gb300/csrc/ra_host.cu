@@ -23,6 +23,10 @@ using ra::kMaxDevices;
 // Up to this many chunks: enough that the first upload and the last download
 // are small next to the compute.
 constexpr int64_t kMaxChunks = 8;
+// A chunk's q, k, v upload should carry at least this many bytes: below it
+// the fixed cost of a chunk's copies, events and launch outweighs what
+// pipelining hides (a problem of a few MB runs as one chunk).
+constexpr int64_t kMinChunkBytes = 16ll << 20;
 
 struct Streams {
   cudaStream_t up = nullptr, comp = nullptr, down = nullptr;
@@ -117,8 +121,10 @@ RA_API ra_status ra_forward_host(const void* q, const void* k, const void* v, vo
 
   // chunks of whole slices
   const int64_t slices = static_cast<int64_t>(B) * H;
-  const int64_t n_chunks = slices < kMaxChunks ? slices : kMaxChunks;
   const int64_t slice_bytes = N * d * elem_bytes(dtype);
+  const int64_t by_size = 3 * slices * slice_bytes / kMinChunkBytes;
+  int64_t n_chunks = slices < kMaxChunks ? slices : kMaxChunks;
+  if (by_size < n_chunks) n_chunks = by_size < 1 ? 1 : by_size;
 
   Events evs;
   cudaEvent_t ev_start, ev_done;
