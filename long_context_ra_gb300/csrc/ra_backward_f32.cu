@@ -25,47 +25,18 @@
 #include <cmath>
 
 #include "ra_internal.h"
+#include "ra_layout.cuh"
 
 namespace ra {
 namespace {
 
 constexpr int kWarps = 4;
 
-// Position of local row r of block j under `layout` (P blocks of c rows).
-__device__ __forceinline__ int64_t bpos(int layout, int64_t j, int64_t r, int64_t P, int64_t c) {
-  if (layout == kZigzag) {
-    const int64_t h = c / 2;
-    return r < h ? j * h + r : (2 * P - 1 - j) * h + (r - h);
-  }
-  if (layout == kStriped) return j + P * r;
-  return j * c + r;
-}
-
-// Block holding position n.
-__device__ __forceinline__ int64_t bblock(int layout, int64_t n, int64_t P, int64_t c) {
-  if (layout == kZigzag) {
-    const int64_t chunk = n / (c / 2);
-    return chunk < P ? chunk : 2 * P - 1 - chunk;
-  }
-  if (layout == kStriped) return n % P;
-  return n / c;
-}
-
-// Local row of position n inside its block.
-__device__ __forceinline__ int64_t blocal(int layout, int64_t n, int64_t P, int64_t c) {
-  if (layout == kZigzag) {
-    const int64_t h = c / 2;
-    return (n / h < P ? 0 : h) + n % h;
-  }
-  if (layout == kStriped) return n / P;
-  return n % c;
-}
-
 // The per-query terms D and nl are stored block-major: (slice, block, local
 // row), so that a query tile's 128 values are contiguous under every layout.
 __device__ __forceinline__ int64_t bmajor(int layout, int64_t slice, int64_t N, int64_t n,
                                           int64_t P, int64_t c) {
-  return slice * N + bblock(layout, n, P, c) * c + blocal(layout, n, P, c);
+  return slice * N + layout_block(layout, n, P, c) * c + layout_local(layout, n, P, c);
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -160,7 +131,7 @@ __global__ void __launch_bounds__(kWarps * 32) dq_f32_kernel(const BackwardArgs 
   if (rid >= a.slices * a.N) return;
   const int64_t slice = rid / a.N, n = rid % a.N;
   const int64_t c = a.N / a.P;
-  const int i = static_cast<int>(bblock(a.layout, n, a.P, c));
+  const int i = static_cast<int>(layout_block(a.layout, n, a.P, c));
   const float* q = static_cast<const float*>(a.q);
   const float* k = static_cast<const float*>(a.k);
   const float* v = static_cast<const float*>(a.v);
@@ -180,9 +151,9 @@ __global__ void __launch_bounds__(kWarps * 32) dq_f32_kernel(const BackwardArgs 
     if (j < 0) j += a.P;
     const int64_t sb = slice * a.N;
     for (int64_t c0 = 0; c0 < c; c0 += 32) {
-      if (a.causal && bpos(a.layout, j, c0, a.P, c) > n) break;  // rest of the block masked
+      if (a.causal && layout_pos(a.layout, j, c0, a.P, c) > n) break;  // rest of the block masked
       const int64_t key = c0 + lane;
-      const int64_t kp = key < c ? bpos(a.layout, j, key, a.P, c) : 0;
+      const int64_t kp = key < c ? layout_pos(a.layout, j, key, a.P, c) : 0;
       float ds = 0.f;
       if (key < c && (!a.causal || kp <= n)) {
         float s, dp;
@@ -224,7 +195,7 @@ __global__ void __launch_bounds__(kWarps * 32) dkv_f32_kernel(const BackwardArgs
   if (rid >= a.slices * a.N) return;
   const int64_t slice = rid / a.N, n = rid % a.N;
   const int64_t c = a.N / a.P;
-  const int j = static_cast<int>(bblock(a.layout, n, a.P, c));
+  const int j = static_cast<int>(layout_block(a.layout, n, a.P, c));
   const float* q = static_cast<const float*>(a.q);
   const float* k = static_cast<const float*>(a.k);
   const float* v = static_cast<const float*>(a.v);
@@ -243,7 +214,7 @@ __global__ void __launch_bounds__(kWarps * 32) dkv_f32_kernel(const BackwardArgs
     const int64_t sb = slice * a.N;
     for (int64_t c0 = 0; c0 < c; c0 += 32) {
       const int64_t row = c0 + lane;
-      const int64_t qp = row < c ? bpos(a.layout, i, row, a.P, c) : 0;
+      const int64_t qp = row < c ? layout_pos(a.layout, i, row, a.P, c) : 0;
       float p = 0.f, ds = 0.f;
       if (row < c && (!a.causal || qp >= n)) {
         float s, dp;
@@ -395,7 +366,7 @@ __device__ __forceinline__ void load_stationary(float* dst, const float* src, in
     const int row = x / DT, e = x % DT;
     const int64_t r = r0 + row;
     float val = 0.f;
-    if (r < c && e < d) val = src[bpos(layout, b, r, P, c) * d + e];
+    if (r < c && e < d) val = src[layout_pos(layout, b, r, P, c) * d + e];
     dst[e * kSS + row] = val;
   }
 }
@@ -410,7 +381,7 @@ __device__ __forceinline__ void load_streamed(float* dT, float* dR, const float*
     const int row = x / DT, e = x % DT;
     const int64_t r = r0 + row;
     float val = 0.f;
-    if (r < c && e < d) val = src[bpos(layout, b, r, P, c) * d + e];
+    if (r < c && e < d) val = src[layout_pos(layout, b, r, P, c) * d + e];
     dT[e * kNS + row] = val;
     if (dR) dR[row * (DT + 4) + e] = val;
   }
@@ -449,7 +420,7 @@ __global__ void __launch_bounds__(kTT) dq_f32_tiled(const BackwardArgs a) {
   for (int x = 0; x < 4; ++x) {
     const int64_t r = r0 + lrow0 + x;
     rvalid[x] = r < c;
-    qpos[x] = rvalid[x] ? bpos(a.layout, i, r, a.P, c) : 0;
+    qpos[x] = rvalid[x] ? layout_pos(a.layout, i, r, a.P, c) : 0;
     lse[x] = rvalid[x] ? a.lse[sb + qpos[x]] : 0.f;
     D[x] = rvalid[x] ? a.delta[sb + static_cast<int64_t>(i) * c + r] : 0.f;
 #pragma unroll
@@ -458,13 +429,13 @@ __global__ void __launch_bounds__(kTT) dq_f32_tiled(const BackwardArgs a) {
       for (int y = 0; y < 4; ++y) acc[x][m][y] = 0.f;
   }
   const int64_t rlast = (r0 + kTM < c ? r0 + kTM : c) - 1;
-  const int64_t qlast = bpos(a.layout, i, rlast, a.P, c);
+  const int64_t qlast = layout_pos(a.layout, i, rlast, a.P, c);
 
   for (int t = 0; t < a.P; ++t) {
     int j = (i - t) % a.P;
     if (j < 0) j += a.P;
     for (int64_t c0 = 0; c0 < c; c0 += kTN) {
-      if (a.causal && bpos(a.layout, j, c0, a.P, c) > qlast) break;  // rest of block masked
+      if (a.causal && layout_pos(a.layout, j, c0, a.P, c) > qlast) break;  // rest of block masked
       __syncthreads();
       load_streamed<DT>(sm + S::kK, sm + S::kKr, k, a.layout, j, c0, a.P, c, d, tid);
       load_streamed<DT>(sm + S::kV, nullptr, v, a.layout, j, c0, a.P, c, d, tid);
@@ -477,7 +448,7 @@ __global__ void __launch_bounds__(kTT) dq_f32_tiled(const BackwardArgs a) {
       for (int y = 0; y < 4; ++y) {
         const int64_t kk = c0 + 4 * kg + y;
         const bool kvalid = kk < c;
-        const int64_t kpos = kvalid ? bpos(a.layout, j, kk, a.P, c) : 0;
+        const int64_t kpos = kvalid ? layout_pos(a.layout, j, kk, a.P, c) : 0;
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
           const bool vis = kvalid && rvalid[x] && (!a.causal || kpos <= qpos[x]);
@@ -540,13 +511,13 @@ __global__ void __launch_bounds__(kTT) dkv_f32_tiled(const BackwardArgs a) {
   for (int x = 0; x < 4; ++x) {
     const int64_t r = r0 + lrow0 + x;
     rvalid[x] = r < c;
-    kpos[x] = rvalid[x] ? bpos(a.layout, j, r, a.P, c) : 0;
+    kpos[x] = rvalid[x] ? layout_pos(a.layout, j, r, a.P, c) : 0;
 #pragma unroll
     for (int m = 0; m < DT / 32; ++m)
 #pragma unroll
       for (int y = 0; y < 4; ++y) gk[x][m][y] = gv[x][m][y] = 0.f;
   }
-  const int64_t kfirst = bpos(a.layout, j, r0, a.P, c);  // the CTA's first key position
+  const int64_t kfirst = layout_pos(a.layout, j, r0, a.P, c);  // the CTA's first key position
 
   for (int t = 0; t < a.P; ++t) {
     const int i = (j + t) % a.P;  // the query block this key block meets at step t
@@ -554,7 +525,7 @@ __global__ void __launch_bounds__(kTT) dkv_f32_tiled(const BackwardArgs a) {
       // causal: a query tile whose last query precedes every key here sees none
       if (a.causal) {
         const int64_t qe = (c0 + kTN < c ? c0 + kTN : c) - 1;
-        if (bpos(a.layout, i, qe, a.P, c) < kfirst) continue;
+        if (layout_pos(a.layout, i, qe, a.P, c) < kfirst) continue;
       }
       __syncthreads();
       load_streamed<DT>(sm + S::kQ, sm + S::kQr, q, a.layout, i, c0, a.P, c, d, tid);
@@ -568,7 +539,7 @@ __global__ void __launch_bounds__(kTT) dkv_f32_tiled(const BackwardArgs a) {
       for (int y = 0; y < 4; ++y) {
         const int64_t qq = c0 + 4 * kg + y;
         const bool qvalid = qq < c;
-        const int64_t qpos = qvalid ? bpos(a.layout, i, qq, a.P, c) : 0;
+        const int64_t qpos = qvalid ? layout_pos(a.layout, i, qq, a.P, c) : 0;
         const float lse = qvalid ? a.lse[sb + qpos] : 0.f;
         const float D = qvalid ? a.delta[sb + static_cast<int64_t>(i) * c + qq] : 0.f;
 #pragma unroll

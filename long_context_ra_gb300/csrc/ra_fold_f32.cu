@@ -28,6 +28,7 @@
 #include <cmath>
 
 #include "ra_internal.h"
+#include "ra_layout.cuh"
 
 namespace ra {
 namespace {
@@ -40,17 +41,6 @@ constexpr int kKS = kBN + 4;   // row stride of the transposed K tile (floats)
 // below this many CTAs the tiled kernel leaves most SMs idle, and the
 // row-per-warp kernel (64 x more CTAs) is faster
 constexpr int64_t kSmallGrid = 32;
-
-// Position of local row r of block j under `layout` (P blocks of c rows).
-__device__ __forceinline__ int64_t pos_of(int layout, int64_t j, int64_t r, int64_t P,
-                                          int64_t c) {
-  if (layout == kZigzag) {
-    const int64_t h = c / 2;
-    return r < h ? j * h + r : (2 * P - 1 - j) * h + (r - h);
-  }
-  if (layout == kStriped) return j + P * r;
-  return j * c + r;
-}
 
 // Shared-memory footprint (floats) for head dimensions up to DT.
 template <int DT>
@@ -78,7 +68,7 @@ struct TileCursor {
   // from (t, c0) forward to the first visible tile, or past the last step
   __device__ void settle() {
     while (t < t1) {
-      if (c0 < ck && !(causal && pos_of(layout, j, c0, P, ck) > qlast)) return;
+      if (c0 < ck && !(causal && layout_pos(layout, j, c0, P, ck) > qlast)) return;
       ++t;
       c0 = 0;
       if (t < t1) set_block();
@@ -139,7 +129,7 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
     const int row = x / DT, e = x % DT;
     const int64_t r = r0 + row;
     float val = 0.f;
-    if (r < cq && e < d) val = q[pos_of(a.layout, i, r, a.P, cq) * d + e];
+    if (r < cq && e < d) val = q[layout_pos(a.layout, i, r, a.P, cq) * d + e];
     qT[e * kQS + row] = val;
   }
 
@@ -153,7 +143,7 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
   for (int x = 0; x < 4; ++x) {
     const int64_t r = r0 + lrow0 + x;
     rvalid[x] = r < cq;
-    qpos[x] = rvalid[x] ? pos_of(a.layout, i, r, a.P, cq) : 0;
+    qpos[x] = rvalid[x] ? layout_pos(a.layout, i, r, a.P, cq) : 0;
     m[x] = -INFINITY;
     l[x] = 0.f;
 #pragma unroll
@@ -179,7 +169,7 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
   }
   // the CTA's last query position (positions grow along a block's rows)
   const int64_t rlast = (r0 + kBM < cq ? r0 + kBM : cq) - 1;
-  const int64_t qlast = pos_of(a.layout, i, rlast, a.P, cq);
+  const int64_t qlast = layout_pos(a.layout, i, rlast, a.P, cq);
 
   // K^T and V tiles; keys past the block and columns past d are zero.  In
   // the 128-wide class the next tile's values are fetched into registers
@@ -200,7 +190,7 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
       const int64_t kk = tc.c0 + key;
       kr[it] = vr[it] = 0.f;
       if (kk < ck && e < d) {
-        const int64_t row = pos_of(a.layout, tc.j, kk, a.P, ck);
+        const int64_t row = layout_pos(a.layout, tc.j, kk, a.P, ck);
         kr[it] = kb[row * d + e];
         vr[it] = vb[row * d + e];
       }
@@ -225,7 +215,7 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
         const int64_t kk = c0 + key;
         float kv = 0.f, vv = 0.f;
         if (kk < ck && e < d) {
-          const int64_t row = pos_of(a.layout, j, kk, a.P, ck);
+          const int64_t row = layout_pos(a.layout, j, kk, a.P, ck);
           kv = kb[row * d + e];
           vv = vb[row * d + e];
         }
@@ -262,7 +252,7 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
       for (int y = 0; y < 4; ++y) {
         const int64_t kk = c0 + 4 * kg + y;
         kvalid[y] = kk < ck;
-        kpos[y] = kvalid[y] ? pos_of(a.layout, j, kk, a.P, ck) : 0;
+        kpos[y] = kvalid[y] ? layout_pos(a.layout, j, kk, a.P, ck) : 0;
       }
       float p[4][4];
 #pragma unroll
@@ -376,16 +366,6 @@ cudaError_t launch_dt(const FoldArgs& a, cudaStream_t s) {
 
 constexpr int kWarps = 4;
 
-// Block holding position n.
-__device__ __forceinline__ int64_t block_of(int layout, int64_t n, int64_t P, int64_t c) {
-  if (layout == kZigzag) {
-    const int64_t chunk = n / (c / 2);
-    return chunk < P ? chunk : 2 * P - 1 - chunk;
-  }
-  if (layout == kStriped) return n % P;
-  return n / c;
-}
-
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
@@ -436,7 +416,7 @@ __global__ void __launch_bounds__(kWarps * 32) fold_f32_rows_kernel(const FoldAr
   const int64_t n = rid % a.nq;
   const int64_t cq = a.nq / a.P;
   const int64_t ck = a.nk / a.P;
-  const int i = static_cast<int>(block_of(a.layout, n, a.P, cq));
+  const int i = static_cast<int>(layout_block(a.layout, n, a.P, cq));
   const int t0 = static_cast<int>(static_cast<int64_t>(g) * a.P / a.G);
   const int t1 = static_cast<int>(static_cast<int64_t>(g + 1) * a.P / a.G);
 
@@ -467,9 +447,9 @@ __global__ void __launch_bounds__(kWarps * 32) fold_f32_rows_kernel(const FoldAr
     const float* kbase = static_cast<const float*>(a.k) + slice * a.nk * d;
     const float* vbase = static_cast<const float*>(a.v) + slice * a.nk * d;
     for (int64_t c0 = 0; c0 < ck; c0 += 32) {
-      if (a.causal && pos_of(a.layout, j, c0, a.P, ck) > n) break;  // rest of block masked
+      if (a.causal && layout_pos(a.layout, j, c0, a.P, ck) > n) break;  // rest of block masked
       const int64_t key = c0 + lane;
-      const int64_t kpos = key < ck ? pos_of(a.layout, j, key, a.P, ck) : 0;
+      const int64_t kpos = key < ck ? layout_pos(a.layout, j, key, a.P, ck) : 0;
       const bool valid = key < ck && (!a.causal || kpos <= n);
       float s = -INFINITY;
       if (valid) s = dot_row(qs[warp], kbase + kpos * d, d, vec) * a.tau;
