@@ -249,7 +249,9 @@ RA_API ra_status ra_forward_split_noalloc(const void* q, const void* k, const vo
  * ra_forward_host -- ra_forward (causal = 0) or ra_forward_causal
  * (causal = 1, with `layout`) for inputs and results in HOST memory.  The
  * pages have no counterpart: it is the same computation with the transfers
- * folded in.  The B*H independent (batch, head) slices are cut into chunks.
+ * folded in.  The B*H independent (batch, head) slices are cut into up to 8
+ * chunks of whole slices, each carrying at least 16 MiB of q, k, v (a
+ * smaller problem is one chunk).
  * Chunk c's q, k, v are copied to the device while earlier chunks compute,
  * and its out, lse are copied back while later chunks compute, so only the
  * first chunk's upload and the last chunk's download are not hidden.
