@@ -697,6 +697,6 @@ RA_API const char* ra_status_string(ra_status s) {
   return "unknown ra_status";
 }
 
-RA_API int32_t ra_version(void) { return 100; }
+RA_API int32_t ra_version(void) { return 200; }  // 0.2.0
 
 }  // extern "C"
