@@ -689,6 +689,9 @@ def main() -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=4, help="workload key (default 4)")
     ap.add_argument("--heads", type=int, default=None, help="override the head count")
+    ap.add_argument("--tokens", type=int, default=None, help="override N")
+    ap.add_argument("--head-dim", type=int, default=None, help="override d")
+    ap.add_argument("--blocks", type=int, default=None, help="override P")
     ap.add_argument("--causal", choices=["contiguous", "zigzag", "striped"], default=None,
                     help="time ra_forward_causal with this layout instead of ra_forward")
     ap.add_argument("--split", type=int, default=None,
@@ -709,6 +712,14 @@ def main() -> None:
     if args.heads is not None and args.heads != w.H:
         # a smaller case of the same workload (for profiler captures)
         w = dataclasses.replace(w, H=args.heads, name=f"{w.name.replace(f'_H{w.H}_', f'_H{args.heads}_')}")
+    # other shapes with the same recipe and dtype (profiler captures, sweeps):
+    # the name states every size
+    shape = {"N": args.tokens, "d": args.head_dim, "P": args.blocks}
+    if any(x is not None for x in shape.values()):
+        kw = {k: x for k, x in shape.items() if x is not None}
+        w = dataclasses.replace(w, **kw)
+        w = dataclasses.replace(w, name=f"{str(w.dtype).replace('torch.', '').replace('bfloat16', 'bf16').replace('float32', 'fp32')}"
+                                        f"_B{w.B}_H{w.H}_N{w.N}_d{w.d}_P{w.P}_{w.recipe}")
     if args.impl == "reference":
         run_reference(args, w)
     else:
