@@ -358,13 +358,18 @@ cudaError_t launch_dt(const FoldArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// ---- small problems: one warp per query row ----
+// ---- small problems: a few warps per query row ----
 // When the tiled kernel would launch only a few CTAs (a few hundred query
-// rows), one warp per row spreads the rows over more SMs.  Each warp walks
-// the blocks in ring order 32 keys at a time, one key per lane, and the lanes
-// split o (lane e holds o[e], o[e + 32], ...).
+// rows), warps take rows instead, and each row's chunks of 32 keys (ring
+// order: block j = (i - t) mod P, local order within it) are dealt round
+// robin to S warps, so that the serial chain of a row is S times shorter.
+// Each warp folds its chunks one key per lane (the lanes split o: lane e
+// holds o[e], o[e + 32], ...) into its own (m, l, o); the S states of a row
+// are then combined by the identity that merges partial states
+//   m* = max m_s,  w_s = exp(m_s - m*),  l* = sum w_s l_s,  o* = sum w_s o_s
+// (the same identity that lets the fold visit the keys in any order).
 
-constexpr int kWarps = 4;
+constexpr int kRowWarps = 8;  // warps per CTA
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -403,79 +408,120 @@ __device__ __forceinline__ float dot_row(const float* __restrict__ qrow,
   return (a0 + a1) + (a2 + a3);
 }
 
-template <int DV>  // o values per lane: d <= 32 * DV
-__global__ void __launch_bounds__(kWarps * 32) fold_f32_rows_kernel(const FoldArgs a) {
-  __shared__ __align__(16) float qs[kWarps][32 * DV];
+// DV: o values per lane (d <= 32 DV); S: warps per row (1, 2, 4 or 8).
+template <int DV, int S>
+__global__ void __launch_bounds__(kRowWarps * 32, 2) fold_f32_rows_kernel(const FoldArgs a) {
+  constexpr int kRows = kRowWarps / S;  // query rows per CTA
+  __shared__ __align__(16) float qs[kRowWarps][32 * DV];
+  __shared__ float part_o[kRowWarps][32 * DV];
+  __shared__ float part_ml[kRowWarps][2];
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  const int sp = warp % S;  // this warp's share of the row's chunks
   const int d = a.d;
-  const int64_t rid = static_cast<int64_t>(blockIdx.x) * kWarps + warp;  // query row
-  const int g = blockIdx.y;                                              // segment
-  if (rid >= a.slices * a.nq) return;  // whole warp leaves together
-  const int64_t slice = rid / a.nq;
-  const int64_t n = rid % a.nq;
+  const int64_t rid = static_cast<int64_t>(blockIdx.x) * kRows + warp / S;  // query row
+  const int g = blockIdx.y;                                                 // segment
+  // a CTA's rows past the end do nothing, but still meet the merge's barrier
+  const bool live = rid < a.slices * a.nq;
+  const int64_t slice = live ? rid / a.nq : 0;
+  const int64_t n = live ? rid % a.nq : 0;
   const int64_t cq = a.nq / a.P;
   const int64_t ck = a.nk / a.P;
   const int i = static_cast<int>(layout_block(a.layout, n, a.P, cq));
   const int t0 = static_cast<int>(static_cast<int64_t>(g) * a.P / a.G);
   const int t1 = static_cast<int>(static_cast<int64_t>(g + 1) * a.P / a.G);
+  const int64_t nch = (ck + 31) / 32;  // chunks per block
 
   // rows of k start on 16-byte boundaries when d is a multiple of 4 and k
   // itself is 16-byte aligned
   const bool vec = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(a.k) % 16 == 0);
-  const float* q = static_cast<const float*>(a.q) + rid * d;
-  for (int e = lane; e < d; e += 32) qs[warp][e] = q[e];
-  __syncwarp();
-
   float m = -INFINITY, l = 0.f;
   float o[DV];
 #pragma unroll
   for (int v = 0; v < DV; ++v) o[v] = 0.f;
-  if (a.mode == kFold) {
-    m = a.st_m[rid];
-    l = a.st_l[rid];
+
+  if (live) {
+    const float* q = static_cast<const float*>(a.q) + rid * d;
+    for (int e = lane; e < d; e += 32) qs[warp][e] = q[e];
+    __syncwarp();
+    if (a.mode == kFold && sp == 0) {  // the incoming state joins as one more part
+      m = a.st_m[rid];
+      l = a.st_l[rid];
 #pragma unroll
-    for (int v = 0; v < DV; ++v) {
-      const int e = lane + 32 * v;
-      if (e < d) o[v] = a.st_o[rid * d + e];
+      for (int v = 0; v < DV; ++v) {
+        const int e = lane + 32 * v;
+        if (e < d) o[v] = a.st_o[rid * d + e];
+      }
+    }
+    const float* kbase = static_cast<const float*>(a.k) + slice * a.nk * d;
+    const float* vbase = static_cast<const float*>(a.v) + slice * a.nk * d;
+    for (int t = t0; t < t1; ++t) {
+      int j = (i - t) % a.P;
+      if (j < 0) j += a.P;
+      // chunk ci of this block is the row's chunk (t - t0) nch + ci
+      int64_t ci = (sp - (static_cast<int64_t>(t - t0) * nch) % S + S) % S;
+      for (; ci < nch; ci += S) {
+        const int64_t c0 = ci * 32;
+        if (a.causal && layout_pos(a.layout, j, c0, a.P, ck) > n) break;  // rest of block masked
+        const int64_t key = c0 + lane;
+        const int64_t kpos = key < ck ? layout_pos(a.layout, j, key, a.P, ck) : 0;
+        const bool valid = key < ck && (!a.causal || kpos <= n);
+        float s = -INFINITY;
+        if (valid) s = dot_row(qs[warp], kbase + kpos * d, d, vec) * a.tau;
+        const float m_new = fmaxf(m, warp_max(s));
+        const float alpha = m_new == -INFINITY ? 1.f : expf(m - m_new);
+        const float p = valid ? expf(s - m_new) : 0.f;
+        l = alpha * l + warp_sum(p);
+#pragma unroll
+        for (int v = 0; v < DV; ++v) o[v] *= alpha;
+        // o += p V over the chunk's keys.  The loop has a fixed trip count
+        // (masked keys and keys past the block's end have p = 0; the latter
+        // read the slice's first row), so the V loads of several keys are
+        // in flight at once.  As on the tensor-core path, a masked key's v
+        // is multiplied by 0 rather than skipped.
+#pragma unroll 8
+        for (int jj = 0; jj < 32; ++jj) {
+          const float pj = __shfl_sync(0xffffffffu, p, jj);
+          const float* vr = vbase + __shfl_sync(0xffffffffu, kpos, jj) * d;
+#pragma unroll
+          for (int v = 0; v < DV; ++v) {
+            const int e = lane + 32 * v;
+            if (e < d) o[v] = fmaf(pj, vr[e], o[v]);
+          }
+        }
+        m = m_new;
+      }
     }
   }
 
-  for (int t = t0; t < t1; ++t) {
-    int j = (i - t) % a.P;
-    if (j < 0) j += a.P;
-    const float* kbase = static_cast<const float*>(a.k) + slice * a.nk * d;
-    const float* vbase = static_cast<const float*>(a.v) + slice * a.nk * d;
-    for (int64_t c0 = 0; c0 < ck; c0 += 32) {
-      if (a.causal && layout_pos(a.layout, j, c0, a.P, ck) > n) break;  // rest of block masked
-      const int64_t key = c0 + lane;
-      const int64_t kpos = key < ck ? layout_pos(a.layout, j, key, a.P, ck) : 0;
-      const bool valid = key < ck && (!a.causal || kpos <= n);
-      float s = -INFINITY;
-      if (valid) s = dot_row(qs[warp], kbase + kpos * d, d, vec) * a.tau;
-      const float m_new = fmaxf(m, warp_max(s));
-      const float alpha = m_new == -INFINITY ? 1.f : expf(m - m_new);
-      const float p = valid ? expf(s - m_new) : 0.f;
-      l = alpha * l + warp_sum(p);
+  if (S > 1) {
+    // every part of the row into shared memory; the row's first warp merges
 #pragma unroll
-      for (int v = 0; v < DV; ++v) o[v] *= alpha;
-      // o += p V over the chunk's keys.  The loop has a fixed trip count
-      // (masked keys and keys past the block's end have p = 0; the latter
-      // read the slice's first row), so the V loads of several keys are in
-      // flight at once.  As on the tensor-core path, a masked key's v is
-      // multiplied by 0 rather than skipped.
-#pragma unroll 8
-      for (int jj = 0; jj < 32; ++jj) {
-        const float pj = __shfl_sync(0xffffffffu, p, jj);
-        const float* vr = vbase + __shfl_sync(0xffffffffu, kpos, jj) * d;
-#pragma unroll
-        for (int v = 0; v < DV; ++v) {
-          const int e = lane + 32 * v;
-          if (e < d) o[v] = fmaf(pj, vr[e], o[v]);
-        }
-      }
-      m = m_new;
+    for (int v = 0; v < DV; ++v) part_o[warp][lane + 32 * v] = o[v];
+    if (lane == 0) {
+      part_ml[warp][0] = m;
+      part_ml[warp][1] = l;
     }
+    __syncthreads();
+    if (sp != 0 || !live) return;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int x = 0; x < S; ++x) mx = fmaxf(mx, part_ml[warp + x][0]);
+    l = 0.f;
+#pragma unroll
+    for (int v = 0; v < DV; ++v) o[v] = 0.f;
+#pragma unroll
+    for (int x = 0; x < S; ++x) {
+      const float mp = part_ml[warp + x][0];
+      // an empty part (m = -inf) adds nothing, also when every part is empty
+      const float w = mp == -INFINITY ? 0.f : expf(mp - mx);
+      l = fmaf(w, part_ml[warp + x][1], l);
+#pragma unroll
+      for (int v = 0; v < DV; ++v) o[v] = fmaf(w, part_o[warp + x][lane + 32 * v], o[v]);
+    }
+    m = mx;
+  } else if (!live) {
+    return;
   }
 
   if (a.mode == kForward) {
@@ -503,12 +549,38 @@ __global__ void __launch_bounds__(kWarps * 32) fold_f32_rows_kernel(const FoldAr
   }
 }
 
+// Warps per row: at most 8, at most one per chunk of the row's segment, and
+// only as many as stay resident at once (two CTAs of 8 warps on every SM).
+int row_split(const FoldArgs& a) {
+  const int64_t rows = a.slices * a.nq * a.G;
+  const int64_t chunks = (a.P / a.G) * ((a.nk / a.P + 31) / 32);  // per row and segment, at least
+  const int64_t want = static_cast<int64_t>(device_sm_count()) * 2 * kRowWarps;
+  int S = 1;
+  while (S < 8 && rows * S * 2 <= want && chunks >= S * 2) S *= 2;
+  return S;
+}
+
+template <int DV, int S>
+cudaError_t launch_rows(const FoldArgs& a, cudaStream_t s) {
+  const int64_t rows = a.slices * a.nq;
+  constexpr int kRows = kRowWarps / S;
+  const dim3 grid(static_cast<unsigned>((rows + kRows - 1) / kRows), static_cast<unsigned>(a.G));
+  fold_f32_rows_kernel<DV, S><<<grid, kRowWarps * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int DV>
 cudaError_t launch_dv(const FoldArgs& a, cudaStream_t s) {
-  const int64_t rows = a.slices * a.nq;
-  const dim3 grid(static_cast<unsigned>((rows + kWarps - 1) / kWarps), static_cast<unsigned>(a.G));
-  fold_f32_rows_kernel<DV><<<grid, kWarps * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  switch (row_split(a)) {
+    case 8:
+      return launch_rows<DV, 8>(a, s);
+    case 4:
+      return launch_rows<DV, 4>(a, s);
+    case 2:
+      return launch_rows<DV, 2>(a, s);
+    default:
+      return launch_rows<DV, 1>(a, s);
+  }
 }
 
 }  // namespace

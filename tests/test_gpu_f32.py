@@ -106,6 +106,44 @@ def test_tiled_causal(O, layout):
     check_forward(O, q, k, v, P, out, lse, causal=True, layout=layout)
 
 
+# Small grids run on the row kernel, whose rows are each split over up to 8
+# warps (the row's chunks of 32 keys dealt round robin, the warps' states
+# merged at the end).  These cases split 4 ways: the mask's early stop and
+# the fold mode's incoming state under the split.
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
+def test_small_grid_causal(O, layout):
+    B, H, N, d, P = 1, 2, 256, 40, 4
+    g = torch.Generator(device=DEV).manual_seed(73)
+    q, k, v = (torch.randn(B, H, N, d, device=DEV, generator=g) * 1.5 for _ in range(3))
+    out, lse = ra.ra_forward_causal(q, k, v, P, layout=layout)
+    check_forward(O, q, k, v, P, out, lse, causal=True, layout=layout)
+
+
+def test_small_grid_fold_chain(O):
+    """ra_fold of 2 x 200 rows against 200-key blocks (seven chunks a row)
+    in ring order, against the forward of the same tensors (the tiled
+    kernel) and the oracle."""
+    B, H, N, d, P = 1, 2, 800, 24, 4
+    c = N // P
+    g = torch.Generator(device=DEV).manual_seed(74)
+    q, k, v = (torch.randn(B, H, N, d, device=DEV, generator=g) * 2 for _ in range(3))
+    out_f, lse_f = ra.ra_forward(q, k, v, P=P)
+    check_forward(O, q, k, v, P, out_f, lse_f)
+    order = O.ring_order(P)
+    for i in (0, 3):
+        st = ra.ra_state_init(ra.new_state(B * H * c, d))
+        qi = q[:, :, i * c:(i + 1) * c].reshape(B * H, c, d).contiguous()
+        for t in range(P):
+            j = int(order[i, t])
+            ra.ra_fold(st, qi, k[:, :, j * c:(j + 1) * c].reshape(B * H, c, d).contiguous(),
+                       v[:, :, j * c:(j + 1) * c].reshape(B * H, c, d).contiguous(), batch=B * H)
+        out, lse = ra.ra_merge([st], out_dtype=torch.float32)
+        check_same(out, out_f[:, :, i * c:(i + 1) * c].reshape(-1, d), torch.float32,
+                   "split-row fold chain vs forward", 1e-5)
+        check_same(lse, lse_f[:, :, i * c:(i + 1) * c].reshape(-1), torch.float32,
+                   "split-row fold chain lse vs forward", 1e-5, relative=False)
+
+
 def test_tiled_partials_and_fold_chain(O):
     """Partial states (G = 3) and a chain of ra_fold calls through the tiled
     kernel (ra_fold of 8 x 256 rows: 32 CTAs), against the oracle's segment
