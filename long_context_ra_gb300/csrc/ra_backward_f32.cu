@@ -14,8 +14,9 @@
 //       (j + t) mod P, and accumulate dK and dV.
 // For d <= 128 and grids of 128 CTAs or more both are tiled (64 stationary
 // rows per CTA, 32-row tiles of the other side staged in shared memory);
-// otherwise one warp owns one row and the lanes split the head dimension
-// (lane e holds elements e, e + 32, ...).
+// otherwise up to 8 warps share one row (each folds every S-th chunk of 32
+// rows of the other side) and the lanes split the head dimension (lane e
+// holds elements e, e + 32, ...).
 // Causal ("Ring attention, explained", "The causal-mask catch"): a query at
 // position n sees keys at positions <= n; `layout` says which positions form
 // each block (contiguous, zigzag or striped), as in the forward.
@@ -29,8 +30,6 @@
 
 namespace ra {
 namespace {
-
-constexpr int kWarps = 4;
 
 // The per-query terms D and nl are stored block-major: (slice, block, local
 // row), so that a query tile's 128 values are contiguous under every layout.
@@ -120,61 +119,101 @@ __device__ __forceinline__ bool rows_vec(const BackwardArgs& a) {
   return a.d % 4 == 0 && m % 16 == 0;
 }
 
-// Gradient of one query row (warp) over all key blocks in ring order.
-template <int DV>
-__global__ void __launch_bounds__(kWarps * 32) dq_f32_kernel(const BackwardArgs a) {
+// Row kernels: one query row (dq) or key row (dkv) per S warps (1, 2, 4 or
+// 8), the row's chunks of 32 rows of the other side dealt round robin to
+// its warps; each warp accumulates its chunks, and the row's first warp
+// adds the S partial sums in shared memory.  A CTA holds the S warps of
+// each of its rows: max(4, S) warps, so that small grids still come in fine
+// pieces.  The split kernels get 128 registers a thread (16 warps an SM),
+// the unsplit ones 64.
+template <int S>
+struct RowCta {
+  static constexpr int kWarps = S < 4 ? 4 : S;
+  static constexpr int kRows = kWarps / S;
+  static constexpr int kMinBlocks = S == 1 ? 8 : 16 / kWarps;
+};
+constexpr int kResidentWarps = 16;  // per SM, at 128 registers a thread
+
+// Gradient of one query row over all key blocks in ring order.
+template <int DV, int S>
+__global__ void __launch_bounds__(RowCta<S>::kWarps * 32, RowCta<S>::kMinBlocks)
+    dq_f32_kernel(const BackwardArgs a) {
+  constexpr int kWarps = RowCta<S>::kWarps;
+  constexpr int kRows = RowCta<S>::kRows;
   __shared__ __align__(16) float qs[kWarps][32 * DV];
   __shared__ __align__(16) float gs[kWarps][32 * DV];
+  __shared__ float part[S > 1 ? kWarps : 1][32 * DV];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int sp = warp % S;
   const int d = a.d;
-  const int64_t rid = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  if (rid >= a.slices * a.N) return;
-  const int64_t slice = rid / a.N, n = rid % a.N;
+  const int64_t rid = static_cast<int64_t>(blockIdx.x) * kRows + warp / S;
+  const bool live = rid < a.slices * a.N;
+  const int64_t slice = live ? rid / a.N : 0, n = live ? rid % a.N : 0;
   const int64_t c = a.N / a.P;
+  const int64_t nch = (c + 31) / 32;
   const int i = static_cast<int>(layout_block(a.layout, n, a.P, c));
   const float* q = static_cast<const float*>(a.q);
   const float* k = static_cast<const float*>(a.k);
   const float* v = static_cast<const float*>(a.v);
   const float* g = static_cast<const float*>(a.dout);
-  for (int e = lane; e < d; e += 32) {
-    qs[warp][e] = q[rid * d + e];
-    gs[warp][e] = g[rid * d + e];
-  }
-  __syncwarp();
-  const float lse = a.lse[rid], D = a.delta[bmajor(a.layout, slice, a.N, n, a.P, c)];
-  const bool vec = rows_vec(a);
   float acc[DV];
 #pragma unroll
   for (int x = 0; x < DV; ++x) acc[x] = 0.f;
-  for (int t = 0; t < a.P; ++t) {
-    int j = (i - t) % a.P;
-    if (j < 0) j += a.P;
+  if (live) {
+    for (int e = lane; e < d; e += 32) {
+      qs[warp][e] = q[rid * d + e];
+      gs[warp][e] = g[rid * d + e];
+    }
+    __syncwarp();
+    const float lse = a.lse[rid], D = a.delta[bmajor(a.layout, slice, a.N, n, a.P, c)];
+    const bool vec = rows_vec(a);
     const int64_t sb = slice * a.N;
-    for (int64_t c0 = 0; c0 < c; c0 += 32) {
-      if (a.causal && layout_pos(a.layout, j, c0, a.P, c) > n) break;  // rest of the block masked
-      const int64_t key = c0 + lane;
-      const int64_t kp = key < c ? layout_pos(a.layout, j, key, a.P, c) : 0;
-      float ds = 0.f;
-      if (key < c && (!a.causal || kp <= n)) {
-        float s, dp;
-        dot2(qs[warp], k + (sb + kp) * d, gs[warp], v + (sb + kp) * d, d, vec, s, dp);
-        const float p = expf(s * a.tau - lse);
-        ds = p * (dp - D);
-      }
-      // fixed trip count (ds = 0 for masked keys and keys past the block's
-      // end, which read the slice's first row): several loads in flight
+    for (int t = 0; t < a.P; ++t) {
+      int j = (i - t) % a.P;
+      if (j < 0) j += a.P;
+      // chunk ci of this block is the row's chunk t nch + ci
+      for (int64_t ci = (sp - (static_cast<int64_t>(t) * nch) % S + S) % S; ci < nch; ci += S) {
+        const int64_t c0 = ci * 32;
+        if (a.causal && layout_pos(a.layout, j, c0, a.P, c) > n) break;  // rest of the block masked
+        const int64_t key = c0 + lane;
+        const int64_t kp = key < c ? layout_pos(a.layout, j, key, a.P, c) : 0;
+        float ds = 0.f;
+        if (key < c && (!a.causal || kp <= n)) {
+          float s, dp;
+          dot2(qs[warp], k + (sb + kp) * d, gs[warp], v + (sb + kp) * d, d, vec, s, dp);
+          const float p = expf(s * a.tau - lse);
+          ds = p * (dp - D);
+        }
+        // fixed trip count (ds = 0 for masked keys and keys past the block's
+        // end, which read the slice's first row): several loads in flight
 #pragma unroll 8
-      for (int jj = 0; jj < 32; ++jj) {
-        const float dsj = __shfl_sync(0xffffffffu, ds, jj);
-        const int64_t kpj = __shfl_sync(0xffffffffu, kp, jj);
-        const float* kr = k + (sb + kpj) * d;
+        for (int jj = 0; jj < 32; ++jj) {
+          const float dsj = __shfl_sync(0xffffffffu, ds, jj);
+          const int64_t kpj = __shfl_sync(0xffffffffu, kp, jj);
+          const float* kr = k + (sb + kpj) * d;
 #pragma unroll
-        for (int x = 0; x < DV; ++x) {
-          const int e = lane + 32 * x;
-          if (e < d) acc[x] = fmaf(dsj, kr[e], acc[x]);
+          for (int x = 0; x < DV; ++x) {
+            const int e = lane + 32 * x;
+            if (e < d) acc[x] = fmaf(dsj, kr[e], acc[x]);
+          }
         }
       }
     }
+  }
+  if (S > 1) {
+#pragma unroll
+    for (int x = 0; x < DV; ++x) part[warp][lane + 32 * x] = acc[x];
+    __syncthreads();
+    if (sp != 0 || !live) return;
+#pragma unroll
+    for (int x = 0; x < DV; ++x) {
+      float sum = part[warp][lane + 32 * x];
+#pragma unroll
+      for (int y = 1; y < S; ++y) sum += part[warp + y][lane + 32 * x];
+      acc[x] = sum;
+    }
+  } else if (!live) {
+    return;
   }
   float* dq = static_cast<float*>(a.dq);
 #pragma unroll
@@ -184,63 +223,94 @@ __global__ void __launch_bounds__(kWarps * 32) dq_f32_kernel(const BackwardArgs 
   }
 }
 
-// Gradients of one key row (warp) over the query blocks its block visits.
-template <int DV>
-__global__ void __launch_bounds__(kWarps * 32) dkv_f32_kernel(const BackwardArgs a) {
+// Gradients of one key row over the query blocks its block visits.
+template <int DV, int S>
+__global__ void __launch_bounds__(RowCta<S>::kWarps * 32, RowCta<S>::kMinBlocks)
+    dkv_f32_kernel(const BackwardArgs a) {
+  constexpr int kWarps = RowCta<S>::kWarps;
+  constexpr int kRows = RowCta<S>::kRows;
   __shared__ __align__(16) float ks[kWarps][32 * DV];
   __shared__ __align__(16) float vs[kWarps][32 * DV];
+  __shared__ float part_k[S > 1 ? kWarps : 1][32 * DV];
+  __shared__ float part_v[S > 1 ? kWarps : 1][32 * DV];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int sp = warp % S;
   const int d = a.d;
-  const int64_t rid = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  if (rid >= a.slices * a.N) return;
-  const int64_t slice = rid / a.N, n = rid % a.N;
+  const int64_t rid = static_cast<int64_t>(blockIdx.x) * kRows + warp / S;
+  const bool live = rid < a.slices * a.N;
+  const int64_t slice = live ? rid / a.N : 0, n = live ? rid % a.N : 0;
   const int64_t c = a.N / a.P;
+  const int64_t nch = (c + 31) / 32;
   const int j = static_cast<int>(layout_block(a.layout, n, a.P, c));
   const float* q = static_cast<const float*>(a.q);
   const float* k = static_cast<const float*>(a.k);
   const float* v = static_cast<const float*>(a.v);
   const float* g = static_cast<const float*>(a.dout);
-  for (int e = lane; e < d; e += 32) {
-    ks[warp][e] = k[rid * d + e];
-    vs[warp][e] = v[rid * d + e];
-  }
-  __syncwarp();
-  const bool vec = rows_vec(a);
   float gk[DV], gv[DV];
 #pragma unroll
   for (int x = 0; x < DV; ++x) gk[x] = gv[x] = 0.f;
-  for (int t = 0; t < a.P; ++t) {
-    const int i = (j + t) % a.P;  // the device holding this block at step t
+  if (live) {
+    for (int e = lane; e < d; e += 32) {
+      ks[warp][e] = k[rid * d + e];
+      vs[warp][e] = v[rid * d + e];
+    }
+    __syncwarp();
+    const bool vec = rows_vec(a);
     const int64_t sb = slice * a.N;
-    for (int64_t c0 = 0; c0 < c; c0 += 32) {
-      const int64_t row = c0 + lane;
-      const int64_t qp = row < c ? layout_pos(a.layout, i, row, a.P, c) : 0;
-      float p = 0.f, ds = 0.f;
-      if (row < c && (!a.causal || qp >= n)) {
-        float s, dp;
-        dot2(q + (sb + qp) * d, ks[warp], g + (sb + qp) * d, vs[warp], d, vec, s, dp);
-        p = expf(s * a.tau - a.lse[sb + qp]);
-        ds = p * (dp - a.delta[sb + static_cast<int64_t>(i) * c + row]);
-      }
-      // fixed trip count (p = ds = 0 for masked rows and rows past the
-      // block's end, which read the slice's first row): loads in flight
+    for (int t = 0; t < a.P; ++t) {
+      const int i = (j + t) % a.P;  // the device holding this block at step t
+      for (int64_t ci = (sp - (static_cast<int64_t>(t) * nch) % S + S) % S; ci < nch; ci += S) {
+        const int64_t row = ci * 32 + lane;
+        const int64_t qp = row < c ? layout_pos(a.layout, i, row, a.P, c) : 0;
+        float p = 0.f, ds = 0.f;
+        if (row < c && (!a.causal || qp >= n)) {
+          float s, dp;
+          dot2(q + (sb + qp) * d, ks[warp], g + (sb + qp) * d, vs[warp], d, vec, s, dp);
+          p = expf(s * a.tau - a.lse[sb + qp]);
+          ds = p * (dp - a.delta[sb + static_cast<int64_t>(i) * c + row]);
+        }
+        // fixed trip count (p = ds = 0 for masked rows and rows past the
+        // block's end, which read the slice's first row): loads in flight
 #pragma unroll 8
-      for (int jj = 0; jj < 32; ++jj) {
-        const float pj = __shfl_sync(0xffffffffu, p, jj);
-        const float dsj = __shfl_sync(0xffffffffu, ds, jj);
-        const int64_t qpj = __shfl_sync(0xffffffffu, qp, jj);
-        const float* qr = q + (sb + qpj) * d;
-        const float* gr = g + (sb + qpj) * d;
+        for (int jj = 0; jj < 32; ++jj) {
+          const float pj = __shfl_sync(0xffffffffu, p, jj);
+          const float dsj = __shfl_sync(0xffffffffu, ds, jj);
+          const int64_t qpj = __shfl_sync(0xffffffffu, qp, jj);
+          const float* qr = q + (sb + qpj) * d;
+          const float* gr = g + (sb + qpj) * d;
 #pragma unroll
-        for (int x = 0; x < DV; ++x) {
-          const int e = lane + 32 * x;
-          if (e < d) {
-            gv[x] = fmaf(pj, gr[e], gv[x]);
-            gk[x] = fmaf(dsj, qr[e], gk[x]);
+          for (int x = 0; x < DV; ++x) {
+            const int e = lane + 32 * x;
+            if (e < d) {
+              gv[x] = fmaf(pj, gr[e], gv[x]);
+              gk[x] = fmaf(dsj, qr[e], gk[x]);
+            }
           }
         }
       }
     }
+  }
+  if (S > 1) {
+#pragma unroll
+    for (int x = 0; x < DV; ++x) {
+      part_k[warp][lane + 32 * x] = gk[x];
+      part_v[warp][lane + 32 * x] = gv[x];
+    }
+    __syncthreads();
+    if (sp != 0 || !live) return;
+#pragma unroll
+    for (int x = 0; x < DV; ++x) {
+      float sk = part_k[warp][lane + 32 * x], sv = part_v[warp][lane + 32 * x];
+#pragma unroll
+      for (int y = 1; y < S; ++y) {
+        sk += part_k[warp + y][lane + 32 * x];
+        sv += part_v[warp + y][lane + 32 * x];
+      }
+      gk[x] = sk;
+      gv[x] = sv;
+    }
+  } else if (!live) {
+    return;
   }
   float* dk = static_cast<float*>(a.dk);
   float* dv = static_cast<float*>(a.dv);
@@ -254,17 +324,42 @@ __global__ void __launch_bounds__(kWarps * 32) dkv_f32_kernel(const BackwardArgs
   }
 }
 
-template <int DV>
-cudaError_t launch_bwd_dv(const BackwardArgs& a, cudaStream_t s) {
+// Warps per row: at most 8, at most one per chunk of the row's walk, and
+// only as many as stay resident at once.
+int bwd_row_split(const BackwardArgs& a) {
   const int64_t rows = a.slices * a.N;
-  const unsigned grid = static_cast<unsigned>((rows + kWarps - 1) / kWarps);
-  dq_f32_kernel<DV><<<grid, kWarps * 32, 0, s>>>(a);
+  const int64_t chunks = static_cast<int64_t>(a.P) * ((a.N / a.P + 31) / 32);
+  const int64_t want = static_cast<int64_t>(device_sm_count()) * kResidentWarps;
+  int S = 1;
+  while (S < 8 && rows * S * 2 <= want && chunks >= S * 2) S *= 2;
+  return S;
+}
+
+template <int DV, int S>
+cudaError_t launch_bwd_rows(const BackwardArgs& a, cudaStream_t s) {
+  const int64_t rows = a.slices * a.N;
+  constexpr int kRows = RowCta<S>::kRows;
+  const unsigned grid = static_cast<unsigned>((rows + kRows - 1) / kRows);
+  dq_f32_kernel<DV, S><<<grid, RowCta<S>::kWarps * 32, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dkv_f32_kernel<DV><<<grid, kWarps * 32, 0, s>>>(a);
+  dkv_f32_kernel<DV, S><<<grid, RowCta<S>::kWarps * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 
+template <int DV>
+cudaError_t launch_bwd_dv(const BackwardArgs& a, cudaStream_t s) {
+  switch (bwd_row_split(a)) {
+    case 8:
+      return launch_bwd_rows<DV, 8>(a, s);
+    case 4:
+      return launch_bwd_rows<DV, 4>(a, s);
+    case 2:
+      return launch_bwd_rows<DV, 2>(a, s);
+    default:
+      return launch_bwd_rows<DV, 1>(a, s);
+  }
+}
 
 // ---- tiled kernels (d <= 128, grids of 128 CTAs or more) ----
 // As the tiled forward: a CTA of 4 warps keeps 64 rows stationary and

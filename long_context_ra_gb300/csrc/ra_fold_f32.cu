@@ -369,7 +369,16 @@ cudaError_t launch_dt(const FoldArgs& a, cudaStream_t s) {
 //   m* = max m_s,  w_s = exp(m_s - m*),  l* = sum w_s l_s,  o* = sum w_s o_s
 // (the same identity that lets the fold visit the keys in any order).
 
-constexpr int kRowWarps = 8;  // warps per CTA
+// A CTA holds the S warps of each of its rows: max(4, S) warps, so that
+// small grids still come in fine pieces.  The split kernels get 128
+// registers a thread (16 warps an SM), the unsplit one 64.
+template <int S>
+struct RowCta {
+  static constexpr int kWarps = S < 4 ? 4 : S;
+  static constexpr int kRows = kWarps / S;
+  static constexpr int kMinBlocks = S == 1 ? 8 : 16 / kWarps;
+};
+constexpr int kResidentWarps = 16;  // per SM, at 128 registers a thread
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -410,11 +419,13 @@ __device__ __forceinline__ float dot_row(const float* __restrict__ qrow,
 
 // DV: o values per lane (d <= 32 DV); S: warps per row (1, 2, 4 or 8).
 template <int DV, int S>
-__global__ void __launch_bounds__(kRowWarps * 32, 2) fold_f32_rows_kernel(const FoldArgs a) {
-  constexpr int kRows = kRowWarps / S;  // query rows per CTA
-  __shared__ __align__(16) float qs[kRowWarps][32 * DV];
-  __shared__ float part_o[kRowWarps][32 * DV];
-  __shared__ float part_ml[kRowWarps][2];
+__global__ void __launch_bounds__(RowCta<S>::kWarps * 32, RowCta<S>::kMinBlocks)
+    fold_f32_rows_kernel(const FoldArgs a) {
+  constexpr int kWarps = RowCta<S>::kWarps;
+  constexpr int kRows = RowCta<S>::kRows;  // query rows per CTA
+  __shared__ __align__(16) float qs[kWarps][32 * DV];
+  __shared__ float part_o[S > 1 ? kWarps : 1][32 * DV];
+  __shared__ float part_ml[S > 1 ? kWarps : 1][2];
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int sp = warp % S;  // this warp's share of the row's chunks
@@ -550,11 +561,11 @@ __global__ void __launch_bounds__(kRowWarps * 32, 2) fold_f32_rows_kernel(const 
 }
 
 // Warps per row: at most 8, at most one per chunk of the row's segment, and
-// only as many as stay resident at once (two CTAs of 8 warps on every SM).
+// only as many as stay resident at once.
 int row_split(const FoldArgs& a) {
   const int64_t rows = a.slices * a.nq * a.G;
   const int64_t chunks = (a.P / a.G) * ((a.nk / a.P + 31) / 32);  // per row and segment, at least
-  const int64_t want = static_cast<int64_t>(device_sm_count()) * 2 * kRowWarps;
+  const int64_t want = static_cast<int64_t>(device_sm_count()) * kResidentWarps;
   int S = 1;
   while (S < 8 && rows * S * 2 <= want && chunks >= S * 2) S *= 2;
   return S;
@@ -563,9 +574,9 @@ int row_split(const FoldArgs& a) {
 template <int DV, int S>
 cudaError_t launch_rows(const FoldArgs& a, cudaStream_t s) {
   const int64_t rows = a.slices * a.nq;
-  constexpr int kRows = kRowWarps / S;
+  constexpr int kRows = RowCta<S>::kRows;
   const dim3 grid(static_cast<unsigned>((rows + kRows - 1) / kRows), static_cast<unsigned>(a.G));
-  fold_f32_rows_kernel<DV, S><<<grid, kRowWarps * 32, 0, s>>>(a);
+  fold_f32_rows_kernel<DV, S><<<grid, RowCta<S>::kWarps * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 

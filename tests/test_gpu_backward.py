@@ -59,8 +59,10 @@ def full_check(O, q, k, v, P, dtype, causal=None):
     assert ra.ra_last_device_status() == 0
 
 
+# Small fp32 problems run on the row kernels, each row split over up to 8
+# warps: 256-row cases with 8 chunks a row take the 8-way split.
 @pytest.mark.parametrize("shape,P", [((1, 2, 40, 8), 4), ((2, 1, 33, 5), 3), ((1, 1, 64, 128), 1),
-                                     ((1, 2, 96, 64), 6)])
+                                     ((1, 2, 96, 64), 6), ((1, 1, 256, 64), 4)])
 def test_f32_backward(O, shape, P):
     q, k, v = (rnd(shape, 10 + s, torch.float32, 1.3) for s in range(3))
     full_check(O, q, k, v, P, torch.float32)
@@ -143,7 +145,8 @@ LAYOUTS = ["contiguous", "zigzag", "striped"]
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)
-@pytest.mark.parametrize("shape,P", [((1, 2, 48, 8), 4), ((2, 1, 36, 33), 6), ((1, 1, 64, 64), 2)])
+@pytest.mark.parametrize("shape,P", [((1, 2, 48, 8), 4), ((2, 1, 36, 33), 6), ((1, 1, 64, 64), 2),
+                                     ((1, 1, 256, 40), 4)])
 def test_f32_backward_causal(O, layout, shape, P):
     q, k, v = (rnd(shape, 40 + s, torch.float32, 1.3) for s in range(3))
     full_check(O, q, k, v, P, torch.float32, causal=layout)
