@@ -25,6 +25,8 @@
 // prefix, and the walk over a block stops at the first tile that starts after
 // the CTA's last query.
 
+#include <cooperative_groups.h>
+
 #include <cmath>
 
 #include "ra_internal.h"
@@ -92,8 +94,11 @@ __device__ __forceinline__ float group_sum(float x) {
   return x + __shfl_xor_sync(0xffffffffu, x, 4);
 }
 
+// split > 1: the CTAs of a cluster of `split` share one query tile, CTA r of
+// the cluster folding the tiles r, r + split, ... of the tile's walk; their
+// states are merged through distributed shared memory at the end.
 template <int DT>  // d <= DT; DT in {64, 128, 256}
-__global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
+__global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a, int split) {
   using S = Smem<DT>;
   constexpr int kCols = DT / 32;  // float4 column groups of o a lane holds
   extern __shared__ __align__(16) float sm[];
@@ -109,7 +114,8 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
   const int64_t cq = a.nq / a.P;
   const int64_t ck = a.nk / a.P;
   const int64_t tiles_q = (cq + kBM - 1) / kBM;
-  int64_t u = blockIdx.x;
+  const int cr = split > 1 ? static_cast<int>(blockIdx.x % split) : 0;  // rank in the cluster
+  int64_t u = blockIdx.x / split;
   const int64_t qt = u % tiles_q;
   u /= tiles_q;
   const int i = static_cast<int>(u % a.P);
@@ -151,7 +157,7 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
 #pragma unroll
       for (int y = 0; y < 4; ++y) o[x][c][y] = 0.f;
   }
-  if (a.mode == kFold) {
+  if (a.mode == kFold && cr == 0) {  // the incoming state joins the split once
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
       if (!rvalid[x]) continue;
@@ -182,6 +188,20 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
   TileCursor cur{t0, t1, i, 0, a.P, a.layout, a.causal != 0, 0, ck, qlast};
   if (cur.valid()) cur.set_block();
   cur.settle();
+  // this CTA's tiles: every split-th visible tile of the walk, from the cr-th
+  int tix = 0;
+  auto skip_others = [&]() {
+    while (cur.valid() && tix % split != cr) {
+      cur.advance();
+      ++tix;
+    }
+  };
+  auto advance_mine = [&]() {
+    cur.advance();
+    ++tix;
+    skip_others();
+  };
+  skip_others();
   auto fetch = [&](const TileCursor& tc) {
 #pragma unroll
     for (int it = 0; it < kPre; ++it) {
@@ -224,7 +244,7 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
       }
     }
     __syncthreads();
-    cur.advance();
+    advance_mine();
     if (kPrefetch && cur.valid()) fetch(cur);  // in flight during this tile's math
     {
 
@@ -304,10 +324,65 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a) {
     }
   }
 
-  // write the rows: out = o / l and lse, or the state (m, l, o)
   float* mo = a.mode == kPartial ? a.part.m[g] : a.st_m;
   float* lo = a.mode == kPartial ? a.part.l[g] : a.st_l;
   float* oo = a.mode == kPartial ? a.part.o[g] : a.st_o;
+  if (split > 1) {
+    // Each CTA's state of the tile's 64 rows ([row][m, l, o]) into its shared
+    // memory; CTA r then merges rows r 64 / split .. of every CTA's state
+    // (the identity that merges partial states) and writes them.
+    constexpr int kRS = DT + 2;
+    static_assert(kBM * kRS <= Smem<DT>::kFloats, "merge rows fit the tiles' space");
+    __syncthreads();  // every warp is done with the tiles
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      float* st = sm + (lrow0 + x) * kRS;
+      if (kg == 0) {
+        st[0] = m[x];
+        st[1] = l[x];
+      }
+#pragma unroll
+      for (int c = 0; c < kCols; ++c)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) st[2 + 4 * kg + 32 * c + y] = o[x][c][y];
+    }
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int rows_per = kBM / split;
+    for (int idx = tid; idx < rows_per * (d + 1); idx += kThreads) {
+      const int rr = cr * rows_per + idx / (d + 1);  // row of the tile
+      const int e = idx % (d + 1) - 1;              // column, or -1: the row's m and l
+      const int64_t r = r0 + rr;
+      if (r >= cq) continue;
+      float M = -INFINITY;
+      for (int p = 0; p < split; ++p) M = fmaxf(M, cluster.map_shared_rank(sm, p)[rr * kRS]);
+      float ls = 0.f, os = 0.f;
+      for (int p = 0; p < split; ++p) {
+        const float* st = cluster.map_shared_rank(sm, p) + rr * kRS;
+        // an empty part (m = -inf) adds nothing, also when every part is empty
+        const float w = st[0] == -INFINITY ? 0.f : expf(st[0] - M);
+        ls = fmaf(w, st[1], ls);
+        if (e >= 0) os = fmaf(w, st[2 + e], os);
+      }
+      const int64_t row = slice * a.nq + layout_pos(a.layout, i, r, a.P, cq);
+      if (a.mode == kForward) {
+        if (e >= 0)
+          static_cast<float*>(a.out)[row * d + e] = os / ls;
+        else
+          a.lse[row] = M + logf(ls);
+      } else if (e >= 0) {
+        oo[row * d + e] = os;
+      } else {
+        mo[row] = M;
+        lo[row] = ls;
+      }
+    }
+    cluster.sync();  // every CTA's shared memory stays until all have read it
+    return;
+  }
+
+  // write the rows: out = o / l and lse, or the state (m, l, o)
 #pragma unroll
   for (int x = 0; x < 4; ++x) {
     if (!rvalid[x]) continue;
@@ -353,9 +428,32 @@ cudaError_t launch_dt(const FoldArgs& a, cudaStream_t s) {
   }
   const int64_t cq = a.nq / a.P;
   const int64_t tiles_q = (cq + kBM - 1) / kBM;
-  const dim3 grid(static_cast<unsigned>(a.slices * a.P * tiles_q), static_cast<unsigned>(a.G));
-  fold_f32_kernel<DT><<<grid, kThreads, Smem<DT>::kBytes, s>>>(a);
-  return cudaGetLastError();
+  const int64_t units = a.slices * a.P * tiles_q;
+  // Too few CTAs for the SMs (two resident per SM below DT = 256, one at
+  // 256): split each query tile's walk over a cluster of up to 8 CTAs, as
+  // long as every CTA keeps at least two K/V tiles.
+  const int64_t resident = static_cast<int64_t>(device_sm_count()) * (DT == 256 ? 1 : 2);
+  const int64_t tiles_kv = (a.P / a.G) * ((a.nk / a.P + kBN - 1) / kBN);  // per unit, at least
+  int split = 1;
+  while (split < 8 && units * a.G * split * 2 <= resident && tiles_kv >= 4 * split) split *= 2;
+  if (split == 1) {
+    const dim3 grid(static_cast<unsigned>(units), static_cast<unsigned>(a.G));
+    fold_f32_kernel<DT><<<grid, kThreads, Smem<DT>::kBytes, s>>>(a, 1);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units * split), static_cast<unsigned>(a.G));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Smem<DT>::kBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fold_f32_kernel<DT>, a, split);
 }
 
 // ---- small problems: a few warps per query row ----

@@ -174,6 +174,27 @@ def test_tiled_partials_and_fold_chain(O):
                "tiled fold chain vs forward", 1e-5)
 
 
+def test_tiled_cluster_split_partials(O):
+    """A grid too small for the SMs: each 64-row query tile's walk is split
+    over a cluster of CTAs whose states merge in distributed shared memory.
+    Partial states (G = 2) of such a grid against the oracle's segment
+    states, and their merge against the forward."""
+    B, H, N, d, P = 1, 2, 2048, 64, 4
+    g = torch.Generator(device=DEV).manual_seed(75)
+    q, k, v = (torch.randn(B, H, N, d, device=DEV, generator=g) for _ in range(3))
+    out_f, lse_f = ra.ra_forward(q, k, v, P=P)
+    check_forward(O, q, k, v, P, out_f, lse_f)
+    parts = ra.ra_forward_partial(q, k, v, P=P, G=2)
+    for gi in range(2):
+        _, _, m, l, o = oracle_ring(O, q, k, v, P, t0=2 * gi, t1=2 * gi + 2, state=True)
+        assert max_err(parts[gi].m, m) <= 1e-5
+        assert np.max(np.abs(parts[gi].l.double().cpu().numpy() / l - 1)) <= 1e-5
+        check_close(parts[gi].o / parts[gi].l[:, None], o / l[:, None], torch.float32,
+                    f"cluster-split partial {gi} o/l", 1e-5)
+    out, lse = ra.ra_merge(parts, out_dtype=torch.float32)
+    check_same(out, out_f.reshape(-1, d), torch.float32, "cluster-split merge vs forward", 1e-5)
+
+
 def test_partial_and_merge_equal_forward(O):
     B, H, N, d, P = 1, 2, 96, 48, 6
     g = torch.Generator(device=DEV).manual_seed(5)
