@@ -25,6 +25,8 @@
 
 #include <cmath>
 
+#include <cooperative_groups.h>
+
 #include "ra_internal.h"
 #include "ra_layout.cuh"
 
@@ -373,8 +375,10 @@ constexpr int kTM = 64;         // stationary rows per CTA
 constexpr int kTN = 32;         // streamed rows per tile
 constexpr int kSS = kTM + 4;    // row stride of transposed stationary tiles, P^T, dS^T
 constexpr int kNS = kTN + 4;    // row stride of transposed streamed tiles
-// Each tiled CTA takes a whole SM (up to 158 KB of shared memory): below
-// about one CTA per SM the row kernels, with 16 x more CTAs, are faster.
+// Each tiled CTA takes a whole SM (up to 158 KB of shared memory): the tiled
+// kernels run when their CTAs, split over clusters where the tiles are too
+// few for the SMs, number at least kTiledMinCtas; below that the row
+// kernels, with many more warps, are faster.
 constexpr int64_t kTiledMinCtas = 128;
 
 template <int DT>
@@ -482,9 +486,49 @@ __device__ __forceinline__ void load_streamed(float* dT, float* dR, const float*
   }
 }
 
+// Sums of a split tile (split > 1: the CTAs of a cluster share one tile of
+// 64 stationary rows, CTA r taking the streamed tiles r, r + split, ... of
+// the walk): each CTA puts its nacc accumulators of the 64 rows into its
+// shared memory ([acc][row][DT]); after a cluster barrier CTA r adds up rows
+// r 64 / split .. over every CTA and writes them through put(row, e, sums);
+// a second barrier keeps every CTA's shared memory until all have read it.
+template <int DT>
+__device__ __forceinline__ void put_rows(float* sm, int z, const float (&acc)[4][DT / 32][4],
+                                         int lrow0, int kg) {
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int m = 0; m < DT / 32; ++m)
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+        sm[(z * kTM + lrow0 + x) * DT + 4 * kg + 32 * m + y] = acc[x][m][y];
+}
+
+// After put_rows of every accumulator (behind a __syncthreads).
+template <int DT, int kAcc, typename Put>
+__device__ __forceinline__ void split_sums(float* sm, int split, int cr, int tid, int d, Put put) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  const int rows_per = kTM / split;
+  for (int idx = tid; idx < rows_per * d; idx += kTT) {
+    const int rr = cr * rows_per + idx / d, e = idx % d;
+    float sums[kAcc];
+#pragma unroll
+    for (int z = 0; z < kAcc; ++z) sums[z] = 0.f;
+    for (int p = 0; p < split; ++p) {
+      const float* peer = cluster.map_shared_rank(sm, p);
+#pragma unroll
+      for (int z = 0; z < kAcc; ++z) sums[z] += peer[(z * kTM + rr) * DT + e];
+    }
+    put(rr, e, sums);
+  }
+  cluster.sync();
+}
+
 // dQ for 64 query rows of block i: the key blocks in ring order (i - t) mod P.
 template <int DT>
-__global__ void __launch_bounds__(kTT) dq_f32_tiled(const BackwardArgs a) {
+__global__ void __launch_bounds__(kTT) dq_f32_tiled(const BackwardArgs a, int split) {
   using S = DqSmem<DT>;
   extern __shared__ __align__(16) float sm[];
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -492,7 +536,8 @@ __global__ void __launch_bounds__(kTT) dq_f32_tiled(const BackwardArgs a) {
   const int d = a.d;
   const int64_t c = a.N / a.P;
   const int64_t tiles = (c + kTM - 1) / kTM;
-  int64_t u = blockIdx.x;
+  const int cr = split > 1 ? static_cast<int>(blockIdx.x % split) : 0;  // rank in the cluster
+  int64_t u = blockIdx.x / split;
   const int64_t qt = u % tiles;
   u /= tiles;
   const int i = static_cast<int>(u % a.P);
@@ -526,11 +571,13 @@ __global__ void __launch_bounds__(kTT) dq_f32_tiled(const BackwardArgs a) {
   const int64_t rlast = (r0 + kTM < c ? r0 + kTM : c) - 1;
   const int64_t qlast = layout_pos(a.layout, i, rlast, a.P, c);
 
+  int tix = 0;  // visible streamed tiles so far; this CTA takes every split-th
   for (int t = 0; t < a.P; ++t) {
     int j = (i - t) % a.P;
     if (j < 0) j += a.P;
     for (int64_t c0 = 0; c0 < c; c0 += kTN) {
       if (a.causal && layout_pos(a.layout, j, c0, a.P, c) > qlast) break;  // rest of block masked
+      if (tix++ % split != cr) continue;
       __syncthreads();
       load_streamed<DT>(sm + S::kK, sm + S::kKr, k, a.layout, j, c0, a.P, c, d, tid);
       load_streamed<DT>(sm + S::kV, nullptr, v, a.layout, j, c0, a.P, c, d, tid);
@@ -560,6 +607,18 @@ __global__ void __launch_bounds__(kTT) dq_f32_tiled(const BackwardArgs a) {
     }
   }
   float* dq = static_cast<float*>(a.dq);
+  if (split > 1) {
+    static_assert(kTM * DT <= DqSmem<DT>::kBytes / 4, "the split's sums fit the tiles' space");
+    __syncthreads();  // every warp is done with the tiles
+    put_rows<DT>(sm, 0, acc, lrow0, kg);
+    split_sums<DT, 1>(sm, split, cr, tid, d, [&](int rr, int e, const float* sums) {
+      const int64_t r = r0 + rr;
+      if (r >= c) return;
+      const int64_t row = (sb + layout_pos(a.layout, i, r, a.P, c)) * d;
+      dq[row + e] = (a.accumulate ? dq[row + e] : 0.f) + sums[0] * a.tau;
+    });
+    return;
+  }
 #pragma unroll
   for (int x = 0; x < 4; ++x) {
     if (!rvalid[x]) continue;
@@ -576,7 +635,7 @@ __global__ void __launch_bounds__(kTT) dq_f32_tiled(const BackwardArgs a) {
 
 // dK, dV for 64 key rows of block j: the query blocks (j + t) mod P.
 template <int DT>
-__global__ void __launch_bounds__(kTT) dkv_f32_tiled(const BackwardArgs a) {
+__global__ void __launch_bounds__(kTT) dkv_f32_tiled(const BackwardArgs a, int split) {
   using S = DkvSmem<DT>;
   extern __shared__ __align__(16) float sm[];
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -584,7 +643,8 @@ __global__ void __launch_bounds__(kTT) dkv_f32_tiled(const BackwardArgs a) {
   const int d = a.d;
   const int64_t c = a.N / a.P;
   const int64_t tiles = (c + kTM - 1) / kTM;
-  int64_t u = blockIdx.x;
+  const int cr = split > 1 ? static_cast<int>(blockIdx.x % split) : 0;  // rank in the cluster
+  int64_t u = blockIdx.x / split;
   const int64_t kt = u % tiles;
   u /= tiles;
   const int j = static_cast<int>(u % a.P);
@@ -614,6 +674,7 @@ __global__ void __launch_bounds__(kTT) dkv_f32_tiled(const BackwardArgs a) {
   }
   const int64_t kfirst = layout_pos(a.layout, j, r0, a.P, c);  // the CTA's first key position
 
+  int tix = 0;  // visible streamed tiles so far; this CTA takes every split-th
   for (int t = 0; t < a.P; ++t) {
     const int i = (j + t) % a.P;  // the query block this key block meets at step t
     for (int64_t c0 = 0; c0 < c; c0 += kTN) {
@@ -622,6 +683,7 @@ __global__ void __launch_bounds__(kTT) dkv_f32_tiled(const BackwardArgs a) {
         const int64_t qe = (c0 + kTN < c ? c0 + kTN : c) - 1;
         if (layout_pos(a.layout, i, qe, a.P, c) < kfirst) continue;
       }
+      if (tix++ % split != cr) continue;
       __syncthreads();
       load_streamed<DT>(sm + S::kQ, sm + S::kQr, q, a.layout, i, c0, a.P, c, d, tid);
       load_streamed<DT>(sm + S::kG, sm + S::kGr, g, a.layout, i, c0, a.P, c, d, tid);
@@ -658,6 +720,20 @@ __global__ void __launch_bounds__(kTT) dkv_f32_tiled(const BackwardArgs a) {
   }
   float* dk = static_cast<float*>(a.dk);
   float* dv = static_cast<float*>(a.dv);
+  if (split > 1) {
+    static_assert(2 * kTM * DT <= DkvSmem<DT>::kBytes / 4, "the split's sums fit the tiles' space");
+    __syncthreads();  // every warp is done with the tiles
+    put_rows<DT>(sm, 0, gk, lrow0, kg);
+    put_rows<DT>(sm, 1, gv, lrow0, kg);
+    split_sums<DT, 2>(sm, split, cr, tid, d, [&](int rr, int e, const float* sums) {
+      const int64_t r = r0 + rr;
+      if (r >= c) return;
+      const int64_t row = (sb + layout_pos(a.layout, j, r, a.P, c)) * d;
+      dk[row + e] = (a.accumulate ? dk[row + e] : 0.f) + sums[0] * a.tau;
+      dv[row + e] = (a.accumulate ? dv[row + e] : 0.f) + sums[1];
+    });
+    return;
+  }
 #pragma unroll
   for (int x = 0; x < 4; ++x) {
     if (!rvalid[x]) continue;
@@ -675,6 +751,18 @@ __global__ void __launch_bounds__(kTT) dkv_f32_tiled(const BackwardArgs a) {
   }
 }
 
+// A tiled CTA takes a whole SM: when there are too few tiles of 64 rows for
+// the SMs, each tile's walk is split over a cluster of 2, 4 or 8 CTAs, as
+// long as every CTA keeps at least two streamed tiles.
+int tiled_split(const BackwardArgs& a) {
+  const int64_t ctas = a.slices * a.P * ((a.N / a.P + kTM - 1) / kTM);
+  const int64_t walk = static_cast<int64_t>(a.P) * ((a.N / a.P + kTN - 1) / kTN);
+  const int64_t sms = device_sm_count();
+  int split = 1;
+  while (split < 8 && ctas * split * 2 <= sms && walk >= 4 * split) split *= 2;
+  return split;
+}
+
 template <int DT>
 cudaError_t launch_tiled(const BackwardArgs& a, cudaStream_t s) {
   static thread_local int configured_device = -1;
@@ -690,13 +778,25 @@ cudaError_t launch_tiled(const BackwardArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
+  const int split = tiled_split(a);
   const int64_t c = a.N / a.P;
-  const unsigned grid = static_cast<unsigned>(a.slices * a.P * ((c + kTM - 1) / kTM));
-  dq_f32_tiled<DT><<<grid, kTT, DqSmem<DT>::kBytes, s>>>(a);
-  e = cudaGetLastError();
+  const unsigned grid = static_cast<unsigned>(a.slices * a.P * ((c + kTM - 1) / kTM) * split);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTT);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = split > 1 ? 1 : 0;
+  cfg.dynamicSmemBytes = DqSmem<DT>::kBytes;
+  e = cudaLaunchKernelEx(&cfg, dq_f32_tiled<DT>, a, split);
   if (e != cudaSuccess) return e;
-  dkv_f32_tiled<DT><<<grid, kTT, DkvSmem<DT>::kBytes, s>>>(a);
-  return cudaGetLastError();
+  cfg.dynamicSmemBytes = DkvSmem<DT>::kBytes;
+  return cudaLaunchKernelEx(&cfg, dkv_f32_tiled<DT>, a, split);
 }
 }  // namespace
 
@@ -715,7 +815,7 @@ cudaError_t launch_delta(const void* out, const void* dout, const float* lse, fl
 
 cudaError_t launch_backward_f32(const BackwardArgs& a, cudaStream_t s) {
   const int64_t tiled_ctas = a.slices * a.P * ((a.N / a.P + kTM - 1) / kTM);
-  if (a.d <= 128 && tiled_ctas >= kTiledMinCtas) {
+  if (a.d <= 128 && tiled_ctas * tiled_split(a) >= kTiledMinCtas) {
     if (a.d <= 64) return launch_tiled<64>(a, s);
     return launch_tiled<128>(a, s);
   }

@@ -80,6 +80,23 @@ def test_f32_backward_tiled(O, shape, P):
     full_check(O, q, k, v, P, torch.float32)
 
 
+# fp32 shapes with too few 64-row tiles for the SMs: each tile's walk is
+# split over a cluster of 2 or 4 CTAs, summed in distributed shared memory
+F32_SPLIT = [((1, 4, 1024, 64), 4), ((1, 1, 2048, 128), 8), ((1, 2, 1024, 40), 2)]
+
+
+@pytest.mark.parametrize("shape,P", F32_SPLIT)
+def test_f32_backward_tiled_cluster_split(O, shape, P):
+    q, k, v = (rnd(shape, 70 + s, torch.float32, 1.3) for s in range(3))
+    full_check(O, q, k, v, P, torch.float32)
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
+def test_f32_backward_tiled_cluster_split_causal(O, layout):
+    q, k, v = (rnd((1, 2, 2048, 64), 74 + s, torch.float32, 1.3) for s in range(3))
+    full_check(O, q, k, v, 4, torch.float32, causal=layout)
+
+
 @pytest.mark.parametrize("layout", ["contiguous", "zigzag", "striped"])
 def test_f32_backward_tiled_causal(O, layout):
     q, k, v = (rnd((1, 8, 1024, 72), 64 + s, torch.float32, 1.3) for s in range(3))
