@@ -40,9 +40,9 @@ constexpr int kBM = 64;        // query rows per CTA
 constexpr int kBN = 32;        // keys per K/V tile
 constexpr int kQS = kBM + 4;   // row stride of the transposed Q and P tiles (floats)
 constexpr int kKS = kBN + 4;   // row stride of the transposed K tile (floats)
-// below this many CTAs the tiled kernel leaves most SMs idle, and the
-// row-per-warp kernel (64 x more CTAs) is faster
-constexpr int64_t kSmallGrid = 32;
+// below this many CTAs (after the cluster split) the tiled kernel leaves
+// most SMs idle, and the split-row kernel is faster
+constexpr int64_t kSmallGrid = 128;
 
 // Shared-memory footprint (floats) for head dimensions up to DT.
 template <int DT>
@@ -414,6 +414,23 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a, in
   }
 }
 
+// CTAs of the tiled kernel before the split: one per 64-row query tile
+int64_t tiled_units(const FoldArgs& a) {
+  return a.slices * a.P * ((a.nq / a.P + kBM - 1) / kBM);
+}
+
+// Too few CTAs for the SMs (two resident per SM below DT = 256, one at
+// 256): each query tile's walk is split over a cluster of up to 8 CTAs, as
+// long as every CTA keeps at least two K/V tiles.
+int tiled_split(const FoldArgs& a, int dt) {
+  const int64_t resident = static_cast<int64_t>(device_sm_count()) * (dt == 256 ? 1 : 2);
+  const int64_t tiles_kv = (a.P / a.G) * ((a.nk / a.P + kBN - 1) / kBN);  // per unit, at least
+  const int64_t ctas = tiled_units(a) * a.G;
+  int split = 1;
+  while (split < 8 && ctas * split * 2 <= resident && tiles_kv >= 4 * split) split *= 2;
+  return split;
+}
+
 template <int DT>
 cudaError_t launch_dt(const FoldArgs& a, cudaStream_t s) {
   static thread_local int configured_device = -1;
@@ -426,16 +443,8 @@ cudaError_t launch_dt(const FoldArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const int64_t cq = a.nq / a.P;
-  const int64_t tiles_q = (cq + kBM - 1) / kBM;
-  const int64_t units = a.slices * a.P * tiles_q;
-  // Too few CTAs for the SMs (two resident per SM below DT = 256, one at
-  // 256): split each query tile's walk over a cluster of up to 8 CTAs, as
-  // long as every CTA keeps at least two K/V tiles.
-  const int64_t resident = static_cast<int64_t>(device_sm_count()) * (DT == 256 ? 1 : 2);
-  const int64_t tiles_kv = (a.P / a.G) * ((a.nk / a.P + kBN - 1) / kBN);  // per unit, at least
-  int split = 1;
-  while (split < 8 && units * a.G * split * 2 <= resident && tiles_kv >= 4 * split) split *= 2;
+  const int64_t units = tiled_units(a);
+  const int split = tiled_split(a, DT);
   if (split == 1) {
     const dim3 grid(static_cast<unsigned>(units), static_cast<unsigned>(a.G));
     fold_f32_kernel<DT><<<grid, kThreads, Smem<DT>::kBytes, s>>>(a, 1);
@@ -696,8 +705,8 @@ cudaError_t launch_dv(const FoldArgs& a, cudaStream_t s) {
 
 cudaError_t launch_fold_f32(const FoldArgs& a, cudaStream_t s) {
   if (a.slices * a.nq == 0) return cudaSuccess;
-  const int64_t tiled_ctas = a.slices * a.P * ((a.nq / a.P + kBM - 1) / kBM) * a.G;
-  if (tiled_ctas < kSmallGrid) {
+  const int dt = a.d <= 64 ? 64 : (a.d <= 128 ? 128 : 256);
+  if (tiled_units(a) * a.G * tiled_split(a, dt) < kSmallGrid) {
     if (a.d <= 32) return launch_dv<1>(a, s);
     if (a.d <= 64) return launch_dv<2>(a, s);
     if (a.d <= 128) return launch_dv<4>(a, s);
