@@ -624,7 +624,7 @@ def run_ours(args, w) -> None:
         alu_peak = sms * 128 * 2 * mhz * 1e6 / 1e12
         roofline.update({"bound": "alu", "peak": alu_peak, "frac": achieved / alu_peak,
                          "traffic": None,
-                         "kernel": "fold_f32 (tiled, or one warp per row on small grids)",
+                         "kernel": "fold_f32 (tiled, split over clusters on small grids, or rows split over warps on the smallest)",
                          "peak_source": f"derived: {sms} SMs x 128 FP32 lanes x 2 flops x "
                                         f"{mhz:.0f} MHz"})
 
