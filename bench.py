@@ -627,6 +627,9 @@ def run_ours(args, w) -> None:
                          "kernel": "fold_f32 (tiled, split over clusters on small grids, or rows split over warps on the smallest)",
                          "peak_source": f"derived: {sms} SMs x 128 FP32 lanes x 2 flops x "
                                         f"{mhz:.0f} MHz"})
+        if ms < 0.1:
+            roofline["note"] = (f"a {flops / 1e6:.1f} MFLOP problem in {ms * 1e3:.1f} us a "
+                                "call: launch- and latency-bound, not ALU-bound")
 
     cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.causal \
