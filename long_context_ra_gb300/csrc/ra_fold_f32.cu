@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a, in
       for (int x = 0; x < 4; ++x)
 #pragma unroll
         for (int y = 0; y < 4; ++y) s[x][y] = 0.f;
-#pragma unroll 4
+#pragma unroll 16
       for (int e = 0; e < d; ++e) {
         const float4 qa = *reinterpret_cast<const float4*>(qT + e * kQS + lrow0);
         const float4 ka = *reinterpret_cast<const float4*>(kT + e * kKS + 4 * kg);
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a, in
         *reinterpret_cast<float4*>(pT + (4 * kg + y) * kQS + lrow0) =
             make_float4(p[0][y], p[1][y], p[2][y], p[3][y]);
       __syncwarp();
-#pragma unroll 4
+#pragma unroll 16
       for (int key = 0; key < kBN; ++key) {
         const float4 pp = *reinterpret_cast<const float4*>(pT + key * kQS + lrow0);
         const float pv[4] = {pp.x, pp.y, pp.z, pp.w};
