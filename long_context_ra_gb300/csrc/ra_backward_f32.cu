@@ -414,7 +414,7 @@ __device__ __forceinline__ void two_blocks(const float* a, const float* b, const
   for (int x = 0; x < 4; ++x)
 #pragma unroll
     for (int y = 0; y < 4; ++y) s[x][y] = t[x][y] = 0.f;
-#pragma unroll 2
+#pragma unroll 8
   for (int e = 0; e < d; ++e) {
     const float4 a4 = *reinterpret_cast<const float4*>(a + e * sa + r0);
     const float4 b4 = *reinterpret_cast<const float4*>(b + e * sb + c0);
@@ -436,7 +436,7 @@ __device__ __forceinline__ void two_blocks(const float* a, const float* b, const
 template <int DT>
 __device__ __forceinline__ void accumulate_rows(const float* wT, const float* src, int r0, int kg,
                                                 float (&acc)[4][DT / 32][4]) {
-#pragma unroll 4
+#pragma unroll 8
   for (int k = 0; k < kTN; ++k) {
     const float4 w4 = *reinterpret_cast<const float4*>(wT + k * kSS + r0);
     const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
