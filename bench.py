@@ -42,7 +42,8 @@ METRIC = "attention TFLOP/s (4·B·H·N²·d) at 1 GB300 and % of dense bf16 ten
 UNIT = "TFLOP/s"
 KERNEL_SOURCES = ["long_context_ra_gb300/csrc/ra_fold_sm103.cu",
                   "long_context_ra_gb300/csrc/sm103_pipeline.cuh",
-                  "long_context_ra_gb300/csrc/sm103_ptx.cuh"]
+                  "long_context_ra_gb300/csrc/sm103_ptx.cuh",
+                  "long_context_ra_gb300/csrc/ra_layout.cuh"]
 
 
 def kernel_sha() -> str:

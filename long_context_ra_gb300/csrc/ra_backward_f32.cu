@@ -538,10 +538,13 @@ __global__ void __launch_bounds__(kTT) dq_f32_tiled(const BackwardArgs a, int sp
   const int64_t tiles = (c + kTM - 1) / kTM;
   const int cr = split > 1 ? static_cast<int>(blockIdx.x % split) : 0;  // rank in the cluster
   int64_t u = blockIdx.x / split;
-  const int64_t qt = u % tiles;
+  int qti = static_cast<int>(u % tiles);
   u /= tiles;
-  const int i = static_cast<int>(u % a.P);
+  int i = static_cast<int>(u % a.P);
   const int64_t slice = u / a.P;
+  // under the mask the heaviest query tiles come first within each slice
+  if (a.causal) causal_order(a.layout, a.P, static_cast<int>(tiles), true, i, qti);
+  const int64_t qt = qti;
   const int64_t sb = slice * a.N;
   const float* q = static_cast<const float*>(a.q) + sb * d;
   const float* k = static_cast<const float*>(a.k) + sb * d;
@@ -645,10 +648,13 @@ __global__ void __launch_bounds__(kTT) dkv_f32_tiled(const BackwardArgs a, int s
   const int64_t tiles = (c + kTM - 1) / kTM;
   const int cr = split > 1 ? static_cast<int>(blockIdx.x % split) : 0;  // rank in the cluster
   int64_t u = blockIdx.x / split;
-  const int64_t kt = u % tiles;
+  int kti = static_cast<int>(u % tiles);
   u /= tiles;
-  const int j = static_cast<int>(u % a.P);
+  int j = static_cast<int>(u % a.P);
   const int64_t slice = u / a.P;
+  // under the mask the heaviest key tiles (the first rows) come first
+  if (a.causal) causal_order(a.layout, a.P, static_cast<int>(tiles), false, j, kti);
+  const int64_t kt = kti;
   const int64_t sb = slice * a.N;
   const float* q = static_cast<const float*>(a.q) + sb * d;
   const float* k = static_cast<const float*>(a.k) + sb * d;

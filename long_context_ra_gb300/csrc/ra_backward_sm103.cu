@@ -37,6 +37,7 @@
 #include <cmath>
 
 #include "ra_internal.h"
+#include "ra_layout.cuh"
 #include "sm103_pipeline.cuh"
 #include "sm103_ptx.cuh"
 
@@ -392,8 +393,7 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
   // unit: (slice, key block j, key tile kt); walk: the query tiles of the
   // blocks i = (j + t) mod P (see KWalk).  Under the mask the heaviest units
   // (the first key rows, seen by the most queries) come first within each
-  // slice: in block order for the contiguous layout; for zigzag, where block
-  // j holds chunks j and 2P-1-j, in chunk order 0 .. 2P-1.
+  // slice (causal_order).
   const int64_t c = a.N / a.P;
   const int tiles = static_cast<int>(c / kBN);
   int64_t u = blockIdx.x;
@@ -401,13 +401,7 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
   u /= tiles;
   int j = static_cast<int>(u % a.P);
   const int64_t slice = u / a.P;
-  if (kCausal && a.layout == kZigzag && tiles % 2 == 0) {
-    const int tpc = tiles / 2;  // key tiles per chunk
-    const int r = j * tiles + kt;
-    const int k = r / tpc;  // chunk
-    j = k < a.P ? k : 2 * a.P - 1 - k;
-    kt = (k < a.P ? 0 : tpc) + r % tpc;
-  }
+  if (kCausal) causal_order(a.layout, a.P, tiles, false, j, kt);
   const bool striped = a.layout == kStriped;
   KWalk walk;
   walk.j = j;
@@ -717,9 +711,7 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
 
   // unit: (slice, query block i, query tile qt); walk: the forward's ring
   // order over key tiles (Walk).  Under the mask the heaviest units (the
-  // last query rows) come first within each slice: in reverse block order
-  // for the contiguous layout; for zigzag, where block i holds chunks i and
-  // 2P-1-i, in chunk order 2P-1 .. 0.
+  // last query rows) come first within each slice (causal_order).
   const int64_t c = a.N / a.P;
   const int tiles = static_cast<int>(c / kBN);
   int64_t u = blockIdx.x;
@@ -727,18 +719,7 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
   u /= tiles;
   int i = static_cast<int>(u % a.P);
   const int64_t slice = u / a.P;
-  if (kCausal) {
-    if (a.layout == kZigzag && tiles % 2 == 0) {
-      const int tpc = tiles / 2;  // query tiles per chunk
-      const int r = i * tiles + qt;
-      const int k = 2 * a.P - 1 - r / tpc;  // chunk
-      i = k < a.P ? k : 2 * a.P - 1 - k;
-      qt = (k < a.P ? 0 : tpc) + tpc - 1 - r % tpc;
-    } else {
-      qt = tiles - 1 - qt;
-      i = a.P - 1 - i;
-    }
-  }
+  if (kCausal) causal_order(a.layout, a.P, tiles, true, i, qt);
   const bool striped = a.layout == kStriped;
   const int64_t qlr0 = static_cast<int64_t>(qt) * kBM;  // first local query row
   Walk walk;

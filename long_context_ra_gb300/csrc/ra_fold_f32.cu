@@ -116,10 +116,13 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a, in
   const int64_t tiles_q = (cq + kBM - 1) / kBM;
   const int cr = split > 1 ? static_cast<int>(blockIdx.x % split) : 0;  // rank in the cluster
   int64_t u = blockIdx.x / split;
-  const int64_t qt = u % tiles_q;
+  int qti = static_cast<int>(u % tiles_q);
   u /= tiles_q;
-  const int i = static_cast<int>(u % a.P);
+  int i = static_cast<int>(u % a.P);
   const int64_t slice = u / a.P;
+  // under the mask the heaviest query tiles come first within each slice
+  if (a.causal) causal_order(a.layout, a.P, static_cast<int>(tiles_q), true, i, qti);
+  const int64_t qt = qti;
   const int g = blockIdx.y;  // segment
   const int t0 = static_cast<int>(static_cast<int64_t>(g) * a.P / a.G);
   const int t1 = static_cast<int>(static_cast<int64_t>(g + 1) * a.P / a.G);

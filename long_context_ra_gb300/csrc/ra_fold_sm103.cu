@@ -48,6 +48,7 @@
 #include <cmath>
 
 #include "ra_internal.h"
+#include "ra_layout.cuh"
 #include "sm103_pipeline.cuh"
 #include "sm103_ptx.cuh"
 
@@ -210,8 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- work unit: (slice, query block i, segment g, tile pair pr) ----
   // Consecutive CTAs share (slice, i, g) and so walk the same K/V tiles in
   // the same order (L2 reuse).  Under the causal mask the heaviest units (the
-  // last query rows) are numbered first within each slice, so that the last
-  // CTAs to start are the lightest.
+  // last query rows) are numbered first within each slice (causal_order).
   const int64_t cq = a.nq / a.P;
   const int64_t ck = a.nk / a.P;
   const int tiles_q = static_cast<int>(cq / kBM);
@@ -223,22 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   u /= a.G;
   int i = static_cast<int>(u % a.P);
   const int64_t slice = u / a.P;
-  if (kCausal) {
-    if (a.layout == kZigzag && tiles_q % 4 == 0) {
-      // zigzag: block i holds chunks i and 2P-1-i of the sequence, so the
-      // order of descending positions runs over the chunks 2P-1 .. 0 (each
-      // half a block, pairs/2 tile pairs) rather than over the blocks
-      const int ppc = pairs / 2;
-      const int r = i * pairs + pr;
-      const int k = 2 * a.P - 1 - r / ppc;  // chunk
-      const int pc = ppc - 1 - r % ppc;     // tile pair within the chunk
-      i = k < a.P ? k : 2 * a.P - 1 - k;
-      pr = (k < a.P ? 0 : ppc) + pc;
-    } else {
-      pr = pairs - 1 - pr;
-      i = a.P - 1 - i;
-    }
-  }
+  if (kCausal) causal_order(a.layout, a.P, pairs, true, i, pr);
   const bool has_t1 = 2 * pr + 1 < tiles_q;
   const bool striped = a.layout == kStriped;
   Walk walk;
