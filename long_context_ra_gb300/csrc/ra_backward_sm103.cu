@@ -30,9 +30,10 @@
 //
 // Warp roles (G elementwise warpgroups; 128 G + 64 threads): warps 0 .. 4G-1
 // elementwise (thread = tile row = TMEM lane), warp 4G TMA producer, warp
-// 4G+1 TMEM allocator and MMA issuer.  G = 4 where the kernel's registers
-// allow it (the plain kernels), else 2 (the causal ones, whose walk state
-// needs more).  Every wait is bounded (see sm103_pipeline.cuh).
+// 4G+1 TMEM allocator and MMA issuer.  G = 4 for the plain kernels and 2
+// for the causal ones, each the faster of the two as measured (the causal
+// kernels fit four warpgroups at 82-92 registers, but ran 6 % slower with
+// them).  Every wait is bounded (see sm103_pipeline.cuh).
 
 #include <cmath>
 
