@@ -27,6 +27,7 @@
 
 #include <cooperative_groups.h>
 
+#include "ra_fork.h"
 #include "ra_internal.h"
 #include "ra_layout.cuh"
 
@@ -342,11 +343,19 @@ cudaError_t launch_bwd_rows(const BackwardArgs& a, cudaStream_t s) {
   const int64_t rows = a.slices * a.N;
   constexpr int kRows = RowCta<S>::kRows;
   const unsigned grid = static_cast<unsigned>((rows + kRows - 1) / kRows);
-  dq_f32_kernel<DV, S><<<grid, RowCta<S>::kWarps * 32, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  // the two kernels are independent: dK/dV on a forked side stream
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  ForkJoin fj;
+  if (e == cudaSuccess) e = fj.fork(s, dev);
   if (e != cudaSuccess) return e;
-  dkv_f32_kernel<DV, S><<<grid, RowCta<S>::kWarps * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  dq_f32_kernel<DV, S><<<grid, RowCta<S>::kWarps * 32, 0, s>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dkv_f32_kernel<DV, S><<<grid, RowCta<S>::kWarps * 32, 0, fj.side>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return fj.join(s);
 }
 
 template <int DV>
@@ -798,11 +807,18 @@ cudaError_t launch_tiled(const BackwardArgs& a, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = split > 1 ? 1 : 0;
+  // the two kernels are independent: dK/dV on a forked side stream
+  ForkJoin fj;
+  e = fj.fork(s, dev);
+  if (e != cudaSuccess) return e;
   cfg.dynamicSmemBytes = DqSmem<DT>::kBytes;
   e = cudaLaunchKernelEx(&cfg, dq_f32_tiled<DT>, a, split);
   if (e != cudaSuccess) return e;
   cfg.dynamicSmemBytes = DkvSmem<DT>::kBytes;
-  return cudaLaunchKernelEx(&cfg, dkv_f32_tiled<DT>, a, split);
+  cfg.stream = fj.side;
+  e = cudaLaunchKernelEx(&cfg, dkv_f32_tiled<DT>, a, split);
+  if (e != cudaSuccess) return e;
+  return fj.join(s);
 }
 }  // namespace
 

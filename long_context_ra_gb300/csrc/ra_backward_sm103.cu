@@ -36,8 +36,8 @@
 // them).  Every wait is bounded (see sm103_pipeline.cuh).
 
 #include <cmath>
-#include <mutex>
 
+#include "ra_fork.h"
 #include "ra_internal.h"
 #include "ra_layout.cuh"
 #include "sm103_pipeline.cuh"
@@ -975,43 +975,6 @@ __global__ void __launch_bounds__(Roles<G>::kThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
 }
-
-// A side stream per device (created on first use) and, per host thread and
-// device, the two events that fork work onto it from a caller's stream and
-// join it back.  An event re-recorded by a later call is safe: a wait binds
-// to the record made before it was enqueued.
-struct ForkJoin {
-  cudaStream_t side = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
-
-  cudaError_t fork(cudaStream_t s, int dev) {
-    static std::mutex mu;
-    static cudaStream_t sides[kMaxDevices] = {};
-    thread_local cudaEvent_t forks[kMaxDevices] = {}, joins[kMaxDevices] = {};
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    {
-      std::lock_guard<std::mutex> lock(mu);
-      if (!sides[dev]) {
-        const cudaError_t e = cudaStreamCreateWithFlags(&sides[dev], cudaStreamNonBlocking);
-        if (e != cudaSuccess) return e;
-      }
-      side = sides[dev];
-    }
-    if (!forks[dev]) {
-      cudaError_t e = cudaEventCreateWithFlags(&forks[dev], cudaEventDisableTiming);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&joins[dev], cudaEventDisableTiming);
-      if (e != cudaSuccess) return e;
-    }
-    ev_fork = forks[dev];
-    ev_join = joins[dev];
-    const cudaError_t e = cudaEventRecord(ev_fork, s);
-    return e == cudaSuccess ? cudaStreamWaitEvent(side, ev_fork, 0) : e;
-  }
-  cudaError_t join(cudaStream_t s) {
-    const cudaError_t e = cudaEventRecord(ev_join, side);
-    return e == cudaSuccess ? cudaStreamWaitEvent(s, ev_join, 0) : e;
-  }
-};
 
 template <int D, bool kCausal>
 cudaError_t launch_d(const BackwardArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
