@@ -1,7 +1,7 @@
 // fp32 fold kernel (FFMA only, no TF32): the exact-precision path for any
 // head dimension 1 <= d <= 256 and any block size.
 //
-// One CTA (4 warps) owns 64 query rows of one query block i ("Ring
+// One CTA (4 or 8 warps) owns 64 or 128 query rows of one query block i ("Ring
 // Attention: the math", section "Sharding the sequence": queries stay home)
 // and walks the key blocks in ring order j = (i - t) mod P (section "The ring
 // schedule: passing K/V around").  Each block is folded 32 keys at a time
@@ -12,7 +12,7 @@
 // Folding a block in chunks is exact by the same identity.
 //
 // The query tile and each 32-key K/V tile are staged in shared memory and
-// shared by the 64 rows.  Warp w owns rows 16w .. 16w + 15; lane (rg, kg) =
+// shared by the CTA's rows.  Warp w owns rows 16w .. 16w + 15; lane (rg, kg) =
 // (lane / 8, lane % 8) computes the 4 x 4 block of scores of rows
 // 16w + 4rg + 0..3 against keys 4kg + 0..3, and holds o of the same 4 rows
 // in the columns 4kg + 32m + 0..3.  A row's max and sum are reduced over the
@@ -35,18 +35,17 @@
 namespace ra {
 namespace {
 
-constexpr int kThreads = 128;  // 4 warps
-constexpr int kBM = 64;        // query rows per CTA
 constexpr int kBN = 32;        // keys per K/V tile
-constexpr int kQS = kBM + 4;   // row stride of the transposed Q and P tiles (floats)
 constexpr int kKS = kBN + 4;   // row stride of the transposed K tile (floats)
-// below this many CTAs (after the cluster split) the tiled kernel leaves
-// most SMs idle, and the split-row kernel is faster
+// below this many CTAs of 64 rows (after the cluster split) the tiled
+// kernel leaves most SMs idle, and the split-row kernel is faster
 constexpr int64_t kSmallGrid = 128;
 
-// Shared-memory footprint (floats) for head dimensions up to DT.
-template <int DT>
+// Shared-memory footprint (floats) for head dimensions up to DT and BM
+// query rows per CTA (2 BM threads: warp w owns rows 16w .. 16w + 15).
+template <int DT, int BM>
 struct Smem {
+  static constexpr int kQS = BM + 4;              // row stride of Q^T and P^T
   static constexpr int kQ = 0;                    // Q^T  [DT][kQS]
   static constexpr int kK = kQ + DT * kQS;        // K^T  [DT][kKS]
   static constexpr int kV = kK + DT * kKS;        // V    [kBN][DT + 4]
@@ -97,9 +96,12 @@ __device__ __forceinline__ float group_sum(float x) {
 // split > 1: the CTAs of a cluster of `split` share one query tile, CTA r of
 // the cluster folding the tiles r, r + split, ... of the tile's walk; their
 // states are merged through distributed shared memory at the end.
-template <int DT>  // d <= DT; DT in {64, 128, 256}
-__global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a, int split) {
-  using S = Smem<DT>;
+template <int DT, int BM>  // d <= DT; DT in {64, 128, 256}; BM query rows per CTA (64, 128)
+__global__ void __launch_bounds__(2 * BM) fold_f32_kernel(const FoldArgs a, int split) {
+  constexpr int kBM = BM;
+  constexpr int kThreads = 2 * BM;
+  using S = Smem<DT, BM>;
+  constexpr int kQS = S::kQS;
   constexpr int kCols = DT / 32;  // float4 column groups of o a lane holds
   extern __shared__ __align__(16) float sm[];
   float* qT = sm + S::kQ;
@@ -331,11 +333,11 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a, in
   float* lo = a.mode == kPartial ? a.part.l[g] : a.st_l;
   float* oo = a.mode == kPartial ? a.part.o[g] : a.st_o;
   if (split > 1) {
-    // Each CTA's state of the tile's 64 rows ([row][m, l, o]) into its shared
-    // memory; CTA r then merges rows r 64 / split .. of every CTA's state
+    // Each CTA's state of the tile's kBM rows ([row][m, l, o]) into its shared
+    // memory; CTA r then merges rows r kBM / split .. of every CTA's state
     // (the identity that merges partial states) and writes them.
     constexpr int kRS = DT + 2;
-    static_assert(kBM * kRS <= Smem<DT>::kFloats, "merge rows fit the tiles' space");
+    static_assert(kBM * kRS <= S::kFloats, "merge rows fit the tiles' space");
     __syncthreads();  // every warp is done with the tiles
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
@@ -417,46 +419,65 @@ __global__ void __launch_bounds__(kThreads) fold_f32_kernel(const FoldArgs a, in
   }
 }
 
-// CTAs of the tiled kernel before the split: one per 64-row query tile
-int64_t tiled_units(const FoldArgs& a) {
-  return a.slices * a.P * ((a.nq / a.P + kBM - 1) / kBM);
+// CTAs of the tiled kernel before the split: one per query tile of bm rows
+int64_t tiled_units(const FoldArgs& a, int bm) {
+  return a.slices * a.P * ((a.nq / a.P + bm - 1) / bm);
 }
 
-// Too few CTAs for the SMs (two resident per SM below DT = 256, one at
-// 256): each query tile's walk is split over a cluster of up to 8 CTAs, as
-// long as every CTA keeps at least two K/V tiles.
-int tiled_split(const FoldArgs& a, int dt) {
-  const int64_t resident = static_cast<int64_t>(device_sm_count()) * (dt == 256 ? 1 : 2);
+// CTAs of one tiled kernel resident on an SM, by registers and shared memory
+int tiled_resident(int dt, int bm) {
+  if (bm == 64) return dt == 256 ? 1 : 2;
+  return dt == 64 ? 2 : 1;
+}
+
+// Too few CTAs for the SMs: each query tile's walk is split over a cluster
+// of up to 8 CTAs, as long as every CTA keeps at least two K/V tiles.
+int tiled_split(const FoldArgs& a, int dt, int bm) {
+  const int64_t resident = static_cast<int64_t>(device_sm_count()) * tiled_resident(dt, bm);
   const int64_t tiles_kv = (a.P / a.G) * ((a.nk / a.P + kBN - 1) / kBN);  // per unit, at least
-  const int64_t ctas = tiled_units(a) * a.G;
+  const int64_t ctas = tiled_units(a, bm) * a.G;
   int split = 1;
   while (split < 8 && ctas * split * 2 <= resident && tiles_kv >= 4 * split) split *= 2;
   return split;
 }
 
-template <int DT>
-cudaError_t launch_dt(const FoldArgs& a, cudaStream_t s) {
+// 128-row tiles (8 warps) share the K/V staging between twice the rows:
+// measured 10-14 % faster than 64-row tiles at d = 64 and 128 and 2x at 256
+// on grids that fill the SMs, and faster on small grids too at d = 64, where
+// two of them fit an SM (split over clusters like the 64-row ones).  At
+// d = 128 and 256 one fits an SM, and on small grids 64-row tiles split
+// over clusters measured faster (14.4 against 7.9 TFLOP/s at H = 1,
+// N = 2048, P = 8).
+int tiled_rows(const FoldArgs& a, int dt) {
+  if (a.nq / a.P < 128) return 64;
+  return dt == 64 || tiled_units(a, 128) * a.G >= device_sm_count() ? 128 : 64;
+}
+
+template <int DT, int BM>
+cudaError_t launch_tiled(const FoldArgs& a, cudaStream_t s) {
+  using S = Smem<DT, BM>;
+  constexpr int kThreads = 2 * BM;
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(fold_f32_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Smem<DT>::kBytes);
+    e = cudaFuncSetAttribute(fold_f32_kernel<DT, BM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             S::kBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const int64_t units = tiled_units(a);
-  const int split = tiled_split(a, DT);
+  const int64_t units = tiled_units(a, BM);
+  const int split = tiled_split(a, DT, BM);
   if (split == 1) {
     const dim3 grid(static_cast<unsigned>(units), static_cast<unsigned>(a.G));
-    fold_f32_kernel<DT><<<grid, kThreads, Smem<DT>::kBytes, s>>>(a, 1);
+    fold_f32_kernel<DT, BM><<<grid, kThreads, S::kBytes, s>>>(a, 1);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(units * split), static_cast<unsigned>(a.G));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Smem<DT>::kBytes;
+  cfg.dynamicSmemBytes = S::kBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -465,7 +486,12 @@ cudaError_t launch_dt(const FoldArgs& a, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fold_f32_kernel<DT>, a, split);
+  return cudaLaunchKernelEx(&cfg, fold_f32_kernel<DT, BM>, a, split);
+}
+
+template <int DT>
+cudaError_t launch_dt(const FoldArgs& a, cudaStream_t s) {
+  return tiled_rows(a, DT) == 128 ? launch_tiled<DT, 128>(a, s) : launch_tiled<DT, 64>(a, s);
 }
 
 // ---- small problems: a few warps per query row ----
@@ -709,7 +735,7 @@ cudaError_t launch_dv(const FoldArgs& a, cudaStream_t s) {
 cudaError_t launch_fold_f32(const FoldArgs& a, cudaStream_t s) {
   if (a.slices * a.nq == 0) return cudaSuccess;
   const int dt = a.d <= 64 ? 64 : (a.d <= 128 ? 128 : 256);
-  if (tiled_units(a) * a.G * tiled_split(a, dt) < kSmallGrid) {
+  if (tiled_units(a, 64) * a.G * tiled_split(a, dt, 64) < kSmallGrid) {
     if (a.d <= 32) return launch_dv<1>(a, s);
     if (a.d <= 64) return launch_dv<2>(a, s);
     if (a.d <= 128) return launch_dv<4>(a, s);

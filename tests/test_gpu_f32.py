@@ -75,7 +75,8 @@ def test_workload1_full(O):
 
 
 @pytest.mark.parametrize("shape,P", [((2, 3, 40, 5), 4), ((1, 2, 97, 33), 1), ((1, 1, 64, 256), 8),
-                                     ((1, 1, 7, 1), 7), ((3, 1, 36, 100), 6)])
+                                     ((1, 1, 7, 1), 7), ((3, 1, 36, 100), 6),
+                                     ((1, 16, 300, 33), 3), ((1, 12, 600, 128), 5)])
 def test_ragged_shapes(O, shape, P):
     g = torch.Generator(device=DEV).manual_seed(sum(shape) * 31 + P)
     q, k, v = (torch.randn(shape, device=DEV, generator=g) * 1.5 for _ in range(3))
@@ -83,10 +84,13 @@ def test_ragged_shapes(O, shape, P):
     check_forward(O, q, k, v, P, out, lse)
 
 
-# Shapes large enough for the tiled fp32 kernel (at least 32 CTAs of 64
-# query rows): ragged query tiles and K/V tiles, d in every width class.
-TILED = [((2, 4, 1000, 100), 4), ((1, 8, 512, 256), 2), ((1, 16, 300, 33), 3),
-         ((2, 8, 256, 64), 1), ((1, 12, 600, 128), 5)]
+# Shapes for the tiled fp32 kernel: ragged query tiles and K/V tiles, d in
+# every width class, tiles of 64 and of 128 rows, split over clusters of 2
+# and 4 CTAs or not (the last three: grids that fill the SMs with 128-row
+# tiles at d = 128, 200 and 48).
+TILED = [((2, 4, 1000, 100), 4), ((1, 8, 512, 256), 2), ((1, 16, 600, 33), 3),
+         ((2, 8, 256, 64), 1), ((1, 12, 1024, 128), 4), ((1, 20, 1024, 128), 1),
+         ((1, 40, 512, 200), 1), ((1, 16, 2048, 48), 1)]
 
 
 @pytest.mark.parametrize("shape,P", TILED)
@@ -146,8 +150,8 @@ def test_small_grid_fold_chain(O):
 
 def test_tiled_partials_and_fold_chain(O):
     """Partial states (G = 3) and a chain of ra_fold calls through the tiled
-    kernel (ra_fold of 8 x 256 rows: 32 CTAs), against the oracle's segment
-    states and the forward."""
+    kernel (ra_fold of 8 x 256 rows), against the oracle's segment states
+    and the forward."""
     B, H, N, d, P = 1, 8, 1536, 40, 6
     c = N // P
     g = torch.Generator(device=DEV).manual_seed(72)
