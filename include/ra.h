@@ -30,6 +30,11 @@
  *     returned RA_OK means the work was validated and enqueued.  Kernel
  *     faults surface through the CUDA runtime as usual; a bounded-wait
  *     watchdog inside the kernels is reported by ra_last_device_status().
+ *     The backward calls run their two independent kernels side by side:
+ *     one on `stream`, one on a library-owned stream forked from `stream`
+ *     by an event and joined back into it by another before the call
+ *     returns, so work enqueued on `stream` afterwards sees both (and
+ *     under CUDA-graph capture the pair becomes two branches).
  *   - Arguments are validated before anything is enqueued; on any error the
  *     call returns the status and launches nothing.  No call throws.
  *   - Calls whose total row count is zero return RA_OK and launch nothing;
