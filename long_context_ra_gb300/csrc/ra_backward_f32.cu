@@ -382,9 +382,9 @@ cudaError_t launch_bwd_dv(const BackwardArgs& a, cudaStream_t s) {
 // and accumulates its rows' gradients over its half's streamed rows in
 // columns 4kg + 32m + 0..3; two halves' sums are added in shared memory at
 // the end.  Eight warps on the same shared memory (one CTA an SM at d = 128)
-// measured 30-47 % faster on large grids; four stay faster at d = 64 on
-// grids too small for the SMs.  Tiles used as a product's reduction operand
-// are stored transposed ([d][rows]) for 16-byte reads.
+// measured 30-47 % faster than four, and the launches use eight.  Tiles used
+// as a product's reduction operand are stored transposed ([d][rows]) for
+// 16-byte reads.
 template <int W>
 struct Warps {
   static constexpr int kThreads = 32 * W;
@@ -510,21 +510,110 @@ __device__ __forceinline__ void load_stationary(float* dst, const float* src, in
   }
 }
 
-// Streamed tile of 32 rows (block b, local rows r0 ..): transposed into dT
-// (column e of row x at dT[e * kNS + x]) and, if dR, row-major into dR.
-template <int DT, int NT>
-__device__ __forceinline__ void load_streamed(float* dT, float* dR, const float* src, int layout,
-                                              int b, int64_t r0, int64_t P, int64_t c, int d,
-                                              int tid) {
-  for (int x = tid; x < kTN * DT; x += NT) {
-    const int row = x / DT, e = x % DT;
-    const int64_t r = r0 + row;
-    float val = 0.f;
-    if (r < c && e < d) val = src[layout_pos(layout, b, r, P, c) * d + e];
-    dT[e * kNS + row] = val;
-    if (dR) dR[row * (DT + 4) + e] = val;
+
+// The streamed tiles a tiled CTA visits, in order (this CTA's share: every
+// split-th visible tile).  kDq: the query-stationary walk, key blocks
+// (base - t) mod P, under the mask a block's tiles after the CTA's last query
+// (lim) end it; else the key-stationary walk, query blocks (base + t) mod P,
+// under the mask a tile whose last query precedes the CTA's first key (lim)
+// is skipped.
+template <bool kDq>
+struct StreamWalk {
+  int P, base, layout, split, cr;
+  bool causal;
+  int64_t c, lim;
+  int t = 0, tix = 0;
+  int64_t c0 = 0;
+  __device__ int block() const {
+    if (kDq) {
+      const int j = (base - t) % P;
+      return j < 0 ? j + P : j;
+    }
+    return (base + t) % P;
   }
-}
+  __device__ bool valid() const { return t < P; }
+  // from (t, c0) to the first visible tile
+  __device__ void visible() {
+    while (t < P) {
+      if (c0 >= c) {
+        ++t;
+        c0 = 0;
+        continue;
+      }
+      if (causal) {
+        const int b = block();
+        if (kDq) {
+          if (layout_pos(layout, b, c0, P, c) > lim) {  // rest of the block masked
+            ++t;
+            c0 = 0;
+            continue;
+          }
+        } else {
+          const int64_t qe = (c0 + kTN < c ? c0 + kTN : c) - 1;
+          if (layout_pos(layout, b, qe, P, c) < lim) {
+            c0 += kTN;
+            continue;
+          }
+        }
+      }
+      return;
+    }
+  }
+  // from (t, c0) to the first of this CTA's tiles
+  __device__ void settle() {
+    visible();
+    while (t < P && tix % split != cr) {
+      ++tix;
+      c0 += kTN;
+      visible();
+    }
+  }
+  __device__ void advance() {
+    ++tix;
+    c0 += kTN;
+    settle();
+  }
+};
+
+// One streamed tile (block b, local rows c0 ..) of src, NT threads: the
+// thread's kPre values, fetched into registers while the previous tile is
+// computed and stored to shared memory (transposed into dT and, if dR,
+// row-major into dR) when that one is done.
+template <int DT, int NT>
+struct Streamed {
+  static constexpr int kPre = kTN * DT / NT;
+  float r[kPre];
+  __device__ void fetch(const float* src, int layout, int b, int64_t c0, int64_t P, int64_t c,
+                        int d, int tid) {
+#pragma unroll
+    for (int it = 0; it < kPre; ++it) {
+      const int x = tid + it * NT;
+      const int row = x / DT, e = x % DT;
+      const int64_t rr = c0 + row;
+      r[it] = (rr < c && e < d) ? src[layout_pos(layout, b, rr, P, c) * d + e] : 0.f;
+    }
+  }
+  // without prefetch: each value loaded and stored in turn (fewer registers)
+  __device__ static void load(float* dT, float* dR, const float* src, int layout, int b,
+                              int64_t c0, int64_t P, int64_t c, int d, int tid) {
+    for (int x = tid; x < kTN * DT; x += NT) {
+      const int row = x / DT, e = x % DT;
+      const int64_t rr = c0 + row;
+      const float val = (rr < c && e < d) ? src[layout_pos(layout, b, rr, P, c) * d + e] : 0.f;
+      dT[e * kNS + row] = val;
+      if (dR) dR[row * (DT + 4) + e] = val;
+    }
+  }
+  __device__ void store(float* dT, float* dR, int tid) const {
+#pragma unroll
+    for (int it = 0; it < kPre; ++it) {
+      const int x = tid + it * NT;
+      const int row = x / DT, e = x % DT;
+      dT[e * kNS + row] = r[it];
+      if (dR) dR[row * (DT + 4) + e] = r[it];
+    }
+  }
+};
 
 // Sums of a split tile (split > 1: the CTAs of a cluster share one tile of
 // 64 stationary rows, CTA r taking the streamed tiles r, r + split, ... of
@@ -581,7 +670,8 @@ __device__ __forceinline__ void split_sums(float* sm, int split, int cr, int tid
 
 // dQ for 64 query rows of block i: the key blocks in ring order (i - t) mod P.
 template <int DT, int W>
-__global__ void __launch_bounds__(32 * W) dq_f32_tiled(const BackwardArgs a, int split) {
+__global__ void __launch_bounds__(32 * W, DT == 64 && W == 8 ? 2 : 1)
+    dq_f32_tiled(const BackwardArgs a, int split) {
   using S = DqSmem<DT>;
   using WW = Warps<W>;
   constexpr int kTT = WW::kThreads;
@@ -633,17 +723,35 @@ __global__ void __launch_bounds__(32 * W) dq_f32_tiled(const BackwardArgs a, int
   const int64_t rlast = (r0 + kTM < c ? r0 + kTM : c) - 1;
   const int64_t qlast = layout_pos(a.layout, i, rlast, a.P, c);
 
-  int tix = 0;  // visible streamed tiles so far; this CTA takes every split-th
-  for (int t = 0; t < a.P; ++t) {
-    int j = (i - t) % a.P;
-    if (j < 0) j += a.P;
-    for (int64_t c0 = 0; c0 < c; c0 += kTN) {
-      if (a.causal && layout_pos(a.layout, j, c0, a.P, c) > qlast) break;  // rest of block masked
-      if (tix++ % split != cr) continue;
+  // K/V tiles in ring order; with eight warps the next one is fetched into
+  // registers while the current one is computed (with four that measured
+  // slower: the registers cost the second CTA on an SM)
+  constexpr bool kPrefetch = W == 8;
+  StreamWalk<true> w{a.P, i, a.layout, split, cr, a.causal != 0, c, qlast};
+  w.settle();
+  Streamed<DT, kTT> nk, nv;
+  if (kPrefetch && w.valid()) {
+    nk.fetch(k, a.layout, w.block(), w.c0, a.P, c, d, tid);
+    nv.fetch(v, a.layout, w.block(), w.c0, a.P, c, d, tid);
+  }
+  while (w.valid()) {
+    {
+      const int j = w.block();
+      const int64_t c0 = w.c0;
+      __syncthreads();  // the previous tile's K, V and dS are no longer read
+      if (kPrefetch) {
+        nk.store(sm + S::kK, sm + S::kKr, tid);
+        nv.store(sm + S::kV, nullptr, tid);
+      } else {
+        Streamed<DT, kTT>::load(sm + S::kK, sm + S::kKr, k, a.layout, j, c0, a.P, c, d, tid);
+        Streamed<DT, kTT>::load(sm + S::kV, nullptr, v, a.layout, j, c0, a.P, c, d, tid);
+      }
       __syncthreads();
-      load_streamed<DT, kTT>(sm + S::kK, sm + S::kKr, k, a.layout, j, c0, a.P, c, d, tid);
-      load_streamed<DT, kTT>(sm + S::kV, nullptr, v, a.layout, j, c0, a.P, c, d, tid);
-      __syncthreads();
+      w.advance();
+      if (kPrefetch && w.valid()) {
+        nk.fetch(k, a.layout, w.block(), w.c0, a.P, c, d, tid);
+        nv.fetch(v, a.layout, w.block(), w.c0, a.P, c, d, tid);
+      }
       float s[4][kNY], dp[4][kNY];
       two_blocks(sm + S::kQ, sm + S::kK, sm + S::kG, sm + S::kV, d, kSS, kNS, lrow0, ccol, s, dp);
       float ds[4][kNY];
@@ -704,7 +812,8 @@ __global__ void __launch_bounds__(32 * W) dq_f32_tiled(const BackwardArgs a, int
 
 // dK, dV for 64 key rows of block j: the query blocks (j + t) mod P.
 template <int DT, int W>
-__global__ void __launch_bounds__(32 * W) dkv_f32_tiled(const BackwardArgs a, int split) {
+__global__ void __launch_bounds__(32 * W, DT == 64 && W == 8 ? 2 : 1)
+    dkv_f32_tiled(const BackwardArgs a, int split) {
   using S = DkvSmem<DT>;
   using WW = Warps<W>;
   constexpr int kTT = WW::kThreads;
@@ -752,20 +861,36 @@ __global__ void __launch_bounds__(32 * W) dkv_f32_tiled(const BackwardArgs a, in
   }
   const int64_t kfirst = layout_pos(a.layout, j, r0, a.P, c);  // the CTA's first key position
 
-  int tix = 0;  // visible streamed tiles so far; this CTA takes every split-th
-  for (int t = 0; t < a.P; ++t) {
-    const int i = (j + t) % a.P;  // the query block this key block meets at step t
-    for (int64_t c0 = 0; c0 < c; c0 += kTN) {
-      // causal: a query tile whose last query precedes every key here sees none
-      if (a.causal) {
-        const int64_t qe = (c0 + kTN < c ? c0 + kTN : c) - 1;
-        if (layout_pos(a.layout, i, qe, a.P, c) < kfirst) continue;
+  // the query blocks (j + t) mod P this key block meets, tile by tile (under
+  // the mask a query tile whose last query precedes every key here sees
+  // none); with eight warps the next Q/dO tile is fetched into registers
+  // during the current one
+  constexpr bool kPrefetch = W == 8;
+  StreamWalk<false> w{a.P, j, a.layout, split, cr, a.causal != 0, c, kfirst};
+  w.settle();
+  Streamed<DT, kTT> nq, ng;
+  if (kPrefetch && w.valid()) {
+    nq.fetch(q, a.layout, w.block(), w.c0, a.P, c, d, tid);
+    ng.fetch(g, a.layout, w.block(), w.c0, a.P, c, d, tid);
+  }
+  while (w.valid()) {
+    {
+      const int i = w.block();  // the query block this key block meets
+      const int64_t c0 = w.c0;
+      __syncthreads();  // the previous tile's Q, dO, P and dS are no longer read
+      if (kPrefetch) {
+        nq.store(sm + S::kQ, sm + S::kQr, tid);
+        ng.store(sm + S::kG, sm + S::kGr, tid);
+      } else {
+        Streamed<DT, kTT>::load(sm + S::kQ, sm + S::kQr, q, a.layout, i, c0, a.P, c, d, tid);
+        Streamed<DT, kTT>::load(sm + S::kG, sm + S::kGr, g, a.layout, i, c0, a.P, c, d, tid);
       }
-      if (tix++ % split != cr) continue;
       __syncthreads();
-      load_streamed<DT, kTT>(sm + S::kQ, sm + S::kQr, q, a.layout, i, c0, a.P, c, d, tid);
-      load_streamed<DT, kTT>(sm + S::kG, sm + S::kGr, g, a.layout, i, c0, a.P, c, d, tid);
-      __syncthreads();
+      w.advance();
+      if (kPrefetch && w.valid()) {
+        nq.fetch(q, a.layout, w.block(), w.c0, a.P, c, d, tid);
+        ng.fetch(g, a.layout, w.block(), w.c0, a.P, c, d, tid);
+      }
       float s[4][kNY], dp[4][kNY];
       two_blocks(sm + S::kK, sm + S::kQ, sm + S::kV, sm + S::kG, d, kSS, kNS, lrow0, ccol, s, dp);
       float p[4][kNY], ds[4][kNY];
@@ -899,15 +1024,12 @@ cudaError_t launch_tiled_w(const BackwardArgs& a, cudaStream_t s) {
   return fj.join(s);
 }
 
-// Eight warps a CTA, except at d <= 64 on grids of fewer 64-row tiles than
-// SMs, where four measured faster (9.4 against 7.5 TFLOP/s at H = 4,
-// N = 1024).
+// Eight warps a CTA, with the next streamed tile prefetched (measured 14.7
+// against 7.0 TFLOP/s for four warps without prefetch at d = 128, 17.3
+// against 11.1 at d = 64; on one small d = 64 grid, H = 4, N = 1024, 8.4
+// against 9.3).
 template <int DT>
 cudaError_t launch_tiled(const BackwardArgs& a, cudaStream_t s) {
-  const int64_t ctas = a.slices * a.P * ((a.N / a.P + kTM - 1) / kTM);
-  if constexpr (DT == 64) {
-    if (ctas < device_sm_count()) return launch_tiled_w<DT, 4>(a, s);
-  }
   return launch_tiled_w<DT, 8>(a, s);
 }
 }  // namespace
