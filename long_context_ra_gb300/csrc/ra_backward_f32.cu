@@ -593,17 +593,6 @@ struct Streamed {
       r[it] = (rr < c && e < d) ? src[layout_pos(layout, b, rr, P, c) * d + e] : 0.f;
     }
   }
-  // without prefetch: each value loaded and stored in turn (fewer registers)
-  __device__ static void load(float* dT, float* dR, const float* src, int layout, int b,
-                              int64_t c0, int64_t P, int64_t c, int d, int tid) {
-    for (int x = tid; x < kTN * DT; x += NT) {
-      const int row = x / DT, e = x % DT;
-      const int64_t rr = c0 + row;
-      const float val = (rr < c && e < d) ? src[layout_pos(layout, b, rr, P, c) * d + e] : 0.f;
-      dT[e * kNS + row] = val;
-      if (dR) dR[row * (DT + 4) + e] = val;
-    }
-  }
   __device__ void store(float* dT, float* dR, int tid) const {
 #pragma unroll
     for (int it = 0; it < kPre; ++it) {
@@ -723,14 +712,12 @@ __global__ void __launch_bounds__(32 * W, DT == 64 && W == 8 ? 2 : 1)
   const int64_t rlast = (r0 + kTM < c ? r0 + kTM : c) - 1;
   const int64_t qlast = layout_pos(a.layout, i, rlast, a.P, c);
 
-  // K/V tiles in ring order; with eight warps the next one is fetched into
-  // registers while the current one is computed (with four that measured
-  // slower: the registers cost the second CTA on an SM)
-  constexpr bool kPrefetch = W == 8;
+  // K/V tiles in ring order, the next one fetched into registers while the
+  // current one is computed
   StreamWalk<true> w{a.P, i, a.layout, split, cr, a.causal != 0, c, qlast};
   w.settle();
   Streamed<DT, kTT> nk, nv;
-  if (kPrefetch && w.valid()) {
+  if (w.valid()) {
     nk.fetch(k, a.layout, w.block(), w.c0, a.P, c, d, tid);
     nv.fetch(v, a.layout, w.block(), w.c0, a.P, c, d, tid);
   }
@@ -739,16 +726,11 @@ __global__ void __launch_bounds__(32 * W, DT == 64 && W == 8 ? 2 : 1)
       const int j = w.block();
       const int64_t c0 = w.c0;
       __syncthreads();  // the previous tile's K, V and dS are no longer read
-      if (kPrefetch) {
-        nk.store(sm + S::kK, sm + S::kKr, tid);
-        nv.store(sm + S::kV, nullptr, tid);
-      } else {
-        Streamed<DT, kTT>::load(sm + S::kK, sm + S::kKr, k, a.layout, j, c0, a.P, c, d, tid);
-        Streamed<DT, kTT>::load(sm + S::kV, nullptr, v, a.layout, j, c0, a.P, c, d, tid);
-      }
+      nk.store(sm + S::kK, sm + S::kKr, tid);
+      nv.store(sm + S::kV, nullptr, tid);
       __syncthreads();
       w.advance();
-      if (kPrefetch && w.valid()) {
+      if (w.valid()) {
         nk.fetch(k, a.layout, w.block(), w.c0, a.P, c, d, tid);
         nv.fetch(v, a.layout, w.block(), w.c0, a.P, c, d, tid);
       }
@@ -863,13 +845,11 @@ __global__ void __launch_bounds__(32 * W, DT == 64 && W == 8 ? 2 : 1)
 
   // the query blocks (j + t) mod P this key block meets, tile by tile (under
   // the mask a query tile whose last query precedes every key here sees
-  // none); with eight warps the next Q/dO tile is fetched into registers
-  // during the current one
-  constexpr bool kPrefetch = W == 8;
+  // none); the next Q/dO tile fetched into registers during the current one
   StreamWalk<false> w{a.P, j, a.layout, split, cr, a.causal != 0, c, kfirst};
   w.settle();
   Streamed<DT, kTT> nq, ng;
-  if (kPrefetch && w.valid()) {
+  if (w.valid()) {
     nq.fetch(q, a.layout, w.block(), w.c0, a.P, c, d, tid);
     ng.fetch(g, a.layout, w.block(), w.c0, a.P, c, d, tid);
   }
@@ -878,16 +858,11 @@ __global__ void __launch_bounds__(32 * W, DT == 64 && W == 8 ? 2 : 1)
       const int i = w.block();  // the query block this key block meets
       const int64_t c0 = w.c0;
       __syncthreads();  // the previous tile's Q, dO, P and dS are no longer read
-      if (kPrefetch) {
-        nq.store(sm + S::kQ, sm + S::kQr, tid);
-        ng.store(sm + S::kG, sm + S::kGr, tid);
-      } else {
-        Streamed<DT, kTT>::load(sm + S::kQ, sm + S::kQr, q, a.layout, i, c0, a.P, c, d, tid);
-        Streamed<DT, kTT>::load(sm + S::kG, sm + S::kGr, g, a.layout, i, c0, a.P, c, d, tid);
-      }
+      nq.store(sm + S::kQ, sm + S::kQr, tid);
+      ng.store(sm + S::kG, sm + S::kGr, tid);
       __syncthreads();
       w.advance();
-      if (kPrefetch && w.valid()) {
+      if (w.valid()) {
         nq.fetch(q, a.layout, w.block(), w.c0, a.P, c, d, tid);
         ng.fetch(g, a.layout, w.block(), w.c0, a.P, c, d, tid);
       }
